@@ -1,0 +1,684 @@
+// Host side of the C ABI declared in include/moestep.h: argument validation, workspace
+// layout, launch configuration and the programmatic-dependent-launch chain.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "internal.h"
+
+namespace moe {
+__global__ void k_router(RouterParams p);
+__global__ void k_topk_route(TopkRouteParams p);
+__global__ void k_finalize(FinalizeParams p);
+__global__ void k_pack(PackParams p);
+__global__ void k_expert_gemm(const __grid_constant__ GemmParams p);
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+thread_local std::string g_err;
+
+moe_status fail(moe_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return st;
+}
+
+moe_status ok() {
+    g_err.clear();
+    return MOE_OK;
+}
+
+moe_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define REQUIRE(cond, ...)                                            \
+    do {                                                              \
+        if (!(cond)) return fail(MOE_ERR_INVALID_ARG, __VA_ARGS__);   \
+    } while (0)
+#define REQUIRE_PTR(p, name)                                                         \
+    do {                                                                             \
+        if (!(p)) return fail(MOE_ERR_INVALID_ARG, "%s is NULL", name);              \
+        if (!aligned16(p)) return fail(MOE_ERR_INVALID_ARG, "%s is not 16-byte aligned", name); \
+    } while (0)
+#define OPT_PTR(p, name)                                                             \
+    do {                                                                             \
+        if ((p) && !aligned16(p)) return fail(MOE_ERR_INVALID_ARG, "%s is not 16-byte aligned", name); \
+    } while (0)
+
+moe_status check_desc(const moe_layer_desc* d) {
+    if (!d) return fail(MOE_ERR_INVALID_ARG, "layer descriptor is NULL");
+    REQUIRE(d->H >= 1024 && d->H <= 8192 && d->H % 256 == 0, "H=%d: need 1024 <= H <= 8192, H %% 256 == 0", d->H);
+    REQUIRE(d->E >= 1 && d->E <= kMaxE, "E=%d: need 1 <= E <= %d", d->E, kMaxE);
+    REQUIRE(d->k >= 1 && d->k <= kMaxK && d->k <= d->E, "k=%d: need 1 <= k <= min(16, E)", d->k);
+    REQUIRE(d->I >= 256 && d->I <= 4096 && d->I % 256 == 0, "I=%d: need 256 <= I <= 4096, I %% 256 == 0", d->I);
+    if (d->w_fmt != MOE_FMT_MXFP8 && d->w_fmt != MOE_FMT_NVFP4)
+        return fail(MOE_ERR_UNSUPPORTED, "routed weight format %d has no kernel (MXFP8=1, NVFP4=2)", d->w_fmt);
+    if (d->has_shared) {
+        REQUIRE(d->I_shared >= 256 && d->I_shared <= 4096 && d->I_shared % 256 == 0,
+                "I_shared=%d: need 256 <= I_shared <= 4096, %% 256 == 0", d->I_shared);
+        if (d->shared_fmt != MOE_FMT_BF16 && d->shared_fmt != MOE_FMT_MXFP8 && d->shared_fmt != MOE_FMT_NVFP4)
+            return fail(MOE_ERR_UNSUPPORTED, "shared weight format %d has no kernel", d->shared_fmt);
+    }
+    REQUIRE(d->routed_scaling_factor == d->routed_scaling_factor, "routed_scaling_factor is NaN");
+    REQUIRE(d->rms_eps >= 0.0f, "rms_eps must be >= 0");
+    if (d->w_fmt == MOE_FMT_NVFP4) REQUIRE(d->gs_a1 > 0.0f && d->gs_a2 > 0.0f, "NVFP4 needs gs_a1, gs_a2 > 0");
+    if (d->has_shared && d->shared_fmt == MOE_FMT_NVFP4)
+        REQUIRE(d->gs_a1_shared > 0.0f && d->gs_a2_shared > 0.0f, "NVFP4 shared needs gs_a1_shared, gs_a2_shared > 0");
+    return MOE_OK;
+}
+
+int shared_fmt_of(const moe_layer_desc* d) { return d->has_shared ? d->shared_fmt : d->w_fmt; }
+bool separate_shared_input(const moe_layer_desc* d) { return d->has_shared && d->shared_fmt != d->w_fmt; }
+
+size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t act_bytes(int fmt, int rows, int K) { return (size_t)round_up(rows, 16) * row_bytes(fmt, K); }
+size_t act_scale_bytes(int fmt, int K) { return (size_t)steps_of(fmt, K) * atoms_per_step(fmt) * kAtomBytes; }
+
+// Routed part of the hidden buffers for up to `rows` rows; the shared block follows it.
+size_t hq_routed(const moe_layer_desc* d, int rows) {
+    const int P = rows * d->k, G = P < d->E ? P : d->E;
+    return al256((size_t)(P + 15 * G) * row_bytes(d->w_fmt, d->I));
+}
+size_t hs_routed(const moe_layer_desc* d, int rows) {
+    const int P = rows * d->k, G = P < d->E ? P : d->E;
+    return al256((size_t)G * act_scale_bytes(d->w_fmt, d->I));
+}
+size_t hq_total(const moe_layer_desc* d, int rows) {
+    return hq_routed(d, rows) + (d->has_shared ? al256(act_bytes(d->shared_fmt, rows, d->I_shared)) : 0);
+}
+size_t hs_total(const moe_layer_desc* d, int rows) {
+    return hs_routed(d, rows) + (d->has_shared ? al256(act_scale_bytes(d->shared_fmt, d->I_shared)) + 256 : 256);
+}
+
+WsLayout layout(const moe_layer_desc* d) {
+    const int max_rows = kMaxRows;
+    WsLayout L{};
+    L.max_rows = max_rows;
+    L.P_max = max_rows * d->k + max_rows;
+    L.G_max = (max_rows * d->k < d->E) ? max_rows * d->k : d->E;
+    L.T_max = L.P_max + d->E + 1;
+    const int Ish = d->has_shared ? d->I_shared : 256;
+    L.U_gu = L.G_max * (2 * d->I / kBlockRows) + 2 * Ish / kBlockRows;
+    L.U_dn = L.G_max * (d->H / kBlockRows) + d->H / kBlockRows;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        size_t r = o;
+        o = al256(o + bytes);
+        return r;
+    };
+    L.header = take(256);
+    L.groups = take(sizeof(Group) * (size_t)L.G_max);
+    L.logits = take(4ull * max_rows * d->E);
+    L.scores = take(4ull * max_rows * d->E);
+    L.topk_idx = take(4ull * max_rows * d->k);
+    L.topk_w = take(4ull * max_rows * d->k);
+    L.counts = take(4ull * (d->E + 1));
+    L.perm = take(4ull * L.P_max);
+    L.inv_perm = take(4ull * L.P_max);
+    L.tiles = take(12ull * L.T_max);
+    L.num_tiles = take(4);
+    L.xq = take(act_bytes(d->w_fmt, max_rows, d->H));
+    L.xs = take(act_scale_bytes(d->w_fmt, d->H) + 256);
+    if (separate_shared_input(d)) {
+        L.xq_sh = take(act_bytes(d->shared_fmt, max_rows, d->H));
+        L.xs_sh = take(act_scale_bytes(d->shared_fmt, d->H) + 256);
+    } else {
+        L.xq_sh = L.xq;
+        L.xs_sh = L.xs;
+    }
+    L.hq_routed_bytes = hq_routed(d, max_rows);
+    L.hs_routed_bytes = hs_routed(d, max_rows);
+    L.hq = take(hq_total(d, max_rows));
+    L.hs = take(hs_total(d, max_rows));
+    L.y = take(4ull * L.P_max * d->H);
+    L.cnt_gu = take(4ull * L.U_gu);
+    L.cnt_dn = take(4ull * L.U_dn);
+    L.partials = take(4ull * kMaxGemmCtas * 2 * kPartialFloats);
+    L.total = o;
+    return L;
+}
+
+struct DevInfo {
+    int dev = -1, sms = 0, smem_optin = 0;
+    bool gemm_attr_set = false;
+};
+thread_local DevInfo g_dev;
+
+moe_status dev_info(DevInfo** out) {
+    int dev;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (g_dev.dev != dev) {
+        g_dev = DevInfo{};
+        g_dev.dev = dev;
+        e = cudaDeviceGetAttribute(&g_dev.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+        e = cudaDeviceGetAttribute(&g_dev.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(smem)");
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (major != 10 || minor != 3) {
+            g_dev.dev = -1;
+            return fail(MOE_ERR_UNSUPPORTED, "device %d is sm_%d%d; the kernels are built for sm_103a", dev, major,
+                        minor);
+        }
+    }
+    *out = &g_dev;
+    return MOE_OK;
+}
+
+// Launch with programmatic stream serialisation (the kernel may start before its
+// predecessor on the stream finishes; it waits in griddepcontrol.wait).
+template <typename Kern, typename Arg>
+moe_status launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st, const Arg& arg,
+                      const char* name) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, arg);
+    if (e != cudaSuccess) return cuda_fail(e, name);
+    return MOE_OK;
+}
+
+// ------------------------------------------------------------------ launch helpers
+moe_status launch_router(const moe_layer_desc* d, const void* x, const void* w_gate, const float* logits_in, int M,
+                         float* logits_out, float* scores, void* xq, void* xs, void* xq_sh, void* xs_sh,
+                         cudaStream_t st) {
+    RouterParams p{};
+    p.x = static_cast<const uint16_t*>(x);
+    p.wg = static_cast<const uint16_t*>(w_gate);
+    p.logits_in = logits_in;
+    p.logits_out = logits_out;
+    p.scores = scores;
+    p.M = M;
+    p.H = d->H;
+    p.E = d->E;
+    int epc = d->E / 128;
+    epc = epc >= 8 ? 8 : (epc >= 4 ? 4 : (epc >= 2 ? 2 : 1));
+    p.experts_per_cta = epc;
+    p.fmt_r = d->w_fmt;
+    p.fmt_s = shared_fmt_of(d);
+    p.quant_shared = separate_shared_input(d) ? 1 : 0;
+    p.xq = static_cast<uint8_t*>(xq);
+    p.xs = static_cast<uint8_t*>(xs);
+    p.xq_sh = static_cast<uint8_t*>(xq_sh);
+    p.xs_sh = static_cast<uint8_t*>(xs_sh);
+    p.gs_r = d->w_fmt == MOE_FMT_NVFP4 ? d->gs_a1 : 1.0f;
+    p.gs_s = (d->has_shared && d->shared_fmt == MOE_FMT_NVFP4) ? d->gs_a1_shared : 1.0f;
+    const int grid = (d->E + epc - 1) / epc;
+    return launch_pdl(k_router, dim3(grid), dim3(256), 0, st, p, "k_router launch");
+}
+
+moe_status launch_topk_route(const moe_layer_desc* d, const WsLayout& L, uint8_t* ws, int M, const float* scores,
+                             const float* bias, int32_t* topk_idx, float* topk_w, int do_topk, int do_route,
+                             int32_t* counts, int32_t* perm, int32_t* inv_perm, int32_t* tiles, int32_t* num_tiles,
+                             cudaStream_t st) {
+    TopkRouteParams p{};
+    p.scores = scores;
+    p.bias = d->has_bias ? bias : nullptr;
+    p.topk_idx = topk_idx;
+    p.topk_w = topk_w;
+    p.M = M;
+    p.E = d->E;
+    p.k = d->k;
+    p.renormalize = d->renormalize;
+    p.has_shared = d->has_shared;
+    p.do_topk = do_topk;
+    p.do_route = do_route;
+    p.rsf = d->routed_scaling_factor;
+    p.counts = counts;
+    p.perm = perm;
+    p.inv_perm = inv_perm;
+    p.tiles = tiles;
+    p.num_tiles = num_tiles;
+    p.groups = reinterpret_cast<Group*>(ws + L.groups);
+    p.hdr = reinterpret_cast<WsHeader*>(ws + L.header);
+    return launch_pdl(k_topk_route, dim3(1), dim3(1024), 0, st, p, "k_topk_route launch");
+}
+
+struct GemmBuffers {
+    const void *xq, *xs, *xq_sh, *xs_sh;  // gate_up inputs
+    void *hq, *hs;                         // gate_up outputs / down inputs
+    float* y;
+    const int32_t* perm;
+};
+
+moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* wr, const moe_qweight* ws_,
+                       const GemmBuffers& b, int M, const WsLayout& L, uint8_t* ws, cudaStream_t st) {
+    DevInfo* di;
+    moe_status s = dev_info(&di);
+    if (s != MOE_OK) return s;
+    GemmParams p{};
+    p.mode = mode;
+    p.M = M;
+    p.k = d->k;
+    p.E = d->E;
+    p.H = d->H;
+    p.Mpad = round_up(M, 16);
+    p.has_shared = d->has_shared;
+    p.perm = b.perm;
+    p.groups = reinterpret_cast<const Group*>(ws + L.groups);
+    p.hdr = reinterpret_cast<const WsHeader*>(ws + L.header);
+    p.y = b.y;
+    p.counters = reinterpret_cast<int32_t*>(ws + (mode == 0 ? L.cnt_gu : L.cnt_dn));
+    p.partials = reinterpret_cast<float*>(ws + L.partials);
+    p.status = reinterpret_cast<int32_t*>(ws + L.header);
+    const size_t hqr = hq_routed(d, M), hsr = hs_routed(d, M);
+    for (int c = 0; c < 2; ++c) {
+        GemmClass& C = p.cls[c];
+        const bool sh = c == 1;
+        if (sh && !d->has_shared) {
+            C.fmt = d->w_fmt;
+            C.MB = 1;
+            C.KS = 1;
+            continue;
+        }
+        const moe_qweight* w = sh ? ws_ : wr;
+        C.fmt = sh ? d->shared_fmt : d->w_fmt;
+        C.w = static_cast<const uint8_t*>(w->packed);
+        C.gs_w = C.fmt == MOE_FMT_NVFP4 ? w->global_scale : nullptr;
+        const int I = sh ? d->I_shared : d->I;
+        C.I = I;
+        C.out_fmt = C.fmt;
+        const float gs1 = sh ? d->gs_a1_shared : d->gs_a1, gs2 = sh ? d->gs_a2_shared : d->gs_a2;
+        if (mode == 0) {
+            C.MB = 2 * I / kBlockRows;
+            C.KS = steps_of(C.fmt, d->H);
+            C.b = static_cast<const uint8_t*>(sh ? b.xq_sh : b.xq);
+            C.bs = static_cast<const uint8_t*>(sh ? b.xs_sh : b.xs);
+            C.gs_a = C.fmt == MOE_FMT_NVFP4 ? gs1 : 1.0f;
+            C.gs_out = C.fmt == MOE_FMT_NVFP4 ? gs2 : 1.0f;
+            C.hq = static_cast<uint8_t*>(b.hq) + (sh ? hqr : 0);
+            C.hs = static_cast<uint8_t*>(b.hs) + (sh ? hsr : 0);
+        } else {
+            C.MB = d->H / kBlockRows;
+            C.KS = steps_of(C.fmt, I);
+            C.b = static_cast<const uint8_t*>(b.hq) + (sh ? hqr : 0);
+            C.bs = static_cast<const uint8_t*>(b.hs) + (sh ? hsr : 0);
+            C.gs_a = C.fmt == MOE_FMT_NVFP4 ? gs2 : 1.0f;
+            C.gs_out = 1.0f;
+        }
+    }
+    const int am = atoms_per_step(p.cls[0].fmt) > atoms_per_step(p.cls[1].fmt) ? atoms_per_step(p.cls[0].fmt)
+                                                                                : atoms_per_step(p.cls[1].fmt);
+    p.atoms_max = am;
+    p.a_off = 0;
+    p.sfa_off = kBlockRows * kStepBytes;
+    p.b_off = round_up(p.sfa_off + am * kAtomBytes, 1024);
+    p.sfb_off = p.b_off + p.Mpad * kStepBytes;
+    p.stage_bytes = round_up(p.sfb_off + am * kAtomBytes, 1024);
+    const int fixed = 1024 + p.Mpad * kBlockRows * 4 + 256;
+    int S = (di->smem_optin - fixed) / (p.stage_bytes + 16);
+    const int tmem_cap = am ? (512 - 2 * 64) / (8 * am) : 16;
+    if (S > tmem_cap) S = tmem_cap;
+    if (S > 16) S = 16;
+    if (S < 2) return fail(MOE_ERR_UNSUPPORTED, "not enough shared memory for the GEMM pipeline");
+    p.stages = S;
+    const size_t smem = (size_t)fixed + (size_t)S * p.stage_bytes + 16 * S;
+    if (!di->gemm_attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(k_expert_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             di->smem_optin);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(k_expert_gemm)");
+        di->gemm_attr_set = true;
+    }
+    int grid = di->sms;
+    if (grid > kMaxGemmCtas) grid = kMaxGemmCtas;
+    return launch_pdl(k_expert_gemm, dim3(grid), dim3(192), smem, st, p,
+                      mode == 0 ? "k_expert_gemm(gate_up) launch" : "k_expert_gemm(down) launch");
+}
+
+moe_status launch_finalize(const moe_layer_desc* d, const float* y, const float* topk_w, const int32_t* inv_perm,
+                           int M, void* residual, const void* gamma, void* out, void* outq, void* outs,
+                           cudaStream_t st) {
+    FinalizeParams p{};
+    p.y = y;
+    p.topk_w = topk_w;
+    p.inv_perm = inv_perm;
+    p.residual = static_cast<uint16_t*>(residual);
+    p.gamma = static_cast<const uint16_t*>(gamma);
+    p.out = static_cast<uint16_t*>(out);
+    p.outq = static_cast<uint8_t*>(outq);
+    p.outs = static_cast<uint8_t*>(outs);
+    p.M = M;
+    p.H = d->H;
+    p.k = d->k;
+    p.has_shared = d->has_shared;
+    p.eps = d->rms_eps;
+    const int grid = outq ? round_up(M, 8) : M;
+    return launch_pdl(k_finalize, dim3(grid), dim3(256), 0, st, p, "k_finalize launch");
+}
+
+moe_status check_qweight(const moe_qweight* w, int fmt, const char* name) {
+    if (!w) return fail(MOE_ERR_INVALID_ARG, "%s is NULL", name);
+    if (!w->packed || !aligned16(w->packed)) return fail(MOE_ERR_INVALID_ARG, "%s.packed is NULL or unaligned", name);
+    if (fmt == MOE_FMT_NVFP4 && !w->global_scale)
+        return fail(MOE_ERR_INVALID_ARG, "%s.global_scale is required for NVFP4", name);
+    return MOE_OK;
+}
+
+}  // namespace
+
+// ================================================================== C ABI
+extern "C" {
+
+const char* moe_last_error_string(void) { return g_err.c_str(); }
+
+size_t moe_packed_bytes(const moe_layer_desc* d, int which) {
+    if (check_desc(d) != MOE_OK) return 0;
+    int fmt, rows, K, n;
+    switch (which) {
+        case MOE_W13: fmt = d->w_fmt; rows = 2 * d->I; K = d->H; n = d->E; break;
+        case MOE_W2: fmt = d->w_fmt; rows = d->H; K = d->I; n = d->E; break;
+        case MOE_SH13: if (!d->has_shared) return 0; fmt = d->shared_fmt; rows = 2 * d->I_shared; K = d->H; n = 1; break;
+        case MOE_SH2: if (!d->has_shared) return 0; fmt = d->shared_fmt; rows = d->H; K = d->I_shared; n = 1; break;
+        default: return 0;
+    }
+    return (size_t)n * (rows / kBlockRows) * steps_of(fmt, K) * record_bytes(fmt);
+}
+
+size_t moe_act_bytes(int fmt, int rows, int K) {
+    if (fmt < 0 || fmt > 2 || rows < 1 || rows > kMaxRows || K <= 0 || row_bytes(fmt, K) % kStepBytes) return 0;
+    return act_bytes(fmt, rows, K);
+}
+size_t moe_act_scale_bytes(int fmt, int rows, int K) {
+    if (fmt < 0 || fmt > 2 || rows < 1 || rows > kMaxRows || K <= 0 || row_bytes(fmt, K) % kStepBytes) return 0;
+    return act_scale_bytes(fmt, K);
+}
+size_t moe_hq_bytes(const moe_layer_desc* d, int max_rows) {
+    if (check_desc(d) != MOE_OK || max_rows < 1 || max_rows > kMaxRows) return 0;
+    return hq_total(d, max_rows);
+}
+size_t moe_hq_scale_bytes(const moe_layer_desc* d, int max_rows) {
+    if (check_desc(d) != MOE_OK || max_rows < 1 || max_rows > kMaxRows) return 0;
+    return hs_total(d, max_rows);
+}
+size_t moe_workspace_bytes(const moe_layer_desc* d) {
+    if (check_desc(d) != MOE_OK) return 0;
+    return layout(d).total;
+}
+
+moe_status moe_workspace_init(const moe_layer_desc* d, void* ws, moe_stream_t stream) {
+    moe_status s = check_desc(d);
+    if (s != MOE_OK) return s;
+    REQUIRE_PTR(ws, "ws");
+    const WsLayout L = layout(d);
+    cudaError_t e = cudaMemsetAsync(ws, 0, L.total, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(ws)");
+    return ok();
+}
+
+moe_status moe_ws_view(const moe_layer_desc* d, void* ws, moe_ws_ptrs* out) {
+    moe_status s = check_desc(d);
+    if (s != MOE_OK) return s;
+    REQUIRE_PTR(ws, "ws");
+    REQUIRE(out != nullptr, "out is NULL");
+    const WsLayout L = layout(d);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    out->status = reinterpret_cast<int32_t*>(w + L.header);
+    out->logits = reinterpret_cast<float*>(w + L.logits);
+    out->scores = reinterpret_cast<float*>(w + L.scores);
+    out->topk_idx = reinterpret_cast<int32_t*>(w + L.topk_idx);
+    out->topk_w = reinterpret_cast<float*>(w + L.topk_w);
+    out->expert_counts = reinterpret_cast<int32_t*>(w + L.counts);
+    out->perm = reinterpret_cast<int32_t*>(w + L.perm);
+    out->inv_perm = reinterpret_cast<int32_t*>(w + L.inv_perm);
+    out->tiles = reinterpret_cast<int32_t*>(w + L.tiles);
+    out->num_tiles = reinterpret_cast<int32_t*>(w + L.num_tiles);
+    out->xq = w + L.xq;
+    out->xq_scales = w + L.xs;
+    out->xq_shared = w + L.xq_sh;
+    out->xq_shared_scales = w + L.xs_sh;
+    out->hq = w + L.hq;
+    out->hq_scales = w + L.hs;
+    out->y_pairs = reinterpret_cast<float*>(w + L.y);
+    return ok();
+}
+
+moe_status moe_pack_weights(const moe_layer_desc* d, int which, const void* codes, const void* scales, void* dst,
+                            moe_stream_t stream) {
+    moe_status s = check_desc(d);
+    if (s != MOE_OK) return s;
+    REQUIRE(which >= 0 && which <= 3, "which=%d: need 0..3", which);
+    REQUIRE(d->has_shared || which < 2, "shared projection requested but has_shared == 0");
+    PackParams p{};
+    const bool sh = which >= 2;
+    p.fmt = sh ? d->shared_fmt : d->w_fmt;
+    p.n_exp = sh ? 1 : d->E;
+    const int I = sh ? d->I_shared : d->I;
+    p.gate_up = (which == MOE_W13 || which == MOE_SH13) ? 1 : 0;
+    p.rows = p.gate_up ? 2 * I : d->H;
+    p.K = p.gate_up ? d->H : I;
+    p.I = I;
+    REQUIRE_PTR(codes, "codes");
+    REQUIRE_PTR(dst, "dst");
+    if (p.fmt != MOE_FMT_BF16) REQUIRE_PTR(scales, "scales");
+    p.codes = static_cast<const uint8_t*>(codes);
+    p.scales = static_cast<const uint8_t*>(scales);
+    p.dst = static_cast<uint8_t*>(dst);
+    k_pack<<<1024, 256, 0, (cudaStream_t)stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "k_pack launch");
+    return ok();
+}
+
+moe_status moe_router_topk(const moe_layer_desc* d, const void* x, const void* w_gate, const float* bias,
+                           const float* logits_in, int M, float* logits_out, int32_t* topk_idx, float* topk_w,
+                           void* xq, void* xq_scales, void* xq_sh, void* xq_sh_scales, void* ws,
+                           moe_stream_t stream) {
+    moe_status s = check_desc(d);
+    if (s != MOE_OK) return s;
+    REQUIRE(M >= 1 && M <= kMaxRows, "M=%d: need 1..%d", M, kMaxRows);
+    REQUIRE_PTR(x, "x");
+    if (!logits_in) REQUIRE_PTR(w_gate, "w_gate");
+    OPT_PTR(logits_in, "logits_in");
+    OPT_PTR(logits_out, "logits_out");
+    if (d->has_bias) REQUIRE_PTR(bias, "bias");
+    REQUIRE_PTR(topk_idx, "topk_idx");
+    REQUIRE_PTR(topk_w, "topk_w");
+    REQUIRE_PTR(xq, "xq");
+    REQUIRE_PTR(xq_scales, "xq_scales");
+    if (separate_shared_input(d)) {
+        REQUIRE_PTR(xq_sh, "xq_sh");
+        if (d->shared_fmt != MOE_FMT_BF16) REQUIRE_PTR(xq_sh_scales, "xq_sh_scales");
+    }
+    REQUIRE_PTR(ws, "ws");
+    const WsLayout L = layout(d);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    float* scores = reinterpret_cast<float*>(w + L.scores);
+    cudaStream_t st = (cudaStream_t)stream;
+    s = launch_router(d, x, w_gate, logits_in, M, logits_out, scores, xq, xq_scales, xq_sh, xq_sh_scales, st);
+    if (s != MOE_OK) return s;
+    s = launch_topk_route(d, L, w, M, scores, bias, topk_idx, topk_w, 1, 0, nullptr, nullptr, nullptr, nullptr,
+                          nullptr, st);
+    if (s != MOE_OK) return s;
+    return ok();
+}
+
+moe_status moe_route_tiles(const moe_layer_desc* d, const int32_t* topk_idx, int M, int32_t* tiles,
+                           int32_t* num_tiles, int32_t* perm, int32_t* inv_perm, int32_t* expert_counts, void* ws,
+                           moe_stream_t stream) {
+    moe_status s = check_desc(d);
+    if (s != MOE_OK) return s;
+    REQUIRE(M >= 1 && M <= kMaxRows, "M=%d: need 1..%d", M, kMaxRows);
+    REQUIRE_PTR(topk_idx, "topk_idx");
+    REQUIRE_PTR(tiles, "tiles");
+    REQUIRE_PTR(num_tiles, "num_tiles");
+    REQUIRE_PTR(perm, "perm");
+    REQUIRE_PTR(inv_perm, "inv_perm");
+    REQUIRE_PTR(expert_counts, "expert_counts");
+    REQUIRE_PTR(ws, "ws");
+    const WsLayout L = layout(d);
+    s = launch_topk_route(d, L, static_cast<uint8_t*>(ws), M, nullptr, nullptr, const_cast<int32_t*>(topk_idx),
+                          nullptr, 0, 1, expert_counts, perm, inv_perm, tiles, num_tiles, (cudaStream_t)stream);
+    if (s != MOE_OK) return s;
+    return ok();
+}
+
+moe_status moe_expert_gate_up(const moe_layer_desc* d, const moe_qweight* w13, const moe_qweight* sh13,
+                              const void* xq, const void* xq_scales, const void* xq_sh, const void* xq_sh_scales,
+                              const int32_t* perm, int M, void* hq, void* hq_scales, void* ws,
+                              moe_stream_t stream) {
+    moe_status s = check_desc(d);
+    if (s != MOE_OK) return s;
+    REQUIRE(M >= 1 && M <= kMaxRows, "M=%d: need 1..%d", M, kMaxRows);
+    if ((s = check_qweight(w13, d->w_fmt, "w13")) != MOE_OK) return s;
+    if (d->has_shared && (s = check_qweight(sh13, d->shared_fmt, "sh13")) != MOE_OK) return s;
+    REQUIRE_PTR(xq, "xq");
+    REQUIRE_PTR(xq_scales, "xq_scales");
+    if (separate_shared_input(d)) {
+        REQUIRE_PTR(xq_sh, "xq_sh");
+        if (d->shared_fmt != MOE_FMT_BF16) REQUIRE_PTR(xq_sh_scales, "xq_sh_scales");
+    }
+    REQUIRE_PTR(perm, "perm");
+    REQUIRE_PTR(hq, "hq");
+    REQUIRE_PTR(hq_scales, "hq_scales");
+    REQUIRE_PTR(ws, "ws");
+    const WsLayout L = layout(d);
+    GemmBuffers b{};
+    b.xq = xq;
+    b.xs = xq_scales;
+    b.xq_sh = separate_shared_input(d) ? xq_sh : xq;
+    b.xs_sh = separate_shared_input(d) ? xq_sh_scales : xq_scales;
+    b.hq = hq;
+    b.hs = hq_scales;
+    b.perm = perm;
+    s = launch_gemm(0, d, w13, sh13, b, M, L, static_cast<uint8_t*>(ws), (cudaStream_t)stream);
+    if (s != MOE_OK) return s;
+    return ok();
+}
+
+moe_status moe_expert_down(const moe_layer_desc* d, const moe_qweight* w2, const moe_qweight* sh2, const void* hq,
+                           const void* hq_scales, int M, float* y_pairs, void* ws, moe_stream_t stream) {
+    moe_status s = check_desc(d);
+    if (s != MOE_OK) return s;
+    REQUIRE(M >= 1 && M <= kMaxRows, "M=%d: need 1..%d", M, kMaxRows);
+    if ((s = check_qweight(w2, d->w_fmt, "w2")) != MOE_OK) return s;
+    if (d->has_shared && (s = check_qweight(sh2, d->shared_fmt, "sh2")) != MOE_OK) return s;
+    REQUIRE_PTR(hq, "hq");
+    REQUIRE_PTR(hq_scales, "hq_scales");
+    REQUIRE_PTR(y_pairs, "y_pairs");
+    REQUIRE_PTR(ws, "ws");
+    const WsLayout L = layout(d);
+    GemmBuffers b{};
+    b.hq = const_cast<void*>(hq);
+    b.hs = const_cast<void*>(hq_scales);
+    b.y = y_pairs;
+    s = launch_gemm(1, d, w2, sh2, b, M, L, static_cast<uint8_t*>(ws), (cudaStream_t)stream);
+    if (s != MOE_OK) return s;
+    return ok();
+}
+
+moe_status moe_finalize_norm(const moe_layer_desc* d, const float* y_pairs, const float* topk_w,
+                             const int32_t* inv_perm, int M, void* residual, const void* gamma, void* out,
+                             void* outq, void* outq_scales, void* ws, moe_stream_t stream) {
+    moe_status s = check_desc(d);
+    if (s != MOE_OK) return s;
+    REQUIRE(M >= 1 && M <= kMaxRows, "M=%d: need 1..%d", M, kMaxRows);
+    REQUIRE_PTR(y_pairs, "y_pairs");
+    REQUIRE_PTR(topk_w, "topk_w");
+    REQUIRE_PTR(inv_perm, "inv_perm");
+    REQUIRE_PTR(residual, "residual");
+    REQUIRE_PTR(gamma, "gamma");
+    REQUIRE_PTR(out, "out");
+    REQUIRE((outq == nullptr) == (outq_scales == nullptr), "outq and outq_scales must both be given or both NULL");
+    OPT_PTR(outq, "outq");
+    OPT_PTR(outq_scales, "outq_scales");
+    (void)ws;
+    s = launch_finalize(d, y_pairs, topk_w, inv_perm, M, residual, gamma, out, outq, outq_scales,
+                        (cudaStream_t)stream);
+    if (s != MOE_OK) return s;
+    return ok();
+}
+
+moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void* ws, moe_stream_t stream) {
+    moe_status s = check_desc(d);
+    if (s != MOE_OK) return s;
+    REQUIRE(a != nullptr, "args is NULL");
+    REQUIRE(M >= 1 && M <= kMaxRows, "M=%d: need 1..%d", M, kMaxRows);
+    REQUIRE_PTR(a->x, "x");
+    REQUIRE_PTR(a->w_gate, "w_gate");
+    if (d->has_bias) REQUIRE_PTR(a->bias, "bias");
+    if ((s = check_qweight(&a->w13, d->w_fmt, "w13")) != MOE_OK) return s;
+    if ((s = check_qweight(&a->w2, d->w_fmt, "w2")) != MOE_OK) return s;
+    if (d->has_shared) {
+        if ((s = check_qweight(&a->sh13, d->shared_fmt, "sh13")) != MOE_OK) return s;
+        if ((s = check_qweight(&a->sh2, d->shared_fmt, "sh2")) != MOE_OK) return s;
+    }
+    REQUIRE_PTR(a->residual, "residual");
+    REQUIRE_PTR(a->gamma, "gamma");
+    REQUIRE_PTR(a->out, "out");
+    if (d->emit_next_mxfp8) {
+        REQUIRE_PTR(a->outq, "outq");
+        REQUIRE_PTR(a->outq_scales, "outq_scales");
+    }
+    REQUIRE_PTR(ws, "ws");
+    const WsLayout L = layout(d);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    cudaStream_t st = (cudaStream_t)stream;
+    float* logits = reinterpret_cast<float*>(w + L.logits);
+    float* scores = reinterpret_cast<float*>(w + L.scores);
+    int32_t* topk_idx = reinterpret_cast<int32_t*>(w + L.topk_idx);
+    float* topk_w = reinterpret_cast<float*>(w + L.topk_w);
+    int32_t* perm = reinterpret_cast<int32_t*>(w + L.perm);
+    int32_t* inv_perm = reinterpret_cast<int32_t*>(w + L.inv_perm);
+    s = launch_router(d, a->x, a->w_gate, nullptr, M, logits, scores, w + L.xq, w + L.xs, w + L.xq_sh, w + L.xs_sh,
+                      st);
+    if (s != MOE_OK) return s;
+    s = launch_topk_route(d, L, w, M, scores, a->bias, topk_idx, topk_w, 1, 1,
+                          reinterpret_cast<int32_t*>(w + L.counts), perm, inv_perm,
+                          reinterpret_cast<int32_t*>(w + L.tiles), reinterpret_cast<int32_t*>(w + L.num_tiles), st);
+    if (s != MOE_OK) return s;
+    GemmBuffers b{};
+    b.xq = w + L.xq;
+    b.xs = w + L.xs;
+    b.xq_sh = w + L.xq_sh;
+    b.xs_sh = w + L.xs_sh;
+    b.hq = w + L.hq;
+    b.hs = w + L.hs;
+    b.y = reinterpret_cast<float*>(w + L.y);
+    b.perm = perm;
+    s = launch_gemm(0, d, &a->w13, &a->sh13, b, M, L, w, st);
+    if (s != MOE_OK) return s;
+    s = launch_gemm(1, d, &a->w2, &a->sh2, b, M, L, w, st);
+    if (s != MOE_OK) return s;
+    s = launch_finalize(d, b.y, topk_w, inv_perm, M, a->residual, a->gamma, a->out,
+                        d->emit_next_mxfp8 ? a->outq : nullptr, d->emit_next_mxfp8 ? a->outq_scales : nullptr, st);
+    if (s != MOE_OK) return s;
+    return ok();
+}
+
+moe_status moe_get_status(void* ws, moe_stream_t stream, int* dev_status) {
+    REQUIRE_PTR(ws, "ws");
+    REQUIRE(dev_status != nullptr, "dev_status is NULL");
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    int v = 0;
+    e = cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status)");
+    *dev_status = v;
+    return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,479 @@
+// Expert GEMMs of the MoE step on the 5th-generation tensor cores (sm_103a).
+//
+// "SGLang-NVIDIA-Mega" README, slot table of "What a covered DeepSeek-V4.1-Flash step
+// runs", row moe: a route kernel and a pair of block-scaled tcgen05 GEMMs with 8-row
+// tiles; row shared_ll: SwiGLU between the shared expert's GEMMs; Qwen3.5 slot table,
+// row mkm: FC1, SwiGLU, NVFP4 requantisation and FC2. "sgl-nvidia-mega pull request 24",
+// Target spec: the engines stream weights from records derived at load, and every map
+// of the same rows gives the same bytes.
+//
+// Design (swap-AB): the expert weight is the MMA's A operand (M = 128 weight rows), the
+// step's rows are N (padded to a multiple of 16). A unit is one (expert group, 128-row
+// weight block); its K loop runs over 128-byte steps. All units of one launch form a
+// single step space that is cut into equal contiguous ranges, one per CTA (stream-K),
+// so every SM streams the same number of weight bytes. A unit cut between CTAs is summed
+// by the last CTA to finish a piece, in piece order (deterministic).
+//
+// Roles: warp 0 lane 0 issues the bulk copies (weight record + activation tile + its
+// scales) into a ring of shared-memory stages; warp 1 lane 0 copies the scales to tensor
+// memory and issues the MMAs into one of two TMEM accumulators; warps 2..5 drain the
+// accumulator and run the epilogue (gate_up: SwiGLU + requantisation into the tiled FC2
+// input; down: fp32 rows in perm order).
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "quant.cuh"
+
+namespace moe {
+
+constexpr int kGemmThreads = 192;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr uint32_t kTmemCols = 512;
+constexpr int kAccCols = 64;
+
+struct Seg {
+    int cls, g, b, ka, kb, KS;
+    long long unit, us;  // global unit id, first global step of the unit
+};
+
+struct Walker {
+    long long T_r, T, t, t1;
+    int MB0, KS0, MB1, KS1;
+    long long NR_units;
+    // Effective grid: never more CTAs than steps, so every working CTA owns at least one
+    // step and the CTAs whose ranges meet a unit are exactly its pieces.
+    __device__ static long long total_steps(const GemmParams& p, int ngroups) {
+        return (long long)ngroups * p.cls[0].MB * p.cls[0].KS + (p.has_shared ? (long long)p.cls[1].MB * p.cls[1].KS : 0);
+    }
+    __device__ void init(const GemmParams& p, int ngroups, int G, int c) {
+        MB0 = p.cls[0].MB;
+        KS0 = p.cls[0].KS;
+        MB1 = p.cls[1].MB;
+        KS1 = p.cls[1].KS;
+        NR_units = (long long)ngroups * MB0;
+        T_r = NR_units * KS0;
+        T = T_r + (p.has_shared ? (long long)MB1 * KS1 : 0);
+        if (c >= G || T == 0) {
+            t = t1 = 0;
+            return;
+        }
+        t = (long long)c * T / G;
+        t1 = (long long)(c + 1) * T / G;
+    }
+    __device__ bool next(Seg& s) {
+        if (t >= t1) return false;
+        if (t < T_r) {
+            const long long u = t / KS0;
+            s.cls = 0;
+            s.KS = KS0;
+            s.g = (int)(u / MB0);
+            s.b = (int)(u % MB0);
+            s.ka = (int)(t - u * KS0);
+            s.unit = u;
+            s.us = u * KS0;
+        } else {
+            const long long tt = t - T_r, u = tt / KS1;
+            s.cls = 1;
+            s.KS = KS1;
+            s.g = -1;
+            s.b = (int)u;
+            s.ka = (int)(tt - u * KS1);
+            s.unit = NR_units + u;
+            s.us = T_r + u * KS1;
+        }
+        const long long room = t1 - t;
+        s.kb = (int)((long long)s.ka + room < (long long)s.KS ? s.ka + room : s.KS);
+        t += s.kb - s.ka;
+        return true;
+    }
+    __device__ long long start(long long c, int G) const { return c * T / G; }
+    __device__ int cta_of(long long step, int G) const { return (int)(((step + 1) * G - 1) / T); }
+};
+
+struct GemmSmem {
+    uint8_t* ring;
+    float* stg;  // [kAccCols][128] fp32 epilogue staging
+    uint64_t* full;
+    uint64_t* empty;
+    uint64_t* acc_full;
+    uint64_t* acc_empty;
+    uint64_t* drain;
+    uint32_t* tmem_base;
+    int* abort_flag;
+    int* bcast;
+    int* never;  // stays 0: lets the exit-time drains ignore the abort flag
+};
+
+__device__ __forceinline__ void set_error(int32_t* status, int* abort_flag, int code) {
+    atomicCAS(status, 0, code);
+    *(volatile int*)abort_flag = 1;
+}
+
+__device__ __forceinline__ float warp_max_f(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Group facts of a segment.
+__device__ __forceinline__ void seg_group(const GemmParams& p, const Seg& s, int& expert, int& rows, int& perm_off,
+                                          int& row_off, int& gidx) {
+    if (s.cls == 0) {
+        const Group gr = p.groups[s.g];
+        expert = gr.expert;
+        rows = gr.rows;
+        perm_off = gr.perm_off;
+        row_off = gr.row_off;
+        gidx = s.g;
+    } else {
+        expert = 0;
+        rows = p.M;
+        perm_off = p.M * p.k;
+        row_off = 0;
+        gidx = 0;
+    }
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_constant__ GemmParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int S = p.stages;
+
+    // ---- shared-memory carve-up
+    GemmSmem sm;
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    sm.ring = base;
+    sm.stg = reinterpret_cast<float*>(base + (size_t)S * p.stage_bytes);
+    uint8_t* misc = reinterpret_cast<uint8_t*>(sm.stg + p.Mpad * kBlockRows);
+    sm.full = reinterpret_cast<uint64_t*>(misc);
+    sm.empty = sm.full + S;
+    sm.acc_full = sm.empty + S;
+    sm.acc_empty = sm.acc_full + 2;
+    sm.drain = sm.acc_empty + 2;
+    sm.tmem_base = reinterpret_cast<uint32_t*>(sm.drain + 1);
+    sm.abort_flag = reinterpret_cast<int*>(sm.tmem_base + 1);
+    sm.bcast = sm.abort_flag + 1;
+    sm.never = sm.abort_flag + 2;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(smem_u32(&sm.full[i]), 1);
+            mbar_init(smem_u32(&sm.empty[i]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&sm.acc_full[i]), 1);
+            mbar_init(smem_u32(&sm.acc_empty[i]), 4);
+        }
+        mbar_init(smem_u32(sm.drain), 1);
+        *sm.abort_flag = 0;
+        *sm.never = 0;
+        fence_mbar_init();
+    }
+    // Everything below reads the previous launches' outputs.
+    pdl_wait();
+    if (warp == 1) {
+        tmem_alloc(smem_u32(sm.tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *sm.tmem_base;
+    pdl_trigger();
+
+    const int ngroups = p.hdr->num_groups;
+    const long long T_all = Walker::total_steps(p, ngroups);
+    const int G = (int)((long long)gridDim.x < T_all ? (long long)gridDim.x : T_all), c = blockIdx.x;
+    volatile int* abort_flag = sm.abort_flag;
+
+    if (warp == 0) {
+        // ================================================================ producer
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            Walker wk;
+            wk.init(p, ngroups, G, c);
+            Seg s;
+            int st = 0;
+            uint32_t ph = 0;
+            uint32_t issued_mask = 0;  // stages with a copy in flight at least once
+            bool ok = true;
+            while (ok && wk.next(s)) {
+                const GemmClass& C = p.cls[s.cls];
+                int expert, rows, perm_off, row_off, gidx;
+                seg_group(p, s, expert, rows, perm_off, row_off, gidx);
+                const int A = atoms_per_step(C.fmt);
+                const uint32_t REC = record_bytes(C.fmt);
+                int Rpad;
+                const uint8_t *bsrc, *bssrc;
+                if (p.mode == 0) {
+                    Rpad = p.Mpad;
+                    bsrc = C.b;
+                    bssrc = C.bs;
+                } else {
+                    Rpad = (s.cls == 0) ? round_up(rows, 16) : p.Mpad;
+                    bsrc = C.b + (size_t)row_off * C.KS * kStepBytes;
+                    bssrc = C.bs + (size_t)gidx * C.KS * A * kAtomBytes;
+                }
+                const uint8_t* wrec = C.w + ((size_t)((size_t)expert * C.MB + s.b) * C.KS + s.ka) * REC;
+                const uint32_t bbytes = (uint32_t)Rpad * kStepBytes;
+                for (int kk = s.ka; kk < s.kb; ++kk) {
+                    if (!mbar_wait_bounded(smem_u32(&sm.empty[st]), ph ^ 1u, abort_flag, kWaitLimitNs)) {
+                        set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* stage = sm.ring + (size_t)st * p.stage_bytes;
+                    const uint32_t fb = smem_u32(&sm.full[st]);
+                    mbar_arrive_expect_tx(fb, REC + bbytes + (uint32_t)A * kAtomBytes);
+                    bulk_g2s_hint(smem_u32(stage + p.a_off), wrec, REC, fb, pol);
+                    bulk_g2s(smem_u32(stage + p.b_off), bsrc + (size_t)kk * bbytes, bbytes, fb);
+                    if (A) bulk_g2s(smem_u32(stage + p.sfb_off), bssrc + (size_t)kk * A * kAtomBytes, A * kAtomBytes, fb);
+                    issued_mask |= 1u << st;
+                    wrec += REC;
+                    if (++st == S) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            // make sure no copy is still writing shared memory when the CTA exits: wait for
+            // the last phase issued on every stage (stages < st were issued in lap ph,
+            // the others in lap ph ^ 1)
+            for (int i = 0; i < S; ++i) {
+                if (!(issued_mask >> i & 1u)) continue;
+                const uint32_t par = (i < st) ? ph : (ph ^ 1u);
+                mbar_wait_bounded(smem_u32(&sm.full[i]), par, sm.never, kWaitLimitNs / 2);
+            }
+        }
+    } else if (warp == 1) {
+        // ================================================================ MMA issuer
+        if (lane == 0) {
+            Walker wk;
+            wk.init(p, ngroups, G, c);
+            Seg s;
+            int st = 0;
+            uint32_t ph = 0;
+            int ab = 0;
+            uint32_t acc_ph[2] = {0u, 0u};
+            bool ok = true;
+            const int am = p.atoms_max;
+            while (ok && wk.next(s)) {
+                const GemmClass& C = p.cls[s.cls];
+                int expert, rows, perm_off, row_off, gidx;
+                seg_group(p, s, expert, rows, perm_off, row_off, gidx);
+                const uint32_t N = (p.mode == 0) ? (uint32_t)p.Mpad : (uint32_t)((s.cls == 0) ? round_up(rows, 16) : p.Mpad);
+                if (!mbar_wait_bounded(smem_u32(&sm.acc_empty[ab]), acc_ph[ab] ^ 1u, abort_flag, kWaitLimitNs)) {
+                    set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + (uint32_t)(ab * kAccCols);
+                for (int kk = s.ka; kk < s.kb; ++kk) {
+                    if (!mbar_wait_bounded(smem_u32(&sm.full[st]), ph, abort_flag, kWaitLimitNs)) {
+                        set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint8_t* stage = sm.ring + (size_t)st * p.stage_bytes;
+                    const uint32_t a_s = smem_u32(stage + p.a_off), b_s = smem_u32(stage + p.b_off);
+                    const uint32_t sfa_t = tmem + 2 * kAccCols + (uint32_t)st * 8 * am;
+                    const uint32_t sfb_t = sfa_t + 4 * am;
+                    if (C.fmt == MOE_FMT_MXFP8) {
+                        tc_cp_sf(sfa_t, smem_desc(smem_u32(stage + p.sfa_off), 0, 128, 0));
+                        tc_cp_sf(sfb_t, smem_desc(smem_u32(stage + p.sfb_off), 0, 128, 0));
+#pragma unroll
+                        for (int sub = 0; sub < 4; ++sub) {
+                            mma_mxf8(d_tmem, smem_desc(a_s + 32 * sub, 16, 1024, 2), smem_desc(b_s + 32 * sub, 16, 1024, 2),
+                                     idesc_mxf8(N, sub), sfa_t, sfb_t, (kk > s.ka || sub > 0) ? 1u : 0u);
+                        }
+                    } else if (C.fmt == MOE_FMT_NVFP4) {
+#pragma unroll
+                        for (int a = 0; a < 4; ++a) {
+                            tc_cp_sf(sfa_t + 4 * a, smem_desc(smem_u32(stage + p.sfa_off + a * kAtomBytes), 0, 128, 0));
+                            tc_cp_sf(sfb_t + 4 * a, smem_desc(smem_u32(stage + p.sfb_off + a * kAtomBytes), 0, 128, 0));
+                        }
+#pragma unroll
+                        for (int sub = 0; sub < 4; ++sub) {
+                            mma_nvf4(d_tmem, smem_desc(a_s + 32 * sub, 16, 1024, 2), smem_desc(b_s + 32 * sub, 16, 1024, 2),
+                                     idesc_nvf4(N), sfa_t + 4 * sub, sfb_t + 4 * sub, (kk > s.ka || sub > 0) ? 1u : 0u);
+                        }
+                    } else {
+#pragma unroll
+                        for (int sub = 0; sub < 4; ++sub) {
+                            mma_bf16(d_tmem, smem_desc(a_s + 32 * sub, 16, 1024, 2), smem_desc(b_s + 32 * sub, 16, 1024, 2),
+                                     idesc_bf16(N), (kk > s.ka || sub > 0) ? 1u : 0u);
+                        }
+                    }
+                    tc_commit(smem_u32(&sm.empty[st]));
+                    if (++st == S) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(smem_u32(&sm.acc_full[ab]));
+                acc_ph[ab] ^= 1u;
+                ab ^= 1;
+            }
+            // wait until every issued MMA has completed before the TMEM is released
+            tc_commit(smem_u32(sm.drain));
+            mbar_wait_bounded(smem_u32(sm.drain), 0u, sm.never, kWaitLimitNs / 2);
+        }
+    } else {
+        // ================================================================ epilogue
+        const int q = warp % 4;           // TMEM lane quarter of this warp
+        const int r = 32 * q + lane;      // accumulator row (weight row of the block)
+        const int et = threadIdx.x - 64;  // 0..127
+        const int ew = et / 32;
+        Walker wk;
+        wk.init(p, ngroups, G, c);
+        Seg s;
+        int ab = 0;
+        uint32_t acc_ph[2] = {0u, 0u};
+        float* stg = sm.stg;
+        while (wk.next(s)) {
+            const GemmClass& C = p.cls[s.cls];
+            int expert, rows, perm_off, row_off, gidx;
+            seg_group(p, s, expert, rows, perm_off, row_off, gidx);
+            const int N = (p.mode == 0) ? p.Mpad : ((s.cls == 0) ? round_up(rows, 16) : p.Mpad);
+            if (!mbar_wait_bounded(smem_u32(&sm.acc_full[ab]), acc_ph[ab], abort_flag, kWaitLimitNs)) {
+                set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
+                break;
+            }
+            acc_ph[ab] ^= 1u;
+            tc_fence_after();
+            const uint32_t t_row = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(ab * kAccCols);
+            for (int c0 = 0; c0 < N; c0 += 16) {
+                float v[16];
+                tmem_ld16(t_row + (uint32_t)c0, v);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) stg[(c0 + i) * kBlockRows + r] = v[i];
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sm.acc_empty[ab]));
+            ab ^= 1;
+            // compact the selected columns: column of group row rg -> stg[rg][r]
+            if (p.mode == 0 && s.cls == 0) {
+                for (int rg = 0; rg < rows; ++rg) {
+                    const int m = p.perm[perm_off + rg] / p.k;
+                    stg[rg * kBlockRows + r] = stg[m * kBlockRows + r];
+                }
+            }
+            // stream-K: pieces of a unit cut between CTAs
+            const long long ue = s.us + s.KS - 1;
+            const int c_first = wk.cta_of(s.us, G), c_last = wk.cta_of(ue, G);
+            const int npieces = c_last - c_first + 1;
+            if (npieces > 1) {
+                const int my_slot = (c == c_first && wk.start(c, G) < s.us) ? 1 : 0;
+                float* part = p.partials + ((size_t)c * 2 + my_slot) * kPartialFloats;
+                for (int rg = 0; rg < rows; ++rg) __stcg(part + rg * kBlockRows + r, stg[rg * kBlockRows + r]);
+                __threadfence();
+                named_bar(1, 128);
+                if (et == 0) {
+                    const int old = atomicAdd(p.counters + s.unit, 1);
+                    *sm.bcast = (old == npieces - 1) ? 1 : 0;
+                }
+                named_bar(1, 128);
+                const int last = *(volatile int*)sm.bcast;
+                named_bar(1, 128);
+                if (!last) continue;
+                __threadfence();
+                for (int rg = 0; rg < rows; ++rg) {
+                    float sum = 0.0f;
+                    for (int pc = 0; pc < npieces; ++pc) {
+                        const int cc = c_first + pc;
+                        const int sl = (pc == 0 && wk.start(cc, G) < s.us) ? 1 : 0;
+                        sum += __ldcg(p.partials + ((size_t)cc * 2 + sl) * kPartialFloats + rg * kBlockRows + r);
+                    }
+                    stg[rg * kBlockRows + r] = sum;
+                }
+                if (et == 0) p.counters[s.unit] = 0;
+            }
+            named_bar(1, 128);
+            // ---- final epilogue
+            const float alpha = C.gs_w ? C.gs_w[expert] * C.gs_a : 1.0f;
+            if (p.mode == 0) {
+                // SwiGLU on (gate, up) = rows (fi, fi + 64); warps take 32 features each
+                const int fi = 32 * (ew & 1) + lane;
+                const int f = 64 * s.b + fi;  // feature in [0, I)
+                const int Rp = (s.cls == 0) ? round_up(rows, 16) : p.Mpad;
+                uint8_t* hq_g = C.hq + (s.cls == 0 ? (size_t)row_off * row_bytes(C.out_fmt, C.I) : 0);
+                const int Aout = atoms_per_step(C.out_fmt);
+                const int KSo = steps_of(C.out_fmt, C.I);
+                uint8_t* hs_g = C.hs + (s.cls == 0 ? (size_t)gidx * KSo * Aout * kAtomBytes : 0);
+                for (int rg = (ew >> 1); rg < rows; rg += 2) {
+                    const float g = stg[rg * kBlockRows + fi] * alpha;
+                    const float u = stg[rg * kBlockRows + fi + 64] * alpha;
+                    const float h = g / (1.0f + expf(-g)) * u;
+                    if (C.out_fmt == MOE_FMT_MXFP8) {
+                        const float amax = warp_max_f(fabsf(h));
+                        const int e = mx_exponent(amax);
+                        const uint32_t qb = e4m3(__fmul_rn(h, exp2_int(-e)));
+                        // gather 4 consecutive features into one word
+                        const uint32_t b1 = __shfl_down_sync(0xffffffffu, qb, 1);
+                        const uint32_t b2 = __shfl_down_sync(0xffffffffu, qb, 2);
+                        const uint32_t b3 = __shfl_down_sync(0xffffffffu, qb, 3);
+                        const int sidx = f / 128, cb = f % 128;
+                        if ((lane & 3) == 0) {
+                            uint8_t* row = hq_g + (size_t)sidx * Rp * kStepBytes + (size_t)rg * kStepBytes;
+                            *reinterpret_cast<uint32_t*>(row + (((cb / 16) ^ (rg & 7)) * 16) + (cb % 16)) =
+                                qb | (b1 << 8) | (b2 << 16) | (b3 << 24);
+                        }
+                        if (lane == 0)
+                            hs_g[(size_t)sidx * kAtomBytes + (rg % 32) * 16 + (rg / 32) * 4 + (cb / 32)] = (uint8_t)(e + 127);
+                    } else if (C.out_fmt == MOE_FMT_NVFP4) {
+                        float amax = fabsf(h);
+#pragma unroll
+                        for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+                        const uint8_t s8 = nv_scale(amax, C.gs_out);
+                        const float dsc = e4m3_to_f32(s8);
+                        const float denom = __fmul_rn(dsc, C.gs_out);
+                        const uint32_t nib = (dsc != 0.0f) ? (e2m1x2(0.0f, __fdiv_rn(h, denom)) & 0xFu) : 0u;
+                        // byte of features (2j, 2j+1): low nibble even feature
+                        const uint32_t nb1 = __shfl_down_sync(0xffffffffu, nib, 1);
+                        const uint32_t byte = nib | (nb1 << 4);
+                        const uint32_t y1 = __shfl_down_sync(0xffffffffu, byte, 2);
+                        const uint32_t y2 = __shfl_down_sync(0xffffffffu, byte, 4);
+                        const uint32_t y3 = __shfl_down_sync(0xffffffffu, byte, 6);
+                        const int sidx = f / 256, cbyte = (f % 256) / 2;
+                        if ((lane & 7) == 0) {
+                            uint8_t* row = hq_g + (size_t)sidx * Rp * kStepBytes + (size_t)rg * kStepBytes;
+                            *reinterpret_cast<uint32_t*>(row + (((cbyte / 16) ^ (rg & 7)) * 16) + (cbyte % 16)) =
+                                (byte & 0xFFu) | ((y1 & 0xFFu) << 8) | ((y2 & 0xFFu) << 16) | ((y3 & 0xFFu) << 24);
+                        }
+                        if ((lane & 15) == 0) {
+                            const int b16 = (f % 256) / 16;
+                            hs_g[(size_t)sidx * 4 * kAtomBytes + (b16 / 4) * kAtomBytes + (rg % 32) * 16 + (rg / 32) * 4 +
+                                 (b16 % 4)] = s8;
+                        }
+                    } else {  // BF16 FC2 input
+                        const uint32_t hb = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(h));
+                        const uint32_t hb1 = __shfl_down_sync(0xffffffffu, hb, 1);
+                        const int sidx = f / 64, cbyte = (f % 64) * 2;
+                        if ((lane & 1) == 0) {
+                            uint8_t* row = hq_g + (size_t)sidx * Rp * kStepBytes + (size_t)rg * kStepBytes;
+                            *reinterpret_cast<uint32_t*>(row + (((cbyte / 16) ^ (rg & 7)) * 16) + (cbyte % 16)) =
+                                hb | (hb1 << 16);
+                        }
+                    }
+                }
+            } else {
+                const int n = kBlockRows * s.b + et;
+                for (int rg = 0; rg < rows; ++rg) {
+                    const int pos = perm_off + rg;
+                    p.y[(size_t)pos * p.H + n] = stg[rg * kBlockRows + et] * alpha;
+                }
+            }
+            named_bar(1, 128);
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace moe

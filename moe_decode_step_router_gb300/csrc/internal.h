@@ -1,0 +1,139 @@
+// Layouts and kernel parameter blocks shared by the host side and the kernels of the
+// library (not part of the public ABI).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/moestep.h"
+
+namespace moe {
+
+constexpr int kMaxRows = 64;         // rows per step
+constexpr int kMaxK = 16;            // top-k
+constexpr int kMaxE = 512;           // routed experts
+constexpr int kTileRows = 8;         // route tile height
+constexpr int kStepBytes = 128;      // K bytes per pipeline step (one 128-byte swizzle row)
+constexpr int kBlockRows = 128;      // weight rows per MMA block (the MMA's M)
+constexpr int kAtomBytes = 512;      // scale atom: 128 rows x 4 bytes
+constexpr int kMaxGemmCtas = 256;    // partial-sum slots are sized for this many CTAs
+constexpr int kPartialFloats = kMaxRows * kBlockRows;  // one stream-K partial
+
+__host__ __device__ inline int round_up(int a, int b) { return (a + b - 1) / b * b; }
+
+__host__ __device__ inline int64_t row_bytes(int fmt, int64_t K) {
+    return fmt == MOE_FMT_BF16 ? 2 * K : (fmt == MOE_FMT_MXFP8 ? K : K / 2);
+}
+__host__ __device__ inline int64_t row_scales(int fmt, int64_t K) {
+    return fmt == MOE_FMT_MXFP8 ? K / 32 : (fmt == MOE_FMT_NVFP4 ? K / 16 : 0);
+}
+// Scale atoms per 128-byte K step (MXFP8 1, NVFP4 4, BF16 0).
+__host__ __device__ inline int atoms_per_step(int fmt) {
+    return fmt == MOE_FMT_MXFP8 ? 1 : (fmt == MOE_FMT_NVFP4 ? 4 : 0);
+}
+__host__ __device__ inline int steps_of(int fmt, int K) { return (int)(row_bytes(fmt, K) / kStepBytes); }
+// Packed record: 128 rows x 128 B of codes plus the step's scale atoms.
+__host__ __device__ inline int record_bytes(int fmt) {
+    return kBlockRows * kStepBytes + atoms_per_step(fmt) * kAtomBytes;
+}
+
+// Group table entry written by the route kernel, one per selected routed expert.
+struct Group {
+    int32_t expert, rows, perm_off, row_off;  // row_off: padded rows before this group
+};
+
+// Workspace header (first 256 bytes of ws).
+struct WsHeader {
+    int32_t status;
+    int32_t num_groups;  // routed groups
+    int32_t num_tiles;
+    int32_t pad0;
+    int32_t err_info[4];
+};
+
+// Byte offsets of the workspace regions for a layer and a maximum row count.
+struct WsLayout {
+    size_t header, groups, logits, scores, topk_idx, topk_w, counts, perm, inv_perm, tiles, num_tiles;
+    size_t xq, xs, xq_sh, xs_sh, hq, hs, y, cnt_gu, cnt_dn, partials, total;
+    int max_rows, P_max, G_max, T_max, U_gu, U_dn;
+    size_t hq_routed_bytes, hs_routed_bytes;  // shared group's data / scales start here
+};
+
+// ---------------------------------------------------------------- kernel parameters
+struct RouterParams {
+    const uint16_t* x;        // bf16 [M, H]
+    const uint16_t* wg;       // bf16 [E, H]
+    const float* logits_in;   // [M, E] or null
+    float* logits_out;        // [M, E] or null
+    float* scores;            // [M, E]
+    int M, H, E, experts_per_cta;
+    // FC1 input quantisation (tiled layout)
+    int fmt_r, fmt_s, quant_shared;
+    uint8_t *xq, *xs, *xq_sh, *xs_sh;
+    float gs_r, gs_s;
+    int num_quant_ctas;       // CTAs (at the front of the grid) that quantise
+};
+
+struct TopkRouteParams {
+    const float* scores;      // [M, E] (topk stage)
+    const float* bias;        // [E] or null
+    int32_t* topk_idx;        // [M, k]
+    float* topk_w;            // [M, k]
+    int M, E, k, renormalize, has_shared, do_topk, do_route;
+    float rsf;
+    int32_t *counts, *perm, *inv_perm, *tiles, *num_tiles;
+    Group* groups;
+    WsHeader* hdr;
+};
+
+struct GemmClass {            // one weight class: routed experts or the shared expert
+    int fmt;                  // weight / activation format
+    const uint8_t* w;         // packed records
+    const float* gs_w;        // NVFP4 per-expert global scales or null
+    int MB, KS;               // 128-row blocks, 128-byte K steps
+    const uint8_t* b;         // tiled B operand base (gate_up: xq; down: hq group region)
+    const uint8_t* bs;        // its scales
+    float gs_a;               // static global scale of the B operand (NVFP4) or 1
+    float gs_out;             // gate_up: static global scale of the NVFP4 output or 1
+    int out_fmt;              // gate_up: format of hq
+    uint8_t* hq;              // gate_up output base for this class
+    uint8_t* hs;
+    int I;                    // gate_up: intermediate size of this class
+};
+
+struct GemmParams {
+    int mode;                 // 0 gate_up, 1 down
+    int M, k, E, H, Mpad;
+    GemmClass cls[2];
+    int has_shared;
+    const int32_t* perm;
+    const Group* groups;
+    const WsHeader* hdr;
+    float* y;                 // down output [P, H]
+    int32_t* counters;
+    float* partials;
+    int32_t* status;
+    int stages, stage_bytes, a_off, sfa_off, b_off, sfb_off, atoms_max;
+};
+
+struct FinalizeParams {
+    const float* y;           // [P, H]
+    const float* topk_w;      // [M, k]
+    const int32_t* inv_perm;  // [M*k + M]
+    uint16_t* residual;       // bf16 [M, H]
+    const uint16_t* gamma;
+    uint16_t* out;
+    uint8_t* outq;            // [M8, H] or null
+    uint8_t* outs;            // [M8, H/32]
+    int M, H, k, has_shared;
+    float eps;
+};
+
+struct PackParams {
+    const uint8_t* codes;
+    const uint8_t* scales;
+    uint8_t* dst;
+    int fmt, n_exp, rows, K, gate_up;  // gate_up: interleave gate/up halves per block
+    int I;                              // gate_up: intermediate size
+};
+
+}  // namespace moe

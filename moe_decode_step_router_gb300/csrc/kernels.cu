@@ -1,0 +1,473 @@
+// Router, route, finalize and packing kernels of the MoE step (sm_103a).
+//
+// Sources: "SGLang-NVIDIA-Mega" README, slot table of "What a covered DeepSeek-V4.1-Flash
+// step runs" (rows gate: one router per row, sigmoid top-k; moe: route kernel and 8-row
+// tiles; shared_ll: one-pass MXFP8 quant of the expert input into its row-tile layout;
+// hop_b: top-k finalize, shared-expert add, RMSNorm, next input's MXFP8 scales per 8-row
+// tile) and Qwen3.5 slot table (row route: router GEMM and NVFP4 quantisation of the MoE
+// input in one launch); "sgl-nvidia-mega pull request 24", "Modifications / Target spec"
+// (one expert group, sigmoid scores, renormalised top-k).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "quant.cuh"
+
+namespace moe {
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// ------------------------------------------------------------------------------------
+// FC1 input quantisation into the tiled layout. Unit = one scale block (MXFP8: 32
+// elements, NVFP4: 16) or one 16-byte chunk (BF16) of one padded row; rows >= M are zero.
+__device__ void quant_unit(const uint16_t* __restrict__ x, int M, int H, int Mpad, int fmt, float gs, uint8_t* xq,
+                           uint8_t* xs, int u) {
+    if (fmt == MOE_FMT_MXFP8) {
+        const int nb = H / 32, m = u / nb, bi = u % nb;
+        float v[32];
+        if (m < M) {
+            const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)m * H + 32 * bi);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint4 w = __ldg(src + i);
+                v[8 * i + 0] = bf16_lo(w.x); v[8 * i + 1] = bf16_hi(w.x);
+                v[8 * i + 2] = bf16_lo(w.y); v[8 * i + 3] = bf16_hi(w.y);
+                v[8 * i + 4] = bf16_lo(w.z); v[8 * i + 5] = bf16_hi(w.z);
+                v[8 * i + 6] = bf16_lo(w.w); v[8 * i + 7] = bf16_hi(w.w);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        const int e = mx_exponent(amax);
+        const float sc = exp2_int(-e);
+        uint32_t wd[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint32_t lo = e4m3x2(__fmul_rn(v[4 * i + 1], sc), __fmul_rn(v[4 * i + 0], sc));
+            uint32_t hi = e4m3x2(__fmul_rn(v[4 * i + 3], sc), __fmul_rn(v[4 * i + 2], sc));
+            wd[i] = lo | (hi << 16);
+        }
+        const int s = bi / 4, c0 = 2 * (bi % 4);
+        uint8_t* row = xq + (size_t)s * Mpad * kStepBytes + (size_t)m * kStepBytes;
+        *reinterpret_cast<uint4*>(row + ((c0 ^ (m & 7)) * 16)) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+        *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (m & 7)) * 16)) = make_uint4(wd[4], wd[5], wd[6], wd[7]);
+        xs[(size_t)s * kAtomBytes + (m % 32) * 16 + (m / 32) * 4 + (bi % 4)] = (uint8_t)(e + 127);
+    } else if (fmt == MOE_FMT_NVFP4) {
+        const int nb = H / 16, m = u / nb, bi = u % nb;
+        float v[16];
+        if (m < M) {
+            const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)m * H + 16 * bi);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                uint4 w = __ldg(src + i);
+                v[8 * i + 0] = bf16_lo(w.x); v[8 * i + 1] = bf16_hi(w.x);
+                v[8 * i + 2] = bf16_lo(w.y); v[8 * i + 3] = bf16_hi(w.y);
+                v[8 * i + 4] = bf16_lo(w.z); v[8 * i + 5] = bf16_hi(w.z);
+                v[8 * i + 6] = bf16_lo(w.w); v[8 * i + 7] = bf16_hi(w.w);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        const uint8_t s8 = nv_scale(amax, gs);
+        const float dsc = e4m3_to_f32(s8);
+        const float denom = __fmul_rn(dsc, gs);
+        uint32_t wd[2] = {0u, 0u};
+        if (dsc != 0.0f) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                uint32_t b = e2m1x2(__fdiv_rn(v[2 * i + 1], denom), __fdiv_rn(v[2 * i], denom));
+                wd[i / 4] |= b << (8 * (i % 4));
+            }
+        }
+        const int s = bi / 16, b16 = bi % 16, c = b16 / 2;
+        uint8_t* row = xq + (size_t)s * Mpad * kStepBytes + (size_t)m * kStepBytes;
+        *reinterpret_cast<uint2*>(row + ((c ^ (m & 7)) * 16) + (b16 % 2) * 8) = make_uint2(wd[0], wd[1]);
+        xs[(size_t)s * 4 * kAtomBytes + (b16 / 4) * kAtomBytes + (m % 32) * 16 + (m / 32) * 4 + (b16 % 4)] = s8;
+    } else {  // BF16: 16-byte chunks copied into the swizzled image
+        const int nc = H / 8, m = u / nc, ci = u % nc;
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (m < M) w = __ldg(reinterpret_cast<const uint4*>(x + (size_t)m * H + 8 * ci));
+        const int s = ci / 8, c = ci % 8;
+        uint8_t* row = xq + (size_t)s * Mpad * kStepBytes + (size_t)m * kStepBytes;
+        *reinterpret_cast<uint4*>(row + ((c ^ (m & 7)) * 16)) = w;
+    }
+}
+
+__device__ __forceinline__ int quant_units(int fmt, int Mpad, int H) {
+    return fmt == MOE_FMT_MXFP8 ? Mpad * (H / 32) : (fmt == MOE_FMT_NVFP4 ? Mpad * (H / 16) : Mpad * (H / 8));
+}
+
+// ------------------------------------------------------------------------------------
+// a1 (+a3): router GEMV with fp32 accumulation, the fp32 sigmoid score evaluated in
+// double and rounded once, and the FC1 input quantisation spread over the same grid.
+// CTA c owns experts [c*epc, (c+1)*epc); each of its 8 warps takes one (expert, row
+// quarter) and its lanes stride over H in 8-element vectors.
+constexpr int kRouterThreads = 256;
+
+__global__ void __launch_bounds__(kRouterThreads) k_router(RouterParams p) {
+    pdl_wait();
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int H = p.H, M = p.M, E = p.E;
+    const int Mpad = round_up(M, 16);
+    // quantisation (all CTAs share the units)
+    {
+        const int nthreads = gridDim.x * blockDim.x, tid = blockIdx.x * blockDim.x + threadIdx.x;
+        const int nr = quant_units(p.fmt_r, Mpad, H);
+        for (int u = tid; u < nr; u += nthreads) quant_unit(p.x, M, H, Mpad, p.fmt_r, p.gs_r, p.xq, p.xs, u);
+        if (p.quant_shared) {
+            const int ns = quant_units(p.fmt_s, Mpad, H);
+            for (int u = tid; u < ns; u += nthreads)
+                quant_unit(p.x, M, H, Mpad, p.fmt_s, p.gs_s, p.xq_sh, p.xs_sh, u);
+        }
+    }
+    // router logits for this CTA's experts
+    const int wpe = 8 / p.experts_per_cta;  // warps per expert
+    const int e = blockIdx.x * p.experts_per_cta + warp / wpe;
+    const int rq = warp % wpe;             // this warp's rows: m = rq, rq + wpe, ...
+    if (e < E) {
+        if (p.logits_in) {
+            for (int m = rq + wpe * lane; m < M; m += 32 * wpe) {
+                const float lg = p.logits_in[(size_t)m * E + e];
+                const float sc = (float)(1.0 / (1.0 + exp(-(double)lg)));
+                p.scores[(size_t)m * E + e] = sc;
+                if (p.logits_out) p.logits_out[(size_t)m * E + e] = lg;
+            }
+        } else {
+            const uint16_t* wrow = p.wg + (size_t)e * H;
+            for (int m0 = rq; m0 < M; m0 += 16 * wpe) {
+                float acc[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+                for (int h = 8 * lane; h < H; h += 256) {
+                    const uint4 w = __ldg(reinterpret_cast<const uint4*>(wrow + h));
+                    const float w0 = bf16_lo(w.x), w1 = bf16_hi(w.x), w2 = bf16_lo(w.y), w3 = bf16_hi(w.y);
+                    const float w4 = bf16_lo(w.z), w5 = bf16_hi(w.z), w6 = bf16_lo(w.w), w7 = bf16_hi(w.w);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int m = m0 + i * wpe;
+                        if (m < M) {
+                            const uint4 xv = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)m * H + h));
+                            float a = acc[i];
+                            a = fmaf(bf16_lo(xv.x), w0, a); a = fmaf(bf16_hi(xv.x), w1, a);
+                            a = fmaf(bf16_lo(xv.y), w2, a); a = fmaf(bf16_hi(xv.y), w3, a);
+                            a = fmaf(bf16_lo(xv.z), w4, a); a = fmaf(bf16_hi(xv.z), w5, a);
+                            a = fmaf(bf16_lo(xv.w), w6, a); a = fmaf(bf16_hi(xv.w), w7, a);
+                            acc[i] = a;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int m = m0 + i * wpe;
+                    const float lg = warp_sum(acc[i]);
+                    if (lane == (i & 31) && m < M) {
+                        const float sc = (float)(1.0 / (1.0 + exp(-(double)lg)));
+                        p.scores[(size_t)m * E + e] = sc;
+                        if (p.logits_out) p.logits_out[(size_t)m * E + e] = lg;
+                    }
+                }
+            }
+        }
+    }
+    pdl_trigger();
+}
+
+// ------------------------------------------------------------------------------------
+// a2 + a4 in one CTA: top-k of the selection key (score + bias) with ties to the lower
+// expert index, renormalised weights (double, rounded once), then the stable counting
+// sort of the (row, slot) pairs into 8-row tiles and the per-expert group table.
+constexpr int kRouteThreads = 1024;
+
+__device__ __forceinline__ void block_scan4(int4 v, int4* out_excl, int4* total, int4* sh_warp) {
+    // inclusive warp scan
+    const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+    int4 s = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int a = __shfl_up_sync(0xffffffffu, s.x, o), b = __shfl_up_sync(0xffffffffu, s.y, o);
+        int c = __shfl_up_sync(0xffffffffu, s.z, o), d = __shfl_up_sync(0xffffffffu, s.w, o);
+        if (lane >= o) { s.x += a; s.y += b; s.z += c; s.w += d; }
+    }
+    if (lane == 31) sh_warp[warp] = s;
+    __syncthreads();
+    if (warp == 0) {
+        int4 t = (lane < (int)(blockDim.x / 32)) ? sh_warp[lane] : make_int4(0, 0, 0, 0);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int a = __shfl_up_sync(0xffffffffu, t.x, o), b = __shfl_up_sync(0xffffffffu, t.y, o);
+            int c = __shfl_up_sync(0xffffffffu, t.z, o), d = __shfl_up_sync(0xffffffffu, t.w, o);
+            if (lane >= o) { t.x += a; t.y += b; t.z += c; t.w += d; }
+        }
+        sh_warp[lane] = t;  // inclusive over warps
+    }
+    __syncthreads();
+    int4 base = (warp > 0) ? sh_warp[warp - 1] : make_int4(0, 0, 0, 0);
+    *out_excl = make_int4(base.x + s.x - v.x, base.y + s.y - v.y, base.z + s.z - v.z, base.w + s.w - v.w);
+    *total = sh_warp[blockDim.x / 32 - 1];
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kRouteThreads) k_topk_route(TopkRouteParams p) {
+    __shared__ unsigned long long sel[kMaxE + 1];
+    __shared__ int4 sh_warp[32];
+    __shared__ int s_bad;
+    pdl_wait();
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int M = p.M, E = p.E, k = p.k;
+    if (p.do_topk) {
+        for (int m = warp; m < M; m += kRouteThreads / 32) {
+            float key[kMaxE / 32], sc[kMaxE / 32];
+#pragma unroll
+            for (int i = 0; i < kMaxE / 32; ++i) {
+                const int e = lane + 32 * i;
+                if (e < E) {
+                    sc[i] = p.scores[(size_t)m * E + e];
+                    key[i] = p.bias ? __fadd_rn(sc[i], p.bias[e]) : sc[i];
+                } else {
+                    sc[i] = 0.0f;
+                    key[i] = -INFINITY;
+                }
+            }
+            uint32_t taken = 0;
+            int my_idx = 0;
+            float my_sc = 0.0f;
+            double ssum = 0.0;
+            for (int j = 0; j < k; ++j) {
+                float bk = -INFINITY;
+                int bi = 0x7fffffff;
+#pragma unroll
+                for (int i = 0; i < kMaxE / 32; ++i) {
+                    const int e = lane + 32 * i;
+                    if (e < E && !((taken >> i) & 1u) && (key[i] > bk || bi == 0x7fffffff)) {
+                        bk = key[i];
+                        bi = e;
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
+                    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                    if (ok > bk || (ok == bk && oi < bi)) { bk = ok; bi = oi; }
+                }
+                float wsc = 0.0f;
+                if ((bi & 31) == lane) {
+                    taken |= 1u << (bi / 32);
+#pragma unroll
+                    for (int i = 0; i < kMaxE / 32; ++i)
+                        if (i == bi / 32) wsc = sc[i];
+                }
+                wsc = __shfl_sync(0xffffffffu, wsc, bi & 31);
+                ssum += (double)wsc;
+                if (lane == j) { my_idx = bi; my_sc = wsc; }
+            }
+            if (lane < k) {
+                p.topk_idx[(size_t)m * k + lane] = my_idx;
+                const double w = p.renormalize ? (double)my_sc / ssum * (double)p.rsf : (double)my_sc * (double)p.rsf;
+                p.topk_w[(size_t)m * k + lane] = (float)w;
+            }
+        }
+        __syncthreads();
+        __threadfence_block();
+    }
+    if (!p.do_route) {
+        pdl_trigger();
+        return;
+    }
+    // ---- route
+    const int P = M * k;
+    if (threadIdx.x == 0) s_bad = 0;
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) sel[e] = 0ull;
+    __syncthreads();
+    for (int q = threadIdx.x; q < P; q += blockDim.x) {
+        const int e = p.topk_idx[q];
+        if (e < 0 || e >= E) {
+            s_bad = 1;
+        } else {
+            atomicOr(&sel[e], 1ull << (q / k));
+        }
+    }
+    __syncthreads();
+    if (s_bad) {
+        if (threadIdx.x == 0) {
+            atomicCAS(&p.hdr->status, 0, (int)MOE_ERR_INVALID_ARG);
+            p.hdr->num_groups = 0;
+            p.hdr->num_tiles = 0;
+            *p.num_tiles = 0;
+        }
+        pdl_trigger();
+        return;
+    }
+    // one thread per expert (E + 1 <= 513 <= blockDim): pairs, tiles, group flag, padded rows
+    const int e = threadIdx.x;
+    int c = 0;
+    if (e < E) c = __popcll(sel[e]);
+    else if (e == E) c = p.has_shared ? M : 0;
+    int4 v = make_int4(c, (c + kTileRows - 1) / kTileRows, (e < E && c > 0) ? 1 : 0, (e < E) ? round_up(c, 16) : 0);
+    if (e > E) v = make_int4(0, 0, 0, 0);
+    int4 ex, tot;
+    block_scan4(v, &ex, &tot, sh_warp);
+    if (e <= E) {
+        p.counts[e] = c;
+        for (int t = 0; t < v.y; ++t) {
+            int32_t* tp = p.tiles + 3 * (ex.y + t);
+            tp[0] = e;
+            tp[1] = ex.x + kTileRows * t;
+            tp[2] = min(kTileRows, c - kTileRows * t);
+        }
+        if (v.z) p.groups[ex.z] = Group{e, c, ex.x, ex.w};
+    }
+    __shared__ int s_off[kMaxE + 1];
+    if (e <= E) s_off[e] = ex.x;
+    if (threadIdx.x == 0) {
+        *p.num_tiles = tot.y;
+        p.hdr->num_tiles = tot.y;
+        p.hdr->num_groups = tot.z;
+    }
+    __syncthreads();
+    for (int q = threadIdx.x; q < P; q += blockDim.x) {
+        const int ee = p.topk_idx[q], m = q / k;
+        const unsigned long long below = (m == 0) ? 0ull : (sel[ee] & ((1ull << m) - 1ull));
+        const int pos = s_off[ee] + __popcll(below);
+        p.perm[pos] = q;
+        p.inv_perm[q] = pos;
+    }
+    if (p.has_shared)
+        for (int m = threadIdx.x; m < M; m += blockDim.x) {
+            p.perm[P + m] = P + m;
+            p.inv_perm[P + m] = P + m;
+        }
+    pdl_trigger();
+}
+
+// ------------------------------------------------------------------------------------
+// a7: weighted combine in fixed slot order + shared row + residual (bf16) + RMSNorm,
+// optional MXFP8 of the output per 32 along H (rows M..round_up(M,8)-1 zero).
+constexpr int kFinThreads = 256;
+constexpr int kFinMaxPer = 8192 / kFinThreads;
+
+__global__ void __launch_bounds__(kFinThreads) k_finalize(FinalizeParams p) {
+    __shared__ float red[kFinThreads / 32];
+    pdl_wait();
+    const int m = blockIdx.x, H = p.H, k = p.k, M = p.M;
+    const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+    const int nper = H / kFinThreads;
+    if (m >= M) {
+        for (int n = threadIdx.x; n < H; n += kFinThreads) p.outq[(size_t)m * H + n] = 0;
+        for (int n = threadIdx.x; n < H / 32; n += kFinThreads) p.outs[(size_t)m * (H / 32) + n] = 0;
+        return;
+    }
+    const int P = M * k;
+    float hv[kFinMaxPer];
+    float ss = 0.0f;
+    int pos[kMaxK + 1];
+    float w[kMaxK];
+    for (int j = 0; j < k; ++j) {
+        pos[j] = p.inv_perm[m * k + j];
+        w[j] = p.topk_w[m * k + j];
+    }
+    const int pos_sh = p.has_shared ? p.inv_perm[P + m] : -1;
+#pragma unroll 4
+    for (int i = 0; i < nper; ++i) {
+        const int n = threadIdx.x + kFinThreads * i;
+        float acc = 0.0f;
+        for (int j = 0; j < k; ++j) acc = fmaf(w[j], __ldcg(p.y + (size_t)pos[j] * H + n), acc);
+        if (pos_sh >= 0) acc = __fadd_rn(acc, __ldcg(p.y + (size_t)pos_sh * H + n));
+        const float r = bf16f(p.residual[(size_t)m * H + n]);
+        const __nv_bfloat16 hb = __float2bfloat16_rn(__fadd_rn(r, acc));
+        p.residual[(size_t)m * H + n] = __bfloat16_as_ushort(hb);
+        const float hf = __bfloat162float(hb);
+        hv[i] = hf;
+        ss = fmaf(hf, hf, ss);
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    float tot = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kFinThreads / 32; ++i) tot += red[i];
+    const float rstd = rsqrtf(tot / (float)H + p.eps);
+#pragma unroll 4
+    for (int i = 0; i < nper; ++i) {
+        const int n = threadIdx.x + kFinThreads * i;
+        const float g = bf16f(p.gamma[n]);
+        const __nv_bfloat16 ob = __float2bfloat16_rn(hv[i] * rstd * g);
+        p.out[(size_t)m * H + n] = __bfloat16_as_ushort(ob);
+        if (p.outq) {
+            const float of = __bfloat162float(ob);
+            const float amax = warp_max(fabsf(of));  // lanes hold 32 consecutive n
+            const int e = mx_exponent(amax);
+            const uint8_t q = e4m3(__fmul_rn(of, exp2_int(-e)));
+            p.outq[(size_t)m * H + n] = q;
+            if (lane == 0) p.outs[(size_t)m * (H / 32) + n / 32] = (uint8_t)(e + 127);
+        }
+    }
+    pdl_trigger();
+}
+
+// ------------------------------------------------------------------------------------
+// Load-time repack of one projection into streaming records (see the ABI header).
+__global__ void k_pack(PackParams p) {
+    const int KS = steps_of(p.fmt, p.K), A = atoms_per_step(p.fmt), MB = p.rows / kBlockRows;
+    const size_t REC = record_bytes(p.fmt);
+    const int64_t rb = row_bytes(p.fmt, p.K), rs = row_scales(p.fmt, p.K);
+    const size_t nrec = (size_t)p.n_exp * MB * KS;
+    // work item: (record, row, 16-byte chunk) for codes and (record, row, atom) for scales
+    const size_t per_rec = (size_t)kBlockRows * 8 + (size_t)kBlockRows * A;
+    const size_t total = nrec * per_rec;
+    for (size_t w = blockIdx.x * (size_t)blockDim.x + threadIdx.x; w < total; w += (size_t)gridDim.x * blockDim.x) {
+        const size_t rec = w / per_rec;
+        const int item = (int)(w % per_rec);
+        const int s = (int)(rec % KS);
+        const int b = (int)((rec / KS) % MB);
+        const int e = (int)(rec / ((size_t)KS * MB));
+        int r, c = 0, a = 0;
+        const bool is_code = item < kBlockRows * 8;
+        if (is_code) {
+            r = item / 8;
+            c = item % 8;
+        } else {
+            r = (item - kBlockRows * 8) / A;
+            a = (item - kBlockRows * 8) % A;
+        }
+        int src_row;
+        if (p.gate_up) src_row = (r < 64) ? (64 * b + r) : (p.I + 64 * b + (r - 64));
+        else src_row = kBlockRows * b + r;
+        uint8_t* dst = p.dst + rec * REC;
+        if (is_code) {
+            const uint4 v = *reinterpret_cast<const uint4*>(p.codes + ((size_t)e * p.rows + src_row) * rb +
+                                                            (size_t)s * kStepBytes + 16 * c);
+            *reinterpret_cast<uint4*>(dst + r * kStepBytes + ((c ^ (r & 7)) * 16)) = v;
+        } else {
+            const uint8_t* sp = p.scales + ((size_t)e * p.rows + src_row) * rs + (size_t)s * 4 * A + 4 * a;
+            uint8_t* dp = dst + kBlockRows * kStepBytes + a * kAtomBytes + (r % 32) * 16 + (r / 32) * 4;
+            dp[0] = sp[0];
+            dp[1] = sp[1];
+            dp[2] = sp[2];
+            dp[3] = sp[3];
+        }
+    }
+}
+
+}  // namespace moe

@@ -1,0 +1,244 @@
+"""GPU parity of each stage of the step against the oracle, through the C ABI.
+
+Routing, route tiles and the FC1 input quantisation are compared bit for bit on the same
+fp32 logits; the expert GEMMs and the finalize within the step's tolerance. Shapes span
+several 128-row blocks, ragged row counts (1..64) and every format pairing the workloads
+use (MXFP8 + MXFP8, NVFP4 + BF16 shared, NVFP4 + MXFP8 shared).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_decode_step_router_gb300 import moestep as ms
+from moe_decode_step_router_gb300 import synth
+
+from gpu_util import (bf16_to_f64, check_output, expert_weights_for, host_weights, make, npy, oracle_layer, rel_l2,
+                      row_bytes, row_scales, u16, untile, untile_scales)
+
+pytestmark = pytest.mark.gpu
+
+SMALL = {
+    "mx_mx": synth.config("tiny_mxfp8", E=16, k=2, I=256, I_sh=256),
+    "mx_mx_bias": synth.config("tiny_mxfp8", E=32, k=8, I=512, I_sh=256, H=2048, has_bias=True, rsf=2.5),
+    "nv_bf16": synth.config("nvfp4_h6144_e256_k8_16rows", H=1024, E=16, k=4, I=256, I_sh=256),
+    "nv_mx": synth.config("nvfp4_h4096_e512_k10", H=1024, E=32, k=4, I=512, I_sh=256),
+}
+
+
+def _alloc(layer, M, dev="cuda"):
+    d, cfg = layer.d, layer.cfg
+    E, k, H = cfg["E"], cfg["k"], cfg["H"]
+    t = {}
+    t["logits"] = torch.zeros(M, E, dtype=torch.float32, device=dev)
+    t["idx"] = torch.zeros(M, k, dtype=torch.int32, device=dev)
+    t["w"] = torch.zeros(M, k, dtype=torch.float32, device=dev)
+    t["xq"] = torch.zeros(ms.moe_act_bytes(cfg["w_fmt"], M, H), dtype=torch.uint8, device=dev)
+    t["xs"] = torch.zeros(max(ms.moe_act_scale_bytes(cfg["w_fmt"], M, H), 16), dtype=torch.uint8, device=dev)
+    t["xq_sh"] = torch.zeros(ms.moe_act_bytes(cfg["sh_fmt"], M, H), dtype=torch.uint8, device=dev)
+    t["xs_sh"] = torch.zeros(max(ms.moe_act_scale_bytes(cfg["sh_fmt"], M, H), 16), dtype=torch.uint8, device=dev)
+    P = M * k + M
+    t["counts"] = torch.zeros(E + 1, dtype=torch.int32, device=dev)
+    t["perm"] = torch.zeros(P, dtype=torch.int32, device=dev)
+    t["inv"] = torch.zeros(P, dtype=torch.int32, device=dev)
+    t["tiles"] = torch.zeros(P + E + 1, 3, dtype=torch.int32, device=dev)
+    t["nt"] = torch.zeros(1, dtype=torch.int32, device=dev)
+    t["hq"] = torch.zeros(ms.moe_hq_bytes(d, M), dtype=torch.uint8, device=dev)
+    t["hs"] = torch.zeros(ms.moe_hq_scale_bytes(d, M), dtype=torch.uint8, device=dev)
+    t["y"] = torch.zeros(P, H, dtype=torch.float32, device=dev)
+    t["out"] = torch.zeros(M, H, dtype=torch.bfloat16, device=dev)
+    return t
+
+
+def _logits(M, E, seed):
+    g = np.random.default_rng(seed)
+    return (g.standard_normal((M, E)) * 2.0).astype(np.float32)
+
+
+def _hq_routed_bytes(cfg, M):
+    P = M * cfg["k"]
+    G = min(P, cfg["E"])
+    return -(-((P + 15 * G) * row_bytes(cfg["w_fmt"], cfg["I"])) // 256) * 256
+
+
+def _hs_routed_bytes(cfg, M):
+    P = M * cfg["k"]
+    G = min(P, cfg["E"])
+    f = cfg["w_fmt"]
+    KS = row_bytes(f, cfg["I"]) // 128
+    return -(-(G * KS * (1 if f == 1 else 4) * 512) // 256) * 256
+
+
+def _gpu_hidden(cfg, M, counts, hq, hs):
+    """Per routed expert: (codes, scales) of its group block; and the shared block."""
+    f, I = cfg["w_fmt"], cfg["I"]
+    rb = row_bytes(f, I)
+    KS = rb // 128
+    A = 1 if f == 1 else 4
+    out = {}
+    row_off = gi = 0
+    for e in range(cfg["E"]):
+        c = int(counts[e])
+        if c == 0:
+            continue
+        Rp = -(-c // 16) * 16
+        blk = hq[row_off * rb:(row_off + Rp) * rb]
+        sblk = hs[gi * KS * A * 512:(gi + 1) * KS * A * 512]
+        out[e] = (untile(blk, f, c, I, Rp), untile_scales(sblk, f, c, I))
+        row_off += Rp
+        gi += 1
+    fs, Is = cfg["sh_fmt"], cfg["I_sh"]
+    hb, sb = _hq_routed_bytes(cfg, M), _hs_routed_bytes(cfg, M)
+    sh_codes = untile(hq[hb:], fs, M, Is)
+    sh_sc = untile_scales(hs[sb:], fs, M, Is) if fs != 0 else None
+    return out, (sh_codes, sh_sc)
+
+
+def _cmp_hidden(fmt, got, ref, I, gs):
+    """Requantised FC2 inputs: nearly all codes equal; dequantised values close."""
+    gq, gsc = got
+    rq, rsc = ref
+    if fmt == 0:
+        g = bf16_to_f64(gq.view(np.uint16))
+        r = bf16_to_f64(rq.view(np.uint16))
+        assert rel_l2(g, r) < 2e-3
+        return
+    same = (gq == rq).mean()
+    assert same > 0.98, "only %.4f of hidden codes agree" % same
+    g = oracle.dequant(fmt, gq, gsc, I, gs)
+    r = oracle.dequant(fmt, rq, rsc, I, gs)
+    assert rel_l2(g, r) < (2e-2 if fmt == 2 else 5e-3)
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("M", [1, 5, 16, 37, 64])
+def test_stages_against_oracle(name, M):
+    cfg = SMALL[name]
+    inp, layer = make(cfg, seed=M, M=M)
+    d = layer.d
+    E, k, H, I = cfg["E"], cfg["k"], cfg["H"], cfg["I"]
+    L = oracle_layer(cfg, inp)
+    t = _alloc(layer, M)
+    li = _logits(M, E, 100 + M)
+    li_d = torch.from_numpy(li).cuda()
+    x16, wg16 = u16(inp["x"]), u16(inp["wg"])
+    bias = npy(inp["bias"])
+    # ---- a1..a3 with given logits: routing and quantisation bit-exact
+    ms.moe_router_topk(d, inp["x"], inp["wg"], inp["bias"], li_d, M, t["logits"], t["idx"], t["w"], t["xq"], t["xs"],
+                       t["xq_sh"], t["xs_sh"], layer.ws)
+    torch.cuda.synchronize()
+    _, _, oidx, ow, _ = oracle.router(L, x16, wg16, bias=bias, logits_in=li)
+    assert (npy(t["idx"]) == oidx).all()
+    assert (npy(t["w"]) == ow.astype(np.float32)).all()
+    fr, fs = cfg["w_fmt"], cfg["sh_fmt"]
+    gs_a1, gs_a2, gs_a1s, gs_a2s = inp["gs_a"]
+    oq, osc = oracle.quant_x(fr, x16, gs_a1)
+    assert (untile(npy(t["xq"]), fr, M, H) == oq).all()
+    assert (untile_scales(npy(t["xs"]), fr, M, H) == osc).all()
+    xq_sh, xs_sh = (t["xq"], t["xs"]) if fs == fr else (t["xq_sh"], t["xs_sh"])
+    oq_s, osc_s = oracle.quant_x(fs, x16, gs_a1s)
+    assert (untile(npy(xq_sh), fs, M, H) == oq_s).all()
+    if fs != 0:
+        assert (untile_scales(npy(xs_sh), fs, M, H) == osc_s).all()
+    # ---- a4 route: bit-exact
+    ms.moe_route_tiles(d, t["idx"], M, t["tiles"], t["nt"], t["perm"], t["inv"], t["counts"], layer.ws)
+    torch.cuda.synchronize()
+    counts, offsets, perm, inv, tiles = oracle.route(L, oidx)
+    assert (npy(t["counts"]) == counts).all()
+    assert (npy(t["perm"]) == perm).all() and (npy(t["inv"]) == inv).all()
+    nt = int(npy(t["nt"])[0])
+    assert nt == len(tiles) and (npy(t["tiles"])[:nt] == tiles).all()
+    # ---- a5 gate_up
+    ms.moe_expert_gate_up(d, layer.qw["w13"], layer.qw["sh13"], t["xq"], t["xs"], xq_sh, xs_sh, t["perm"], M,
+                          t["hq"], t["hs"], layer.ws)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    w13, w2, sh13, sh2 = host_weights(inp, E)
+    xdq = oracle.dequant(fr, oq, osc, H, gs_a1)
+    xdq_s = oracle.dequant(fs, oq_s, osc_s if fs else None, H, gs_a1s)
+    got_h, got_sh = _gpu_hidden(cfg, M, counts, npy(t["hq"]), npy(t["hs"]))
+    ref_y = {}
+    for e, (gq, gsc) in got_h.items():
+        rows = [perm[offsets[e] + r] for r in range(counts[e])]
+        rq, rs, ys = [], [], []
+        for p in rows:
+            hq, hs, _, y = oracle.expert_row(fr, H, I, w13[e], w2[e], xdq[p // k], gs_a2)
+            rq.append(hq)
+            rs.append(hs)
+            ref_y[p] = y
+        _cmp_hidden(fr, (gq, gsc), (np.stack(rq), np.stack(rs) if fr else None), I, gs_a2)
+    shq, shs = [], []
+    for m in range(M):
+        hq, hs, _, y = oracle.expert_row(fs, H, cfg["I_sh"], sh13, sh2, xdq_s[m], gs_a2s)
+        shq.append(hq)
+        shs.append(hs)
+        ref_y[M * k + m] = y
+    _cmp_hidden(fs, got_sh, (np.stack(shq), np.stack(shs) if fs else None), cfg["I_sh"], gs_a2s)
+    # ---- a6 down
+    ms.moe_expert_down(d, layer.qw["w2"], layer.qw["sh2"], t["hq"], t["hs"], M, t["y"], layer.ws)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    y = npy(t["y"])
+    for p, yr in ref_y.items():
+        assert rel_l2(y[inv[p]], yr) < (3e-2 if fr == 2 else 1e-2), (p, rel_l2(y[inv[p]], yr))
+    # ---- a7 finalize, and the whole step against the oracle's own step
+    res = inp["residual"].clone()
+    ms.moe_finalize_norm(d, t["y"], t["w"], t["inv"], M, res, inp["gamma"], t["out"], None, None, layer.ws)
+    torch.cuda.synchronize()
+    ref = oracle.step_rows(L, np.arange(M), x16, u16(inp["residual"]), u16(inp["gamma"]), wg16, bias, w13, w2, sh13,
+                           sh2, logits_in=li)
+    check_output(u16(t["out"]), ref["out"], "out")
+    check_output(u16(res), ref["res_out"], "residual")
+
+
+def test_router_gemv_logits_and_routing():
+    cfg = synth.config("tiny_mxfp8", E=64, k=6, H=4096, has_bias=True, rsf=2.5)
+    M = 33
+    inp, layer = make(cfg, seed=3, M=M)
+    t = _alloc(layer, M)
+    ms.moe_router_topk(layer.d, inp["x"], inp["wg"], inp["bias"], None, M, t["logits"], t["idx"], t["w"], t["xq"],
+                       t["xs"], t["xq_sh"], t["xs_sh"], layer.ws)
+    torch.cuda.synchronize()
+    L = oracle_layer(cfg, inp)
+    x16, wg16 = u16(inp["x"]), u16(inp["wg"])
+    ol, os_, oidx, ow, margin = oracle.router(L, x16, wg16, bias=npy(inp["bias"]))
+    # fp32 accumulation bound: H * 2^-24 * sum |x w| per logit
+    absdot = np.abs(bf16_to_f64(x16)) @ np.abs(bf16_to_f64(wg16)).T
+    err = np.abs(npy(t["logits"]).astype(np.float64) - ol)
+    assert (err <= cfg["H"] * 2 ** -24 * absdot + 1e-30).all()
+    ok_rows = margin >= 1e-5
+    assert ok_rows.mean() > 0.5
+    assert (npy(t["idx"])[ok_rows] == oidx[ok_rows]).all()
+
+
+@pytest.mark.parametrize("M,skew", [(1, False), (8, False), (48, True), (64, True)])
+def test_route_multi_tile_bitexact(M, skew):
+    cfg = synth.config("mxfp8_skew_48rows", H=1024, E=256, k=8, I=256, I_sh=256)
+    inp, layer = make(cfg, seed=1, M=M)
+    g = np.random.default_rng(M)
+    p = (np.arange(1, 257) ** -1.2) if skew else np.ones(256)
+    idx = np.stack([g.choice(256, 8, replace=False, p=p / p.sum()) for _ in range(M)]).astype(np.int32)
+    t = _alloc(layer, M)
+    ms.moe_route_tiles(layer.d, torch.from_numpy(idx).cuda(), M, t["tiles"], t["nt"], t["perm"], t["inv"],
+                       t["counts"], layer.ws)
+    torch.cuda.synchronize()
+    counts, offsets, perm, inv, tiles = oracle.route(oracle_layer(cfg, inp), idx)
+    assert (npy(t["counts"]) == counts).all() and (npy(t["perm"]) == perm).all()
+    assert (npy(t["inv"]) == inv).all()
+    nt = int(npy(t["nt"])[0])
+    assert nt == len(tiles) and (npy(t["tiles"])[:nt] == tiles).all()
+    if skew:
+        assert (tiles[:, 2] == 8).any() and (counts[:256] > 8).any()
+
+
+def test_route_rejects_out_of_range_expert_ids():
+    cfg = synth.config("tiny_mxfp8")
+    inp, layer = make(cfg, seed=0, M=4)
+    t = _alloc(layer, 4)
+    idx = torch.tensor([[0, 1], [2, 16], [3, 4], [5, 6]], dtype=torch.int32, device="cuda")
+    t["nt"].fill_(-1)
+    ms.moe_route_tiles(layer.d, idx, 4, t["tiles"], t["nt"], t["perm"], t["inv"], t["counts"], layer.ws)
+    assert layer.status() == ms.MOE_ERR_INVALID_ARG
+    assert int(npy(t["nt"])[0]) == 0
+    ms.moe_workspace_init(layer.d, layer.ws)
+    assert layer.status() == 0

@@ -1,0 +1,140 @@
+"""End-to-end moe_step (five PDL-chained launches) against the oracle, in eager mode and
+under CUDA-graph replay; bitwise determinism over repeated replays; row-map invariance;
+and the full-size workloads, checked on rows the oracle computes one by one."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_decode_step_router_gb300 import synth
+
+from gpu_util import check_output, expert_weights_for, host_weights, make, npy, oracle_layer, u16
+
+pytestmark = pytest.mark.gpu
+
+SMALL = {
+    "mx_mx": synth.config("tiny_mxfp8", E=16, k=2, I=256, I_sh=256, emit_next=True),
+    "mx_bias": synth.config("tiny_mxfp8", H=2048, E=64, k=8, I=512, I_sh=512, has_bias=True, rsf=2.5),
+    "nv_bf16": synth.config("nvfp4_h6144_e256_k8_16rows", H=1024, E=16, k=4, I=256, I_sh=256),
+    "nv_mx": synth.config("nvfp4_h4096_e512_k10", H=1024, E=32, k=4, I=512, I_sh=256, emit_next=True),
+}
+
+
+def _outputs(cfg, M, dev="cuda"):
+    H = cfg["H"]
+    out = torch.zeros(M, H, dtype=torch.bfloat16, device=dev)
+    M8 = -(-M // 8) * 8
+    oq = torch.zeros(M8, H, dtype=torch.uint8, device=dev) if cfg.get("emit_next") else None
+    os_ = torch.zeros(M8, H // 32, dtype=torch.uint8, device=dev) if cfg.get("emit_next") else None
+    return out, oq, os_
+
+
+def _run(layer, inp, M):
+    out, oq, os_ = _outputs(layer.cfg, M)
+    res = inp["residual"].clone()
+    layer.step(inp["x"], res, out, oq, os_)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    return out, res, oq, os_
+
+
+def _oracle_rows(cfg, inp, rows):
+    L = oracle_layer(cfg, inp)
+    x16, wg16 = u16(inp["x"]), u16(inp["wg"])
+    bias = npy(inp["bias"])
+    sel = []
+    _, _, idx, _, _ = oracle.router(L, x16[rows], wg16, bias=bias)
+    w13, w2 = expert_weights_for(inp, idx.ravel())
+    _, _, sh13, sh2 = host_weights(dict(inp, w13=inp["w13"], w2=inp["w2"]), 0)
+    return oracle.step_rows(L, np.asarray(rows), x16, u16(inp["residual"]), u16(inp["gamma"]), wg16, bias, w13, w2,
+                            sh13, sh2, want_q=bool(cfg.get("emit_next")))
+
+
+def _check_rows(layer, inp, rows, out, res, oq, os_, ref):
+    M = out.shape[0]
+    idx = layer.ws_tensor("topk_idx", torch.int32, (M, layer.cfg["k"]))
+    gidx = npy(idx)[rows]
+    ok = (ref["margin"] >= 1e-5)
+    assert (gidx[ok] == ref["topk_idx"][ok]).all(), "routing differs on rows with a clear margin"
+    keep = ok | (gidx == ref["topk_idx"]).all(1)
+    if keep.any():
+        check_output(u16(out)[rows][keep], ref["out"][keep], "out")
+        check_output(u16(res)[rows][keep], ref["res_out"][keep], "residual")
+        if oq is not None:
+            q, s = npy(oq)[rows][keep], npy(os_)[rows][keep]
+            eq = (q == ref["outq"][keep]).mean()
+            assert eq > 0.95, "next-layer MXFP8 codes agree on only %.3f" % eq
+            assert (np.abs(s.astype(int) - ref["outs"][keep].astype(int)) <= 1).all()
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("M", [1, 8, 23, 64])
+def test_step_matches_oracle(name, M):
+    cfg = SMALL[name]
+    inp, layer = make(cfg, seed=10 + M, M=M)
+    out, res, oq, os_ = _run(layer, inp, M)
+    rows = list(range(M))
+    ref = _oracle_rows(cfg, inp, rows)
+    _check_rows(layer, inp, rows, out, res, oq, os_, ref)
+    if oq is not None:  # padding rows of the 8-row tiles are zero
+        assert (npy(oq)[M:] == 0).all() and (npy(os_)[M:] == 0).all()
+
+
+def test_graph_replay_equals_eager_and_is_deterministic():
+    cfg = SMALL["nv_mx"]
+    M = 19
+    inp, layer = make(cfg, seed=5, M=M)
+    out_e, res_e, oq_e, os_e = _run(layer, inp, M)
+    out, oq, os_ = _outputs(cfg, M)
+    res = inp["residual"].clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        layer.step(inp["x"], res, out, oq, os_)
+    first = None
+    for i in range(50):
+        res.copy_(inp["residual"])
+        g.replay()
+        torch.cuda.synchronize()
+        cur = (u16(out).tobytes(), u16(res).tobytes(), npy(oq).tobytes())
+        if first is None:
+            first = cur
+            assert cur[0] == u16(out_e).tobytes() and cur[1] == u16(res_e).tobytes()
+        assert cur == first, "replay %d differs" % i
+    assert layer.status() == 0
+
+
+def test_row_map_invariance():
+    cfg = SMALL["mx_bias"]
+    M = 24
+    inp, layer = make(cfg, seed=9, M=M)
+    out1, res1, _, _ = _run(layer, inp, M)
+    p = torch.randperm(M, generator=torch.Generator().manual_seed(1))
+    inp2 = dict(inp, x=inp["x"][p].contiguous(), residual=inp["residual"][p].contiguous())
+    out2, res2, _, _ = _run(layer, inp2, M)
+    assert torch.equal(out1[p], out2) and torch.equal(res1[p], res2)
+
+
+FULL = [("tiny_mxfp8", None), ("mxfp8_h7168_e256_k8_8rows", None), ("nvfp4_h6144_e256_k8_16rows", None),
+        ("mxfp8_skew_48rows", None), ("nvfp4_h4096_e512_k10", 1), ("nvfp4_h4096_e512_k10", 8),
+        ("nvfp4_h4096_e512_k10", 64)]
+
+
+@pytest.mark.parametrize("name,M", FULL, ids=["%s-%s" % (n, m) for n, m in FULL])
+def test_full_size_sampled_rows(name, M):
+    cfg = synth.config(name) if M is None else synth.config(name, M=M)
+    M = cfg["M"]
+    inp, layer = make(cfg, seed=0, M=M)
+    out, res, oq, os_ = _run(layer, inp, M)
+    rows = sorted({0, M - 1, M // 2})
+    ref = _oracle_rows(cfg, inp, rows)
+    _check_rows(layer, inp, rows, out, res, oq, os_, ref)
+    # routing of every row vs the oracle on the GPU's own logits is checked in the stage tests;
+    # here: every row's output is finite and the skewed workload has hot experts with several tiles
+    assert torch.isfinite(out.float()).all()
+    if cfg.get("skew"):
+        counts = npy(layer.ws_tensor("expert_counts", torch.int32, (cfg["E"] + 1,)))
+        assert (counts[:cfg["E"]] > 8).any()
+        idle = (counts[:cfg["E"]] == 0).mean()
+        assert 0.25 < idle < 0.55
