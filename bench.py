@@ -34,6 +34,7 @@ def _args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default=HEADLINE)
     ap.add_argument("--rows", type=int, default=None)
+    ap.add_argument("--experts", type=int, default=None, help="override E (smaller profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
     return ap.parse_args()
@@ -92,6 +93,16 @@ class Clocks:
                 "samples": len(sm)}
 
 
+def _cfg(a):
+    from moe_decode_step_router_gb300 import synth
+    over = {}
+    if a.rows is not None:
+        over["M"] = a.rows
+    if a.experts is not None:
+        over["E"] = a.experts
+    return synth.config(a.config, **over)
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -142,7 +153,7 @@ def _reference_arm(a):
     ws, rank, _ = _dist()
     if rank != 0:
         return 0
-    cfg = synth.config(a.config) if a.rows is None else synth.config(a.config, M=a.rows)
+    cfg = _cfg(a)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = synth.make_inputs(cfg, a.seed, device=dev)
     import numpy as np
@@ -191,7 +202,7 @@ def main():
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
-    cfg = synth.config(a.config) if a.rows is None else synth.config(a.config, M=a.rows)
+    cfg = _cfg(a)
     M, H = cfg["M"], cfg["H"]
     inp = synth.make_inputs(cfg, a.seed, device=dev)
     layer = MoELayer(cfg, inp, dev)

@@ -148,6 +148,8 @@ WsLayout layout(const moe_layer_desc* d) {
     L.cnt_gu = take(4ull * L.U_gu);
     L.cnt_dn = take(4ull * L.U_dn);
     L.partials = take(4ull * kMaxGemmCtas * 2 * kPartialFloats);
+    L.rpart = take(4ull * ((d->H + 511) / 512) * d->E * kMaxRows);
+    L.rcnt = take(4ull * ((d->E + 7) / 8));
     L.total = o;
     return L;
 }
@@ -155,6 +157,7 @@ WsLayout layout(const moe_layer_desc* d) {
 struct DevInfo {
     int dev = -1, sms = 0, smem_optin = 0;
     bool gemm_attr_set = false;
+    bool router_attr_set = false;
 };
 thread_local DevInfo g_dev;
 
@@ -203,9 +206,9 @@ moe_status launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_
 }
 
 // ------------------------------------------------------------------ launch helpers
-moe_status launch_router(const moe_layer_desc* d, const void* x, const void* w_gate, const float* logits_in, int M,
-                         float* logits_out, float* scores, void* xq, void* xs, void* xq_sh, void* xs_sh,
-                         cudaStream_t st) {
+moe_status launch_router(const moe_layer_desc* d, const WsLayout& L, uint8_t* ws, const void* x,
+                         const void* w_gate, const float* logits_in, int M, float* logits_out, float* scores,
+                         void* xq, void* xs, void* xq_sh, void* xs_sh, cudaStream_t st) {
     RouterParams p{};
     p.x = static_cast<const uint16_t*>(x);
     p.wg = static_cast<const uint16_t*>(w_gate);
@@ -215,9 +218,8 @@ moe_status launch_router(const moe_layer_desc* d, const void* x, const void* w_g
     p.M = M;
     p.H = d->H;
     p.E = d->E;
-    int epc = d->E / 128;
-    epc = epc >= 8 ? 8 : (epc >= 4 ? 4 : (epc >= 2 ? 2 : 1));
-    p.experts_per_cta = epc;
+    p.part = reinterpret_cast<float*>(ws + L.rpart);
+    p.counters = reinterpret_cast<int32_t*>(ws + L.rcnt);
     p.fmt_r = d->w_fmt;
     p.fmt_s = shared_fmt_of(d);
     p.quant_shared = separate_shared_input(d) ? 1 : 0;
@@ -227,8 +229,19 @@ moe_status launch_router(const moe_layer_desc* d, const void* x, const void* w_g
     p.xs_sh = static_cast<uint8_t*>(xs_sh);
     p.gs_r = d->w_fmt == MOE_FMT_NVFP4 ? d->gs_a1 : 1.0f;
     p.gs_s = (d->has_shared && d->shared_fmt == MOE_FMT_NVFP4) ? d->gs_a1_shared : 1.0f;
-    const int grid = (d->E + epc - 1) / epc;
-    return launch_pdl(k_router, dim3(grid), dim3(256), 0, st, p, "k_router launch");
+    const int nslices = logits_in ? 1 : (d->H + 511) / 512;
+    const int nblocks = (d->E + 7) / 8;
+    const size_t smem = logits_in ? 0 : (size_t)(M + 8) * (512 + 8) * 2;
+    DevInfo* di;
+    moe_status s = dev_info(&di);
+    if (s != MOE_OK) return s;
+    if (!di->router_attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(k_router, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (kMaxRows + 8) * (512 + 8) * 2);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(k_router)");
+        di->router_attr_set = true;
+    }
+    return launch_pdl(k_router, dim3(nslices, nblocks), dim3(256), smem, st, p, "k_router launch");
 }
 
 moe_status launch_topk_route(const moe_layer_desc* d, const WsLayout& L, uint8_t* ws, int M, const float* scores,
@@ -324,19 +337,22 @@ moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* wr,
     const int am = atoms_per_step(p.cls[0].fmt) > atoms_per_step(p.cls[1].fmt) ? atoms_per_step(p.cls[0].fmt)
                                                                                 : atoms_per_step(p.cls[1].fmt);
     p.atoms_max = am;
+    // NVFP4 stages carry 8 scale copies; issuing them from two extra warps keeps the MMA
+    // thread's issue stream short. MXFP8-only launches copy in the MMA thread (one hop less).
+    p.sf_warps = am == 4 ? 1 : 0;
     p.a_off = 0;
     p.sfa_off = kBlockRows * kStepBytes;
     p.b_off = round_up(p.sfa_off + am * kAtomBytes, 1024);
     p.sfb_off = p.b_off + p.Mpad * kStepBytes;
     p.stage_bytes = round_up(p.sfb_off + am * kAtomBytes, 1024);
-    const int fixed = 1024 + p.Mpad * kBlockRows * 4 + 256;
-    int S = (di->smem_optin - fixed) / (p.stage_bytes + 16);
+    const int fixed = 1024 + p.Mpad * kBlockRows * 4 + 512;
+    int S = (di->smem_optin - fixed) / (p.stage_bytes + 24);  // + full/empty/ready barriers
     const int tmem_cap = am ? (512 - 2 * 64) / (8 * am) : 16;
     if (S > tmem_cap) S = tmem_cap;
     if (S > 16) S = 16;
     if (S < 2) return fail(MOE_ERR_UNSUPPORTED, "not enough shared memory for the GEMM pipeline");
     p.stages = S;
-    const size_t smem = (size_t)fixed + (size_t)S * p.stage_bytes + 16 * S;
+    const size_t smem = (size_t)fixed + (size_t)S * p.stage_bytes + 24 * S;
     if (!di->gemm_attr_set) {
         cudaError_t e = cudaFuncSetAttribute(k_expert_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              di->smem_optin);
@@ -345,7 +361,7 @@ moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* wr,
     }
     int grid = di->sms;
     if (grid > kMaxGemmCtas) grid = kMaxGemmCtas;
-    return launch_pdl(k_expert_gemm, dim3(grid), dim3(192), smem, st, p,
+    return launch_pdl(k_expert_gemm, dim3(grid), dim3(256), smem, st, p,
                       mode == 0 ? "k_expert_gemm(gate_up) launch" : "k_expert_gemm(down) launch");
 }
 
@@ -366,8 +382,24 @@ moe_status launch_finalize(const moe_layer_desc* d, const float* y, const float*
     p.k = d->k;
     p.has_shared = d->has_shared;
     p.eps = d->rms_eps;
-    const int grid = outq ? round_up(M, 8) : M;
-    return launch_pdl(k_finalize, dim3(grid), dim3(256), 0, st, p, "k_finalize launch");
+    const int rows = outq ? round_up(M, 8) : M;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(8, rows);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 8;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_finalize, p);
+    if (e != cudaSuccess) return cuda_fail(e, "k_finalize launch");
+    return MOE_OK;
 }
 
 moe_status check_qweight(const moe_qweight* w, int fmt, const char* name) {
@@ -508,7 +540,8 @@ moe_status moe_router_topk(const moe_layer_desc* d, const void* x, const void* w
     uint8_t* w = static_cast<uint8_t*>(ws);
     float* scores = reinterpret_cast<float*>(w + L.scores);
     cudaStream_t st = (cudaStream_t)stream;
-    s = launch_router(d, x, w_gate, logits_in, M, logits_out, scores, xq, xq_scales, xq_sh, xq_sh_scales, st);
+    s = launch_router(d, L, w, x, w_gate, logits_in, M, logits_out, scores, xq, xq_scales, xq_sh, xq_sh_scales,
+                      st);
     if (s != MOE_OK) return s;
     s = launch_topk_route(d, L, w, M, scores, bias, topk_idx, topk_w, 1, 0, nullptr, nullptr, nullptr, nullptr,
                           nullptr, st);
@@ -643,8 +676,8 @@ moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void
     float* topk_w = reinterpret_cast<float*>(w + L.topk_w);
     int32_t* perm = reinterpret_cast<int32_t*>(w + L.perm);
     int32_t* inv_perm = reinterpret_cast<int32_t*>(w + L.inv_perm);
-    s = launch_router(d, a->x, a->w_gate, nullptr, M, logits, scores, w + L.xq, w + L.xs, w + L.xq_sh, w + L.xs_sh,
-                      st);
+    s = launch_router(d, L, w, a->x, a->w_gate, nullptr, M, logits, scores, w + L.xq, w + L.xs, w + L.xq_sh,
+                      w + L.xs_sh, st);
     if (s != MOE_OK) return s;
     s = launch_topk_route(d, L, w, M, scores, a->bias, topk_idx, topk_w, 1, 1,
                           reinterpret_cast<int32_t*>(w + L.counts), perm, inv_perm,

@@ -15,10 +15,11 @@
 // by the last CTA to finish a piece, in piece order (deterministic).
 //
 // Roles: warp 0 lane 0 issues the bulk copies (weight record + activation tile + its
-// scales) into a ring of shared-memory stages; warp 1 lane 0 copies the scales to tensor
-// memory and issues the MMAs into one of two TMEM accumulators; warps 2..5 drain the
-// accumulator and run the epilogue (gate_up: SwiGLU + requantisation into the tiled FC2
-// input; down: fp32 rows in perm order).
+// scales) into a ring of shared-memory stages; in launches with NVFP4 weights warps 6
+// and 7 copy each stage's A and B block scales into tensor memory (otherwise the MMA
+// thread does it); warp 1 lane 0 issues the MMAs into one of two TMEM
+// accumulators; warps 2..5 drain the accumulator and run the epilogue (gate_up: SwiGLU
+// + requantisation into the tiled FC2 input; down: fp32 rows in perm order).
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -27,7 +28,7 @@
 
 namespace moe {
 
-constexpr int kGemmThreads = 192;
+constexpr int kGemmThreads = 256;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint32_t kTmemCols = 512;
 constexpr int kAccCols = 64;
@@ -99,6 +100,8 @@ struct GemmSmem {
     uint64_t* acc_full;
     uint64_t* acc_empty;
     uint64_t* drain;
+    uint64_t* sf_ready;  // [S] scale factors of the stage are in tensor memory
+    uint64_t* sf_drain;
     uint32_t* tmem_base;
     int* abort_flag;
     int* bcast;
@@ -135,6 +138,59 @@ __device__ __forceinline__ void seg_group(const GemmParams& p, const Seg& s, int
     }
 }
 
+// Issues the MMAs of one segment from the single MMA thread. At small N the issue stream
+// of that thread, not the tensor pipe, limits the rate, so the scale-factor copies run
+// on their own warp and every descriptor is precomputed and advanced with integer adds
+// (a shared-memory descriptor holds address >> 4 in its low 14 bits: +16 bytes is +1);
+// the format branch is taken once per segment.
+template <int FMT, bool CP>
+__device__ __forceinline__ bool mma_segment(uint32_t ready0, uint32_t empty0, int& st, uint32_t& ph, int S, int ka,
+                                            int kb, uint64_t adesc0, uint64_t bdesc0, uint64_t sfadesc0,
+                                            uint64_t sfbdesc0, uint32_t stage16, uint32_t d_tmem, uint32_t sf_t0,
+                                            uint32_t sf_stride, uint32_t sfb_cols, uint32_t N, volatile int* abort) {
+    uint32_t id[4];
+#pragma unroll
+    for (int sub = 0; sub < 4; ++sub)
+        id[sub] = FMT == MOE_FMT_MXFP8 ? idesc_mxf8(N, sub) : (FMT == MOE_FMT_NVFP4 ? idesc_nvf4(N) : idesc_bf16(N));
+    for (int kk = ka; kk < kb; ++kk) {
+        if (!mbar_wait_bounded(ready0 + 8u * st, ph, abort, kWaitLimitNs)) return false;
+        tc_fence_after();
+        const uint64_t so = (uint64_t)st * stage16;
+        const uint64_t ad = adesc0 + so, bd = bdesc0 + so;
+        const uint32_t sfa = sf_t0 + (uint32_t)st * sf_stride, sfb = sfa + sfb_cols;
+        const uint32_t acc0 = kk > ka ? 1u : 0u;
+        if (FMT == MOE_FMT_MXFP8) {
+            if (CP) {
+                tc_cp_sf(sfa, sfadesc0 + so);
+                tc_cp_sf(sfb, sfbdesc0 + so);
+            }
+#pragma unroll
+            for (int sub = 0; sub < 4; ++sub)
+                mma_mxf8(d_tmem, ad + 2 * sub, bd + 2 * sub, id[sub], sfa, sfb, sub ? 1u : acc0);
+        } else if (FMT == MOE_FMT_NVFP4) {
+            if (CP) {
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    tc_cp_sf(sfa + 4 * a, sfadesc0 + so + 32 * a);
+                    tc_cp_sf(sfb + 4 * a, sfbdesc0 + so + 32 * a);
+                }
+            }
+#pragma unroll
+            for (int sub = 0; sub < 4; ++sub)
+                mma_nvf4(d_tmem, ad + 2 * sub, bd + 2 * sub, id[sub], sfa + 4 * sub, sfb + 4 * sub, sub ? 1u : acc0);
+        } else {
+#pragma unroll
+            for (int sub = 0; sub < 4; ++sub) mma_bf16(d_tmem, ad + 2 * sub, bd + 2 * sub, id[sub], sub ? 1u : acc0);
+        }
+        tc_commit(empty0 + 8u * st);
+        if (++st == S) {
+            st = 0;
+            ph ^= 1u;
+        }
+    }
+    return true;
+}
+
 __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_constant__ GemmParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -151,7 +207,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
     sm.acc_full = sm.empty + S;
     sm.acc_empty = sm.acc_full + 2;
     sm.drain = sm.acc_empty + 2;
-    sm.tmem_base = reinterpret_cast<uint32_t*>(sm.drain + 1);
+    sm.sf_ready = sm.drain + 1;
+    sm.sf_drain = sm.sf_ready + S;
+    sm.tmem_base = reinterpret_cast<uint32_t*>(sm.sf_drain + 2);
     sm.abort_flag = reinterpret_cast<int*>(sm.tmem_base + 1);
     sm.bcast = sm.abort_flag + 1;
     sm.never = sm.abort_flag + 2;
@@ -166,6 +224,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             mbar_init(smem_u32(&sm.acc_empty[i]), 4);
         }
         mbar_init(smem_u32(sm.drain), 1);
+        for (int i = 0; i < S; ++i) mbar_init(smem_u32(&sm.sf_ready[i]), 2);
+        mbar_init(smem_u32(&sm.sf_drain[0]), 1);
+        mbar_init(smem_u32(&sm.sf_drain[1]), 1);
         *sm.abort_flag = 0;
         *sm.never = 0;
         fence_mbar_init();
@@ -257,6 +318,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             uint32_t acc_ph[2] = {0u, 0u};
             bool ok = true;
             const int am = p.atoms_max;
+            // with copy warps the MMA thread waits for the stage's scales, else for its data
+            const uint32_t wait0 = p.sf_warps ? smem_u32(&sm.sf_ready[0]) : smem_u32(&sm.full[0]);
+            const uint32_t empty0 = smem_u32(&sm.empty[0]);
+            const uint32_t ring = smem_u32(sm.ring);
+            const uint64_t adesc0 = smem_desc(ring + p.a_off, 16, 1024, 2);
+            const uint64_t bdesc0 = smem_desc(ring + p.b_off, 16, 1024, 2);
+            const uint64_t sfadesc0 = smem_desc(ring + p.sfa_off, 0, 128, 0);
+            const uint64_t sfbdesc0 = smem_desc(ring + p.sfb_off, 0, 128, 0);
+            const uint32_t stage16 = (uint32_t)p.stage_bytes >> 4;
+            const uint32_t sf_t0 = tmem + 2 * kAccCols;
             while (ok && wk.next(s)) {
                 const GemmClass& C = p.cls[s.cls];
                 int expert, rows, perm_off, row_off, gidx;
@@ -268,49 +339,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + (uint32_t)(ab * kAccCols);
-                for (int kk = s.ka; kk < s.kb; ++kk) {
-                    if (!mbar_wait_bounded(smem_u32(&sm.full[st]), ph, abort_flag, kWaitLimitNs)) {
-                        set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    uint8_t* stage = sm.ring + (size_t)st * p.stage_bytes;
-                    const uint32_t a_s = smem_u32(stage + p.a_off), b_s = smem_u32(stage + p.b_off);
-                    const uint32_t sfa_t = tmem + 2 * kAccCols + (uint32_t)st * 8 * am;
-                    const uint32_t sfb_t = sfa_t + 4 * am;
-                    if (C.fmt == MOE_FMT_MXFP8) {
-                        tc_cp_sf(sfa_t, smem_desc(smem_u32(stage + p.sfa_off), 0, 128, 0));
-                        tc_cp_sf(sfb_t, smem_desc(smem_u32(stage + p.sfb_off), 0, 128, 0));
-#pragma unroll
-                        for (int sub = 0; sub < 4; ++sub) {
-                            mma_mxf8(d_tmem, smem_desc(a_s + 32 * sub, 16, 1024, 2), smem_desc(b_s + 32 * sub, 16, 1024, 2),
-                                     idesc_mxf8(N, sub), sfa_t, sfb_t, (kk > s.ka || sub > 0) ? 1u : 0u);
-                        }
-                    } else if (C.fmt == MOE_FMT_NVFP4) {
-#pragma unroll
-                        for (int a = 0; a < 4; ++a) {
-                            tc_cp_sf(sfa_t + 4 * a, smem_desc(smem_u32(stage + p.sfa_off + a * kAtomBytes), 0, 128, 0));
-                            tc_cp_sf(sfb_t + 4 * a, smem_desc(smem_u32(stage + p.sfb_off + a * kAtomBytes), 0, 128, 0));
-                        }
-#pragma unroll
-                        for (int sub = 0; sub < 4; ++sub) {
-                            mma_nvf4(d_tmem, smem_desc(a_s + 32 * sub, 16, 1024, 2), smem_desc(b_s + 32 * sub, 16, 1024, 2),
-                                     idesc_nvf4(N), sfa_t + 4 * sub, sfb_t + 4 * sub, (kk > s.ka || sub > 0) ? 1u : 0u);
-                        }
-                    } else {
-#pragma unroll
-                        for (int sub = 0; sub < 4; ++sub) {
-                            mma_bf16(d_tmem, smem_desc(a_s + 32 * sub, 16, 1024, 2), smem_desc(b_s + 32 * sub, 16, 1024, 2),
-                                     idesc_bf16(N), (kk > s.ka || sub > 0) ? 1u : 0u);
-                        }
-                    }
-                    tc_commit(smem_u32(&sm.empty[st]));
-                    if (++st == S) {
-                        st = 0;
-                        ph ^= 1u;
-                    }
+#define MOE_SEG(F, CPV)                                                                                   \
+    mma_segment<F, CPV>(wait0, empty0, st, ph, S, s.ka, s.kb, adesc0, bdesc0, sfadesc0, sfbdesc0, stage16, d_tmem, \
+                        sf_t0, 8 * am, 4 * am, N, abort_flag)
+                if (p.sf_warps) {
+                    if (C.fmt == MOE_FMT_MXFP8) ok = MOE_SEG(MOE_FMT_MXFP8, false);
+                    else if (C.fmt == MOE_FMT_NVFP4) ok = MOE_SEG(MOE_FMT_NVFP4, false);
+                    else ok = MOE_SEG(MOE_FMT_BF16, false);
+                } else {
+                    if (C.fmt == MOE_FMT_MXFP8) ok = MOE_SEG(MOE_FMT_MXFP8, true);
+                    else if (C.fmt == MOE_FMT_NVFP4) ok = MOE_SEG(MOE_FMT_NVFP4, true);
+                    else ok = MOE_SEG(MOE_FMT_BF16, true);
                 }
+#undef MOE_SEG
+                if (!ok) set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
                 if (!ok) break;
                 tc_commit(smem_u32(&sm.acc_full[ab]));
                 acc_ph[ab] ^= 1u;
@@ -319,6 +361,55 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             // wait until every issued MMA has completed before the TMEM is released
             tc_commit(smem_u32(sm.drain));
             mbar_wait_bounded(smem_u32(sm.drain), 0u, sm.never, kWaitLimitNs / 2);
+        }
+    } else if (warp >= 6) {
+        // ================================================================ scale-factor copies
+        // (launches with NVFP4 weights): warp 6 copies the A scales, warp 7 the B scales
+        if (lane == 0 && p.sf_warps) {
+            const bool is_b = warp == 7;
+            Walker wk;
+            wk.init(p, ngroups, G, c);
+            Seg s;
+            int st = 0;
+            uint32_t ph = 0;
+            const int am = p.atoms_max;
+            const uint32_t full0 = smem_u32(&sm.full[0]), ready0 = smem_u32(&sm.sf_ready[0]);
+            const uint32_t ring = smem_u32(sm.ring);
+            const uint64_t sfadesc0 = smem_desc(ring + p.sfa_off, 0, 128, 0);
+            const uint64_t sfbdesc0 = smem_desc(ring + p.sfb_off, 0, 128, 0);
+            const uint32_t stage16 = (uint32_t)p.stage_bytes >> 4;
+            const uint32_t sf_t0 = tmem + 2 * kAccCols;
+            bool ok = true;
+            while (ok && wk.next(s)) {
+                const int fmt = p.cls[s.cls].fmt;
+                const int A = atoms_per_step(fmt);
+                for (int kk = s.ka; kk < s.kb; ++kk) {
+                    if (!mbar_wait_bounded(full0 + 8u * st, ph, abort_flag, kWaitLimitNs)) {
+                        set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    if (A) {
+                        tc_fence_after();
+                        const uint64_t so = (uint64_t)st * stage16;
+                        const uint32_t sfa = sf_t0 + (uint32_t)st * 8 * am, sfb = sfa + 4 * am;
+                        if (is_b) {
+                            for (int a = 0; a < A; ++a) tc_cp_sf(sfb + 4 * a, sfbdesc0 + so + 32 * a);
+                        } else {
+                            for (int a = 0; a < A; ++a) tc_cp_sf(sfa + 4 * a, sfadesc0 + so + 32 * a);
+                        }
+                        tc_commit(ready0 + 8u * st);
+                    } else {
+                        mbar_arrive(ready0 + 8u * st);
+                    }
+                    if (++st == S) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            tc_commit(smem_u32(&sm.sf_drain[warp - 6]));
+            mbar_wait_bounded(smem_u32(&sm.sf_drain[warp - 6]), 0u, sm.never, kWaitLimitNs / 2);
         }
     } else {
         // ================================================================ epilogue

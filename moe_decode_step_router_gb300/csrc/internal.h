@@ -53,7 +53,7 @@ struct WsHeader {
 // Byte offsets of the workspace regions for a layer and a maximum row count.
 struct WsLayout {
     size_t header, groups, logits, scores, topk_idx, topk_w, counts, perm, inv_perm, tiles, num_tiles;
-    size_t xq, xs, xq_sh, xs_sh, hq, hs, y, cnt_gu, cnt_dn, partials, total;
+    size_t xq, xs, xq_sh, xs_sh, hq, hs, y, cnt_gu, cnt_dn, partials, rpart, rcnt, total;
     int max_rows, P_max, G_max, T_max, U_gu, U_dn;
     size_t hq_routed_bytes, hs_routed_bytes;  // shared group's data / scales start here
 };
@@ -65,12 +65,13 @@ struct RouterParams {
     const float* logits_in;   // [M, E] or null
     float* logits_out;        // [M, E] or null
     float* scores;            // [M, E]
-    int M, H, E, experts_per_cta;
+    int M, H, E;
+    float* part;              // [H/512][E][64] partial logits (workspace)
+    int32_t* counters;        // [ceil(E/8)] arrivals per expert block (self-resetting)
     // FC1 input quantisation (tiled layout)
     int fmt_r, fmt_s, quant_shared;
     uint8_t *xq, *xs, *xq_sh, *xs_sh;
     float gs_r, gs_s;
-    int num_quant_ctas;       // CTAs (at the front of the grid) that quantise
 };
 
 struct TopkRouteParams {
@@ -112,7 +113,7 @@ struct GemmParams {
     int32_t* counters;
     float* partials;
     int32_t* status;
-    int stages, stage_bytes, a_off, sfa_off, b_off, sfb_off, atoms_max;
+    int stages, stage_bytes, a_off, sfa_off, b_off, sfb_off, atoms_max, sf_warps;
 };
 
 struct FinalizeParams {

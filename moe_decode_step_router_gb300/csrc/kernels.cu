@@ -120,20 +120,28 @@ __device__ __forceinline__ int quant_units(int fmt, int Mpad, int H) {
 }
 
 // ------------------------------------------------------------------------------------
-// a1 (+a3): router GEMV with fp32 accumulation, the fp32 sigmoid score evaluated in
-// double and rounded once, and the FC1 input quantisation spread over the same grid.
-// CTA c owns experts [c*epc, (c+1)*epc); each of its 8 warps takes one (expert, row
-// quarter) and its lanes stride over H in 8-element vectors.
+// a1 (+a3): router GEMV with fp32 accumulation and the fp32 sigmoid score evaluated in
+// double and rounded once; the FC1 input quantisation is spread over the same grid.
+// Grid (H slices) x (blocks of 8 experts). A CTA stages its x slice [M][512] and the
+// block's Wg slice [8][512] in shared memory; warp w owns expert e0 + w, its lanes split
+// (row, h range). Partial logits go to the workspace; the last CTA of an expert block
+// sums them in slice order (deterministic) and applies the sigmoid.
 constexpr int kRouterThreads = 256;
+constexpr int kRouterEB = 8;      // experts per block (one per warp)
+constexpr int kRouterHS = 512;    // H slice
+constexpr int kRouterPitch = kRouterHS + 8;
 
 __global__ void __launch_bounds__(kRouterThreads) k_router(RouterParams p) {
+    extern __shared__ __align__(16) uint16_t rsm[];
+    __shared__ int s_last;
     pdl_wait();
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int H = p.H, M = p.M, E = p.E;
     const int Mpad = round_up(M, 16);
-    // quantisation (all CTAs share the units)
+    // FC1 input quantisation (all CTAs share the units)
     {
-        const int nthreads = gridDim.x * blockDim.x, tid = blockIdx.x * blockDim.x + threadIdx.x;
+        const int nthreads = gridDim.x * gridDim.y * blockDim.x;
+        const int tid = (blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
         const int nr = quant_units(p.fmt_r, Mpad, H);
         for (int u = tid; u < nr; u += nthreads) quant_unit(p.x, M, H, Mpad, p.fmt_r, p.gs_r, p.xq, p.xs, u);
         if (p.quant_shared) {
@@ -142,55 +150,77 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(RouterParams p) {
                 quant_unit(p.x, M, H, Mpad, p.fmt_s, p.gs_s, p.xq_sh, p.xs_sh, u);
         }
     }
-    // router logits for this CTA's experts
-    const int wpe = 8 / p.experts_per_cta;  // warps per expert
-    const int e = blockIdx.x * p.experts_per_cta + warp / wpe;
-    const int rq = warp % wpe;             // this warp's rows: m = rq, rq + wpe, ...
-    if (e < E) {
-        if (p.logits_in) {
-            for (int m = rq + wpe * lane; m < M; m += 32 * wpe) {
-                const float lg = p.logits_in[(size_t)m * E + e];
-                const float sc = (float)(1.0 / (1.0 + exp(-(double)lg)));
-                p.scores[(size_t)m * E + e] = sc;
-                if (p.logits_out) p.logits_out[(size_t)m * E + e] = lg;
-            }
-        } else {
-            const uint16_t* wrow = p.wg + (size_t)e * H;
-            for (int m0 = rq; m0 < M; m0 += 16 * wpe) {
-                float acc[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
-                for (int h = 8 * lane; h < H; h += 256) {
-                    const uint4 w = __ldg(reinterpret_cast<const uint4*>(wrow + h));
-                    const float w0 = bf16_lo(w.x), w1 = bf16_hi(w.x), w2 = bf16_lo(w.y), w3 = bf16_hi(w.y);
-                    const float w4 = bf16_lo(w.z), w5 = bf16_hi(w.z), w6 = bf16_lo(w.w), w7 = bf16_hi(w.w);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int m = m0 + i * wpe;
-                        if (m < M) {
-                            const uint4 xv = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)m * H + h));
-                            float a = acc[i];
-                            a = fmaf(bf16_lo(xv.x), w0, a); a = fmaf(bf16_hi(xv.x), w1, a);
-                            a = fmaf(bf16_lo(xv.y), w2, a); a = fmaf(bf16_hi(xv.y), w3, a);
-                            a = fmaf(bf16_lo(xv.z), w4, a); a = fmaf(bf16_hi(xv.z), w5, a);
-                            a = fmaf(bf16_lo(xv.w), w6, a); a = fmaf(bf16_hi(xv.w), w7, a);
-                            acc[i] = a;
-                        }
-                    }
-                }
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int m = m0 + i * wpe;
-                    const float lg = warp_sum(acc[i]);
-                    if (lane == (i & 31) && m < M) {
-                        const float sc = (float)(1.0 / (1.0 + exp(-(double)lg)));
-                        p.scores[(size_t)m * E + e] = sc;
-                        if (p.logits_out) p.logits_out[(size_t)m * E + e] = lg;
-                    }
-                }
+    const int e0 = blockIdx.y * kRouterEB, slice = blockIdx.x, nslices = gridDim.x;
+    if (!p.logits_in) {
+        const int h0 = slice * kRouterHS;
+        const int len = min(kRouterHS, H - h0);        // 512, or 256 for the last slice
+        uint16_t* xs = rsm;                            // [M][pitch]
+        uint16_t* ws = rsm + (size_t)M * kRouterPitch;  // [8][pitch]
+        const int VPR = len / 8;                       // 16-byte vectors per row slice
+        for (int v = threadIdx.x; v < (M + kRouterEB) * VPR; v += blockDim.x) {
+            const int r = v / VPR, c = v % VPR;
+            uint4 val = make_uint4(0u, 0u, 0u, 0u);
+            if (r < M) {
+                val = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)r * H + h0) + c);
+                *reinterpret_cast<uint4*>(xs + (size_t)r * kRouterPitch + 8 * c) = val;
+            } else {
+                const int e = e0 + (r - M);
+                if (e < E) val = __ldg(reinterpret_cast<const uint4*>(p.wg + (size_t)e * H + h0) + c);
+                *reinterpret_cast<uint4*>(ws + (size_t)(r - M) * kRouterPitch + 8 * c) = val;
             }
         }
+        __syncthreads();
+        // lanes: R row lanes x (32 / R) h splits; rows above 32 handled as a second pass
+        int R = 1;
+        while (R < M && R < 32) R <<= 1;
+        const int nsplit = 32 / R, r = lane % R, sp = lane / R;
+        const int hl = len / nsplit, hb = sp * hl;
+        const int e = e0 + warp;
+        const uint16_t* wrow = ws + (size_t)warp * kRouterPitch;
+        for (int rr = r; rr < ((M + 31) / 32) * 32 && rr < 64; rr += 32) {
+            float acc = 0.0f;
+            if (rr < M) {
+                const uint16_t* xrow = xs + (size_t)rr * kRouterPitch;
+                for (int h = hb; h < hb + hl; h += 8) {
+                    const uint4 xv = *reinterpret_cast<const uint4*>(xrow + h);
+                    const uint4 wv = *reinterpret_cast<const uint4*>(wrow + h);
+                    acc = fmaf(bf16_lo(xv.x), bf16_lo(wv.x), acc); acc = fmaf(bf16_hi(xv.x), bf16_hi(wv.x), acc);
+                    acc = fmaf(bf16_lo(xv.y), bf16_lo(wv.y), acc); acc = fmaf(bf16_hi(xv.y), bf16_hi(wv.y), acc);
+                    acc = fmaf(bf16_lo(xv.z), bf16_lo(wv.z), acc); acc = fmaf(bf16_hi(xv.z), bf16_hi(wv.z), acc);
+                    acc = fmaf(bf16_lo(xv.w), bf16_lo(wv.w), acc); acc = fmaf(bf16_hi(xv.w), bf16_hi(wv.w), acc);
+                }
+            }
+            for (int o = R; o < 32; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if (sp == 0 && rr < M && e < E) __stcg(p.part + ((size_t)slice * E + e) * kMaxRows + rr, acc);
+        }
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const int old = atomicAdd(p.counters + blockIdx.y, 1);
+            s_last = (old == nslices - 1) ? 1 : 0;
+        }
+        __syncthreads();
+        if (!s_last) {
+            pdl_trigger();
+            return;
+        }
+        __threadfence();
     }
+    // the last CTA of the block: sum the slices in order, sigmoid in double, write scores
+    for (int q = threadIdx.x; q < kRouterEB * M; q += blockDim.x) {
+        const int e = e0 + q / M, m = q % M;
+        if (e >= E) continue;
+        float lg;
+        if (p.logits_in) {
+            lg = p.logits_in[(size_t)m * E + e];
+        } else {
+            lg = 0.0f;
+            for (int sl = 0; sl < nslices; ++sl) lg += __ldcg(p.part + ((size_t)sl * E + e) * kMaxRows + m);
+        }
+        p.scores[(size_t)m * E + e] = (float)(1.0 / (1.0 + exp(-(double)lg)));
+        if (p.logits_out) p.logits_out[(size_t)m * E + e] = lg;
+    }
+    if (threadIdx.x == 0 && !p.logits_in) p.counters[blockIdx.y] = 0;
     pdl_trigger();
 }
 
@@ -364,62 +394,103 @@ __global__ void __launch_bounds__(kRouteThreads) k_topk_route(TopkRouteParams p)
 // ------------------------------------------------------------------------------------
 // a7: weighted combine in fixed slot order + shared row + residual (bf16) + RMSNorm,
 // optional MXFP8 of the output per 32 along H (rows M..round_up(M,8)-1 zero).
-constexpr int kFinThreads = 256;
-constexpr int kFinMaxPer = 8192 / kFinThreads;
+// One cluster of kFinCluster CTAs per row, each CTA a contiguous H slice; the sum of
+// squares is reduced over distributed shared memory in rank order (deterministic).
+constexpr int kFinThreads = 128;
+constexpr int kFinCluster = 8;
+constexpr int kFinMaxPer = 8192 / (kFinCluster * kFinThreads);
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float dsmem_ld(const float* local, uint32_t rank) {
+    uint32_t a = smem_u32(local), ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+    return v;
+}
 
 __global__ void __launch_bounds__(kFinThreads) k_finalize(FinalizeParams p) {
     __shared__ float red[kFinThreads / 32];
+    __shared__ float part;
+    __shared__ float w_s[kMaxK];
+    __shared__ int pos_s[kMaxK + 1];
     pdl_wait();
-    const int m = blockIdx.x, H = p.H, k = p.k, M = p.M;
+    const int m = blockIdx.y, H = p.H, k = p.k, M = p.M;
     const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
-    const int nper = H / kFinThreads;
-    if (m >= M) {
-        for (int n = threadIdx.x; n < H; n += kFinThreads) p.outq[(size_t)m * H + n] = 0;
-        for (int n = threadIdx.x; n < H / 32; n += kFinThreads) p.outs[(size_t)m * (H / 32) + n] = 0;
+    const int slice = H / kFinCluster, base = (int)cluster_rank() * slice;
+    if (m >= M) {  // padding rows of the 8-row output tiles
+        for (int n = base + threadIdx.x; n < base + slice; n += kFinThreads) p.outq[(size_t)m * H + n] = 0;
+        for (int n = base / 32 + threadIdx.x; n < (base + slice) / 32; n += kFinThreads)
+            p.outs[(size_t)m * (H / 32) + n] = 0;
+        cluster_sync();
+        cluster_sync();
         return;
     }
     const int P = M * k;
+    if (threadIdx.x < k) {
+        pos_s[threadIdx.x] = p.inv_perm[m * k + threadIdx.x];
+        w_s[threadIdx.x] = p.topk_w[m * k + threadIdx.x];
+    }
+    if (threadIdx.x == kMaxK) pos_s[kMaxK] = p.has_shared ? p.inv_perm[P + m] : -1;
+    __syncthreads();
     float hv[kFinMaxPer];
     float ss = 0.0f;
-    int pos[kMaxK + 1];
-    float w[kMaxK];
-    for (int j = 0; j < k; ++j) {
-        pos[j] = p.inv_perm[m * k + j];
-        w[j] = p.topk_w[m * k + j];
-    }
-    const int pos_sh = p.has_shared ? p.inv_perm[P + m] : -1;
-#pragma unroll 4
-    for (int i = 0; i < nper; ++i) {
-        const int n = threadIdx.x + kFinThreads * i;
-        float acc = 0.0f;
-        for (int j = 0; j < k; ++j) acc = fmaf(w[j], __ldcg(p.y + (size_t)pos[j] * H + n), acc);
-        if (pos_sh >= 0) acc = __fadd_rn(acc, __ldcg(p.y + (size_t)pos_sh * H + n));
-        const float r = bf16f(p.residual[(size_t)m * H + n]);
-        const __nv_bfloat16 hb = __float2bfloat16_rn(__fadd_rn(r, acc));
-        p.residual[(size_t)m * H + n] = __bfloat16_as_ushort(hb);
-        const float hf = __bfloat162float(hb);
-        hv[i] = hf;
-        ss = fmaf(hf, hf, ss);
+#pragma unroll
+    for (int i = 0; i < kFinMaxPer; ++i) {
+        const int n = base + threadIdx.x + kFinThreads * i;
+        hv[i] = 0.0f;
+        if (n < base + slice) {
+            float yv[kMaxK];
+#pragma unroll
+            for (int j = 0; j < kMaxK; ++j) yv[j] = (j < k) ? __ldcg(p.y + (size_t)pos_s[j] * H + n) : 0.0f;
+            float acc = 0.0f;
+#pragma unroll
+            for (int j = 0; j < kMaxK; ++j)
+                if (j < k) acc = fmaf(w_s[j], yv[j], acc);
+            if (pos_s[kMaxK] >= 0) acc = __fadd_rn(acc, __ldcg(p.y + (size_t)pos_s[kMaxK] * H + n));
+            const float r = bf16f(p.residual[(size_t)m * H + n]);
+            const __nv_bfloat16 hb = __float2bfloat16_rn(__fadd_rn(r, acc));
+            p.residual[(size_t)m * H + n] = __bfloat16_as_ushort(hb);
+            const float hf = __bfloat162float(hb);
+            hv[i] = hf;
+            ss = fmaf(hf, hf, ss);
+        }
     }
     ss = warp_sum(ss);
     if (lane == 0) red[warp] = ss;
     __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kFinThreads / 32; ++i) t += red[i];
+        part = t;
+    }
+    cluster_sync();
     float tot = 0.0f;
 #pragma unroll
-    for (int i = 0; i < kFinThreads / 32; ++i) tot += red[i];
+    for (int rk = 0; rk < kFinCluster; ++rk) tot += dsmem_ld(&part, (uint32_t)rk);
+    cluster_sync();  // no CTA leaves while another still reads its partial
     const float rstd = rsqrtf(tot / (float)H + p.eps);
-#pragma unroll 4
-    for (int i = 0; i < nper; ++i) {
-        const int n = threadIdx.x + kFinThreads * i;
+#pragma unroll
+    for (int i = 0; i < kFinMaxPer; ++i) {
+        const int n0 = base + kFinThreads * i + 32 * warp;  // this warp's 32-element block
+        if (n0 >= base + slice) break;
+        const int n = n0 + lane;
         const float g = bf16f(p.gamma[n]);
         const __nv_bfloat16 ob = __float2bfloat16_rn(hv[i] * rstd * g);
         p.out[(size_t)m * H + n] = __bfloat16_as_ushort(ob);
         if (p.outq) {
             const float of = __bfloat162float(ob);
-            const float amax = warp_max(fabsf(of));  // lanes hold 32 consecutive n
+            const float amax = warp_max(fabsf(of));
             const int e = mx_exponent(amax);
-            const uint8_t q = e4m3(__fmul_rn(of, exp2_int(-e)));
-            p.outq[(size_t)m * H + n] = q;
+            p.outq[(size_t)m * H + n] = e4m3(__fmul_rn(of, exp2_int(-e)));
             if (lane == 0) p.outs[(size_t)m * (H / 32) + n / 32] = (uint8_t)(e + 127);
         }
     }
