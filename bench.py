@@ -35,6 +35,7 @@ def _args():
     ap.add_argument("--config", default=HEADLINE)
     ap.add_argument("--rows", type=int, default=None)
     ap.add_argument("--experts", type=int, default=None, help="override E (smaller profiling cases)")
+    ap.add_argument("--inter", type=int, default=None, help="override I and shared I (smaller profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
     return ap.parse_args()
@@ -100,6 +101,8 @@ def _cfg(a):
         over["M"] = a.rows
     if a.experts is not None:
         over["E"] = a.experts
+    if a.inter is not None:
+        over["I"] = over["I_sh"] = a.inter
     return synth.config(a.config, **over)
 
 

@@ -345,7 +345,7 @@ moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* wr,
     p.b_off = round_up(p.sfa_off + am * kAtomBytes, 1024);
     p.sfb_off = p.b_off + p.Mpad * kStepBytes;
     p.stage_bytes = round_up(p.sfb_off + am * kAtomBytes, 1024);
-    const int fixed = 1024 + p.Mpad * kBlockRows * 4 + 512;
+    const int fixed = 1024 + p.Mpad * kBlockRows * 4 + 640;
     int S = (di->smem_optin - fixed) / (p.stage_bytes + 24);  // + full/empty/ready barriers
     const int tmem_cap = am ? (512 - 2 * 64) / (8 * am) : 16;
     if (S > tmem_cap) S = tmem_cap;
@@ -385,7 +385,7 @@ moe_status launch_finalize(const moe_layer_desc* d, const float* y, const float*
     const int rows = outq ? round_up(M, 8) : M;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(8, rows);
-    cfg.blockDim = dim3(128);
+    cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];

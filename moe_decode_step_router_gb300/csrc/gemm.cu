@@ -31,7 +31,8 @@ namespace moe {
 constexpr int kGemmThreads = 256;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint32_t kTmemCols = 512;
-constexpr int kAccCols = 64;
+constexpr int kAccCols = 64;   // two buffers of 64 columns = the 128-column accumulator region
+constexpr int kMaxAcc = 8;    // up to 8 buffers of round_up(M,16) columns in that region
 
 struct Seg {
     int cls, g, b, ka, kb, KS;
@@ -205,8 +206,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
     sm.full = reinterpret_cast<uint64_t*>(misc);
     sm.empty = sm.full + S;
     sm.acc_full = sm.empty + S;
-    sm.acc_empty = sm.acc_full + 2;
-    sm.drain = sm.acc_empty + 2;
+    sm.acc_empty = sm.acc_full + kMaxAcc;
+    sm.drain = sm.acc_empty + kMaxAcc;
     sm.sf_ready = sm.drain + 1;
     sm.sf_drain = sm.sf_ready + S;
     sm.tmem_base = reinterpret_cast<uint32_t*>(sm.sf_drain + 2);
@@ -219,7 +220,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             mbar_init(smem_u32(&sm.full[i]), 1);
             mbar_init(smem_u32(&sm.empty[i]), 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kMaxAcc; ++i) {
             mbar_init(smem_u32(&sm.acc_full[i]), 1);
             mbar_init(smem_u32(&sm.acc_empty[i]), 4);
         }
@@ -240,6 +241,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *sm.tmem_base;
+    // accumulator buffers of Mpad columns each in the 128-column region: the MMA thread
+    // runs up to nacc - 1 units ahead of the epilogue
+    const int nacc = min(kMaxAcc, 2 * kAccCols / p.Mpad);
     pdl_trigger();
 
     const int ngroups = p.hdr->num_groups;
@@ -315,7 +319,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             int st = 0;
             uint32_t ph = 0;
             int ab = 0;
-            uint32_t acc_ph[2] = {0u, 0u};
+            uint32_t acc_ph = 0u;  // bit b: phase of accumulator buffer b
             bool ok = true;
             const int am = p.atoms_max;
             // with copy warps the MMA thread waits for the stage's scales, else for its data
@@ -333,12 +337,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                 int expert, rows, perm_off, row_off, gidx;
                 seg_group(p, s, expert, rows, perm_off, row_off, gidx);
                 const uint32_t N = (p.mode == 0) ? (uint32_t)p.Mpad : (uint32_t)((s.cls == 0) ? round_up(rows, 16) : p.Mpad);
-                if (!mbar_wait_bounded(smem_u32(&sm.acc_empty[ab]), acc_ph[ab] ^ 1u, abort_flag, kWaitLimitNs)) {
+                if (!mbar_wait_bounded(smem_u32(&sm.acc_empty[ab]), ((acc_ph >> ab) & 1u) ^ 1u, abort_flag,
+                                       kWaitLimitNs)) {
                     set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem + (uint32_t)(ab * kAccCols);
+                const uint32_t d_tmem = tmem + (uint32_t)(ab * p.Mpad);
 #define MOE_SEG(F, CPV)                                                                                   \
     mma_segment<F, CPV>(wait0, empty0, st, ph, S, s.ka, s.kb, adesc0, bdesc0, sfadesc0, sfbdesc0, stage16, d_tmem, \
                         sf_t0, 8 * am, 4 * am, N, abort_flag)
@@ -355,8 +360,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                 if (!ok) set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
                 if (!ok) break;
                 tc_commit(smem_u32(&sm.acc_full[ab]));
-                acc_ph[ab] ^= 1u;
-                ab ^= 1;
+                acc_ph ^= 1u << ab;
+                if (++ab == nacc) ab = 0;
             }
             // wait until every issued MMA has completed before the TMEM is released
             tc_commit(smem_u32(sm.drain));
@@ -421,20 +426,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
         wk.init(p, ngroups, G, c);
         Seg s;
         int ab = 0;
-        uint32_t acc_ph[2] = {0u, 0u};
+        uint32_t acc_ph = 0u;
         float* stg = sm.stg;
         while (wk.next(s)) {
             const GemmClass& C = p.cls[s.cls];
             int expert, rows, perm_off, row_off, gidx;
             seg_group(p, s, expert, rows, perm_off, row_off, gidx);
             const int N = (p.mode == 0) ? p.Mpad : ((s.cls == 0) ? round_up(rows, 16) : p.Mpad);
-            if (!mbar_wait_bounded(smem_u32(&sm.acc_full[ab]), acc_ph[ab], abort_flag, kWaitLimitNs)) {
+            if (!mbar_wait_bounded(smem_u32(&sm.acc_full[ab]), (acc_ph >> ab) & 1u, abort_flag, kWaitLimitNs)) {
                 set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
                 break;
             }
-            acc_ph[ab] ^= 1u;
+            acc_ph ^= 1u << ab;
             tc_fence_after();
-            const uint32_t t_row = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(ab * kAccCols);
+            const uint32_t t_row = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(ab * p.Mpad);
             for (int c0 = 0; c0 < N; c0 += 16) {
                 float v[16];
                 tmem_ld16(t_row + (uint32_t)c0, v);
@@ -444,7 +449,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sm.acc_empty[ab]));
-            ab ^= 1;
+            if (++ab == nacc) ab = 0;
             // compact the selected columns: column of group row rg -> stg[rg][r]
             if (p.mode == 0 && s.cls == 0) {
                 for (int rg = 0; rg < rows; ++rg) {
@@ -471,14 +476,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                 named_bar(1, 128);
                 if (!last) continue;
                 __threadfence();
-                for (int rg = 0; rg < rows; ++rg) {
-                    float sum = 0.0f;
-                    for (int pc = 0; pc < npieces; ++pc) {
-                        const int cc = c_first + pc;
-                        const int sl = (pc == 0 && wk.start(cc, G) < s.us) ? 1 : 0;
-                        sum += __ldcg(p.partials + ((size_t)cc * 2 + sl) * kPartialFloats + rg * kBlockRows + r);
+                // sum the pieces in piece order; loads of 8 rows x 4 pieces are issued
+                // before their adds (clamped addresses keep them unconditional)
+                const int sl0 = (wk.start(c_first, G) < s.us) ? 1 : 0;
+                for (int rg0 = 0; rg0 < rows; rg0 += 8) {
+                    float sum[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) sum[i] = 0.0f;
+                    for (int pc0 = 0; pc0 < npieces; pc0 += 4) {
+                        float v[4][8];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int pc = min(pc0 + q, npieces - 1);
+                            const float* src = p.partials + ((size_t)(c_first + pc) * 2 + (pc == 0 ? sl0 : 0)) *
+                                                                kPartialFloats + r;
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) v[q][i] = __ldcg(src + min(rg0 + i, rows - 1) * kBlockRows);
+                        }
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (pc0 + q < npieces)
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) sum[i] += v[q][i];
                     }
-                    stg[rg * kBlockRows + r] = sum;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (rg0 + i < rows) stg[(rg0 + i) * kBlockRows + r] = sum[i];
                 }
                 if (et == 0) p.counters[s.unit] = 0;
             }

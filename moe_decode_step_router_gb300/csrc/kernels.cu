@@ -130,6 +130,7 @@ constexpr int kRouterThreads = 256;
 constexpr int kRouterEB = 8;      // experts per block (one per warp)
 constexpr int kRouterHS = 512;    // H slice
 constexpr int kRouterPitch = kRouterHS + 8;
+constexpr int kRouterMaxSlices = 8192 / kRouterHS;
 
 __global__ void __launch_bounds__(kRouterThreads) k_router(RouterParams p) {
     extern __shared__ __align__(16) uint16_t rsm[];
@@ -214,8 +215,16 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(RouterParams p) {
         if (p.logits_in) {
             lg = p.logits_in[(size_t)m * E + e];
         } else {
-            lg = 0.0f;
-            for (int sl = 0; sl < nslices; ++sl) lg += __ldcg(p.part + ((size_t)sl * E + e) * kMaxRows + m);
+            // issue every slice's load before the first add (a loop-carried load would
+            // expose one L2 round trip per slice), then sum in slice order
+            float v[kRouterMaxSlices];
+#pragma unroll
+            for (int sl = 0; sl < kRouterMaxSlices; ++sl)
+                v[sl] = __ldcg(p.part + ((size_t)min(sl, nslices - 1) * E + e) * kMaxRows + m);
+            lg = v[0];
+#pragma unroll
+            for (int sl = 1; sl < kRouterMaxSlices; ++sl)
+                if (sl < nslices) lg += v[sl];
         }
         p.scores[(size_t)m * E + e] = (float)(1.0 / (1.0 + exp(-(double)lg)));
         if (p.logits_out) p.logits_out[(size_t)m * E + e] = lg;
@@ -229,6 +238,13 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(RouterParams p) {
 // expert index, renormalised weights (double, rounded once), then the stable counting
 // sort of the (row, slot) pairs into 8-row tiles and the per-expert group table.
 constexpr int kRouteThreads = 1024;
+
+// Order-preserving map of an fp32 key to u32: a larger key gives a larger integer; every
+// finite key maps above 0, which marks taken or absent experts.
+__device__ __forceinline__ uint32_t key_u32(float f) {
+    const uint32_t u = __float_as_uint(__fadd_rn(f, 0.0f));  // -0 -> +0: equal keys tie
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
 
 __device__ __forceinline__ void block_scan4(int4 v, int4* out_excl, int4* total, int4* sh_warp) {
     // inclusive warp scan
@@ -268,45 +284,43 @@ __global__ void __launch_bounds__(kRouteThreads) k_topk_route(TopkRouteParams p)
     const int M = p.M, E = p.E, k = p.k;
     if (p.do_topk) {
         for (int m = warp; m < M; m += kRouteThreads / 32) {
-            float key[kMaxE / 32], sc[kMaxE / 32];
+            // keys as order-preserving u32 (0 = taken / absent); lane owns e = lane + 32 i
+            uint32_t ku[kMaxE / 32];
+            float sc[kMaxE / 32];
 #pragma unroll
             for (int i = 0; i < kMaxE / 32; ++i) {
                 const int e = lane + 32 * i;
+                sc[i] = 0.0f;
+                ku[i] = 0u;
                 if (e < E) {
                     sc[i] = p.scores[(size_t)m * E + e];
-                    key[i] = p.bias ? __fadd_rn(sc[i], p.bias[e]) : sc[i];
-                } else {
-                    sc[i] = 0.0f;
-                    key[i] = -INFINITY;
+                    ku[i] = key_u32(p.bias ? __fadd_rn(sc[i], p.bias[e]) : sc[i]);
                 }
             }
-            uint32_t taken = 0;
+            // this lane's best: largest key, lowest index among equals (ascending scan)
+            uint32_t lb = 0u;
+            int li = 0;
+#pragma unroll
+            for (int i = 0; i < kMaxE / 32; ++i)
+                if (ku[i] > lb) { lb = ku[i]; li = i; }
             int my_idx = 0;
             float my_sc = 0.0f;
             double ssum = 0.0;
             for (int j = 0; j < k; ++j) {
-                float bk = -INFINITY;
-                int bi = 0x7fffffff;
-#pragma unroll
-                for (int i = 0; i < kMaxE / 32; ++i) {
-                    const int e = lane + 32 * i;
-                    if (e < E && !((taken >> i) & 1u) && (key[i] > bk || bi == 0x7fffffff)) {
-                        bk = key[i];
-                        bi = e;
-                    }
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
-                    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-                    if (ok > bk || (ok == bk && oi < bi)) { bk = ok; bi = oi; }
-                }
+                const uint32_t wmax = __reduce_max_sync(0xffffffffu, lb);
+                const uint32_t cand = (lb == wmax) ? (uint32_t)(lane + 32 * li) : 0xffffffffu;
+                const int bi = (int)__reduce_min_sync(0xffffffffu, cand);
                 float wsc = 0.0f;
                 if ((bi & 31) == lane) {
-                    taken |= 1u << (bi / 32);
+                    const int ti = bi >> 5;
 #pragma unroll
                     for (int i = 0; i < kMaxE / 32; ++i)
-                        if (i == bi / 32) wsc = sc[i];
+                        if (i == ti) { wsc = sc[i]; ku[i] = 0u; }
+                    lb = 0u;
+                    li = 0;
+#pragma unroll
+                    for (int i = 0; i < kMaxE / 32; ++i)
+                        if (ku[i] > lb) { lb = ku[i]; li = i; }
                 }
                 wsc = __shfl_sync(0xffffffffu, wsc, bi & 31);
                 ssum += (double)wsc;
@@ -319,7 +333,6 @@ __global__ void __launch_bounds__(kRouteThreads) k_topk_route(TopkRouteParams p)
             }
         }
         __syncthreads();
-        __threadfence_block();
     }
     if (!p.do_route) {
         pdl_trigger();
@@ -394,11 +407,11 @@ __global__ void __launch_bounds__(kRouteThreads) k_topk_route(TopkRouteParams p)
 // ------------------------------------------------------------------------------------
 // a7: weighted combine in fixed slot order + shared row + residual (bf16) + RMSNorm,
 // optional MXFP8 of the output per 32 along H (rows M..round_up(M,8)-1 zero).
-// One cluster of kFinCluster CTAs per row, each CTA a contiguous H slice; the sum of
-// squares is reduced over distributed shared memory in rank order (deterministic).
-constexpr int kFinThreads = 128;
+// One cluster of kFinCluster CTAs per row, each CTA a contiguous H slice handled as
+// float4 vectors (all k+1 row loads of a vector in flight at once); the sum of squares is
+// reduced over distributed shared memory in rank order (deterministic).
+constexpr int kFinThreads = 256;
 constexpr int kFinCluster = 8;
-constexpr int kFinMaxPer = 8192 / (kFinCluster * kFinThreads);
 
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
@@ -425,43 +438,64 @@ __global__ void __launch_bounds__(kFinThreads) k_finalize(FinalizeParams p) {
     const int m = blockIdx.y, H = p.H, k = p.k, M = p.M;
     const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
     const int slice = H / kFinCluster, base = (int)cluster_rank() * slice;
+    const int n = base + 4 * (int)threadIdx.x;  // this thread's 4 elements
+    const bool act = 4 * (int)threadIdx.x < slice;
     if (m >= M) {  // padding rows of the 8-row output tiles
-        for (int n = base + threadIdx.x; n < base + slice; n += kFinThreads) p.outq[(size_t)m * H + n] = 0;
-        for (int n = base / 32 + threadIdx.x; n < (base + slice) / 32; n += kFinThreads)
-            p.outs[(size_t)m * (H / 32) + n] = 0;
+        if (act) *reinterpret_cast<uint32_t*>(p.outq + (size_t)m * H + n) = 0u;
+        if (act && (n % 32) == 0) p.outs[(size_t)m * (H / 32) + n / 32] = 0;
         cluster_sync();
         cluster_sync();
         return;
     }
     const int P = M * k;
-    if (threadIdx.x < k) {
-        pos_s[threadIdx.x] = p.inv_perm[m * k + threadIdx.x];
-        w_s[threadIdx.x] = p.topk_w[m * k + threadIdx.x];
+    // slots beyond k read slot k-1's row (an L2 hit) with weight 0, so every load is
+    // unconditional and all of them are in flight before the first FMA
+    if (threadIdx.x < kMaxK) {
+        const int j = min((int)threadIdx.x, k - 1);
+        pos_s[threadIdx.x] = p.inv_perm[m * k + j];
+        w_s[threadIdx.x] = (int)threadIdx.x < k ? p.topk_w[m * k + j] : 0.0f;
     }
     if (threadIdx.x == kMaxK) pos_s[kMaxK] = p.has_shared ? p.inv_perm[P + m] : -1;
     __syncthreads();
-    float hv[kFinMaxPer];
+    float hv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     float ss = 0.0f;
+    if (act) {
+        float4 yv[kMaxK + 1];
+        const int psh = pos_s[kMaxK];
+        const int kl = (k + 3) & ~3;  // slots loaded: k rounded up to 4 (the rest weigh 0)
 #pragma unroll
-    for (int i = 0; i < kFinMaxPer; ++i) {
-        const int n = base + threadIdx.x + kFinThreads * i;
-        hv[i] = 0.0f;
-        if (n < base + slice) {
-            float yv[kMaxK];
+        for (int j = 0; j < kMaxK; ++j)
+            if ((j & 3) == 0 && j >= kl) break;
+            else yv[j] = __ldcg(reinterpret_cast<const float4*>(p.y + (size_t)pos_s[j] * H + n));
+        yv[kMaxK] = __ldcg(reinterpret_cast<const float4*>(p.y + (size_t)max(psh, pos_s[0]) * H + n));
+        const uint2 rr = *reinterpret_cast<const uint2*>(p.residual + (size_t)m * H + n);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int j = 0; j < kMaxK; ++j) yv[j] = (j < k) ? __ldcg(p.y + (size_t)pos_s[j] * H + n) : 0.0f;
-            float acc = 0.0f;
-#pragma unroll
-            for (int j = 0; j < kMaxK; ++j)
-                if (j < k) acc = fmaf(w_s[j], yv[j], acc);
-            if (pos_s[kMaxK] >= 0) acc = __fadd_rn(acc, __ldcg(p.y + (size_t)pos_s[kMaxK] * H + n));
-            const float r = bf16f(p.residual[(size_t)m * H + n]);
-            const __nv_bfloat16 hb = __float2bfloat16_rn(__fadd_rn(r, acc));
-            p.residual[(size_t)m * H + n] = __bfloat16_as_ushort(hb);
-            const float hf = __bfloat162float(hb);
-            hv[i] = hf;
-            ss = fmaf(hf, hf, ss);
+        for (int j = 0; j < kMaxK; ++j) {
+            if (j < k) {  // fixed slot order; FMAs only, no load below this point
+                const float w = w_s[j];
+                acc[0] = fmaf(w, yv[j].x, acc[0]);
+                acc[1] = fmaf(w, yv[j].y, acc[1]);
+                acc[2] = fmaf(w, yv[j].z, acc[2]);
+                acc[3] = fmaf(w, yv[j].w, acc[3]);
+            }
         }
+        if (psh >= 0) {
+            acc[0] = __fadd_rn(acc[0], yv[kMaxK].x);
+            acc[1] = __fadd_rn(acc[1], yv[kMaxK].y);
+            acc[2] = __fadd_rn(acc[2], yv[kMaxK].z);
+            acc[3] = __fadd_rn(acc[3], yv[kMaxK].w);
+        }
+        const float r[4] = {bf16_lo(rr.x), bf16_hi(rr.x), bf16_lo(rr.y), bf16_hi(rr.y)};
+        uint32_t hb[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat16 b = __float2bfloat16_rn(__fadd_rn(r[i], acc[i]));
+            hb[i] = __bfloat16_as_ushort(b);
+            hv[i] = __bfloat162float(b);
+            ss = fmaf(hv[i], hv[i], ss);
+        }
+        *reinterpret_cast<uint2*>(p.residual + (size_t)m * H + n) = make_uint2(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16));
     }
     ss = warp_sum(ss);
     if (lane == 0) red[warp] = ss;
@@ -478,20 +512,29 @@ __global__ void __launch_bounds__(kFinThreads) k_finalize(FinalizeParams p) {
     for (int rk = 0; rk < kFinCluster; ++rk) tot += dsmem_ld(&part, (uint32_t)rk);
     cluster_sync();  // no CTA leaves while another still reads its partial
     const float rstd = rsqrtf(tot / (float)H + p.eps);
+    if (act) {
+        const uint2 gg = *reinterpret_cast<const uint2*>(p.gamma + n);
+        const float g[4] = {bf16_lo(gg.x), bf16_hi(gg.x), bf16_lo(gg.y), bf16_hi(gg.y)};
+        uint32_t ob[4];
+        float of[4];
 #pragma unroll
-    for (int i = 0; i < kFinMaxPer; ++i) {
-        const int n0 = base + kFinThreads * i + 32 * warp;  // this warp's 32-element block
-        if (n0 >= base + slice) break;
-        const int n = n0 + lane;
-        const float g = bf16f(p.gamma[n]);
-        const __nv_bfloat16 ob = __float2bfloat16_rn(hv[i] * rstd * g);
-        p.out[(size_t)m * H + n] = __bfloat16_as_ushort(ob);
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat16 b = __float2bfloat16_rn(hv[i] * rstd * g[i]);
+            ob[i] = __bfloat16_as_ushort(b);
+            of[i] = __bfloat162float(b);
+        }
+        *reinterpret_cast<uint2*>(p.out + (size_t)m * H + n) = make_uint2(ob[0] | (ob[1] << 16), ob[2] | (ob[3] << 16));
         if (p.outq) {
-            const float of = __bfloat162float(ob);
-            const float amax = warp_max(fabsf(of));
+            // a 32-element MX block = 8 consecutive lanes x 4 elements
+            float amax = fmaxf(fmaxf(fabsf(of[0]), fabsf(of[1])), fmaxf(fabsf(of[2]), fabsf(of[3])));
+#pragma unroll
+            for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o, 8));
             const int e = mx_exponent(amax);
-            p.outq[(size_t)m * H + n] = e4m3(__fmul_rn(of, exp2_int(-e)));
-            if (lane == 0) p.outs[(size_t)m * (H / 32) + n / 32] = (uint8_t)(e + 127);
+            const float sc = exp2_int(-e);
+            const uint32_t lo = e4m3x2(__fmul_rn(of[1], sc), __fmul_rn(of[0], sc));
+            const uint32_t hi = e4m3x2(__fmul_rn(of[3], sc), __fmul_rn(of[2], sc));
+            *reinterpret_cast<uint32_t*>(p.outq + (size_t)m * H + n) = lo | (hi << 16);
+            if ((n % 32) == 0) p.outs[(size_t)m * (H / 32) + n / 32] = (uint8_t)(e + 127);
         }
     }
     pdl_trigger();
