@@ -225,6 +225,28 @@ moe_status moe_finalize_norm(const moe_layer_desc* d, const float* y_pairs, cons
  * ws (see moe_ws_view). M in [1, 64]. Capture-safe. */
 moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void* ws, moe_stream_t stream);
 
+/* The router step (a1 + a2 + a3, as moe_router_topk) for callers that cannot give the
+ * library any device memory: a host framework that owns every allocation and offers
+ * plugins no allocator, or a serving loop that must not allocate once running (an
+ * allocation can synchronise the device or fail under memory pressure). The pages have no
+ * counterpart: their engines allocate their buffers at load.
+ *  - Takes no workspace and allocates nothing: its scratch (partial logits, scores,
+ *    arrival counters; about 1.2 MiB) is one fixed array inside the library, held by every
+ *    GPU that loads the library until the process exits. Inputs and outputs are the
+ *    caller's, exactly as for moe_router_topk, and the results are the same.
+ *  - Limit: when the GEMV runs (logits_in == NULL), ceil(H/512) * E must be <= 4096;
+ *    larger layers are rejected with MOE_ERR_UNSUPPORTED before anything is launched.
+ *  - The first call on a device looks up the array's device address (with that device
+ *    current); make that first call before any stream capture.
+ *  - Every call uses the same array and it keeps the last call's contents (each call
+ *    clears the counters it needs at zero). Calls that overlap on the GPU race: issue them
+ *    on one stream, or order them.
+ *  - Device-side status has no workspace to go to; host-side errors are returned as usual. */
+moe_status moe_router_topk_noalloc(const moe_layer_desc* d, const void* x, const void* w_gate, const float* bias,
+                                   const float* logits_in, int M, float* logits_out, int32_t* topk_idx,
+                                   float* topk_w, void* xq, void* xq_scales, void* xq_sh, void* xq_sh_scales,
+                                   moe_stream_t stream);
+
 /* Synchronises `stream` and reads the workspace status word into *dev_status. */
 moe_status moe_get_status(void* ws, moe_stream_t stream, int* dev_status);
 

@@ -5,6 +5,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "internal.h"
@@ -698,6 +699,102 @@ moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void
     if (s != MOE_OK) return s;
     s = launch_finalize(d, b.y, topk_w, inv_perm, M, a->residual, a->gamma, a->out,
                         d->emit_next_mxfp8 ? a->outq : nullptr, d->emit_next_mxfp8 ? a->outq_scales : nullptr, st);
+    if (s != MOE_OK) return s;
+    return ok();
+}
+
+// ------------------------------------------------------------------------------------
+// Router step without a caller workspace (moe_router_topk_noalloc).
+//
+// Some callers cannot give the library device memory: a host framework that owns every
+// allocation and hands plugins no allocator, or a serving loop that must not allocate once
+// it is running (an allocation can synchronise the device or fail under memory pressure).
+// For them the router step keeps its scratch (partial logits, scores, arrival counters) in
+// one fixed array in the library's own device memory, allocated when the library is
+// loaded and held by every GPU that loads it until the process exits.
+//
+// Layout: [256 B header][256 B per-block counters][scores 64 x 512 fp32][partial logits].
+// The partial-logit region holds 1 MiB, so ceil(H / 512) * E may be at most 4096 when the
+// GEMV runs (logits_in == NULL).
+constexpr size_t kNaHeader = 0, kNaCounters = 256, kNaScores = 512;
+constexpr size_t kNaPartials = kNaScores + 4ull * kMaxRows * kMaxE;
+constexpr size_t kNaPartialFloats = (1u << 20) / 4;
+constexpr size_t kNoAllocScratchBytes = kNaPartials + 4ull * kNaPartialFloats;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the array per device, looked up once per device (with that device
+// current) on its first call; the host-side name of the array is not a device address.
+static uint8_t* noalloc_scratch(moe_status* st) {
+    static std::mutex mu;
+    static uint8_t* addr[128] = {};
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        *st = cuda_fail(e, "cudaGetDevice");
+        return nullptr;
+    }
+    if (dev < 0 || dev >= 128) {
+        *st = fail(MOE_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    if (!addr[dev]) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess || !ptr) {
+            *st = cuda_fail(e, "cudaGetSymbolAddress(noalloc scratch)");
+            return nullptr;
+        }
+        addr[dev] = static_cast<uint8_t*>(ptr);
+    }
+    *st = MOE_OK;
+    return addr[dev];
+}
+
+extern "C" moe_status moe_router_topk_noalloc(const moe_layer_desc* d, const void* x, const void* w_gate,
+                                              const float* bias, const float* logits_in, int M, float* logits_out,
+                                              int32_t* topk_idx, float* topk_w, void* xq, void* xq_scales,
+                                              void* xq_sh, void* xq_sh_scales, moe_stream_t stream) {
+    moe_status s = check_desc(d);
+    if (s != MOE_OK) return s;
+    REQUIRE(M >= 1 && M <= kMaxRows, "M=%d: need 1..%d", M, kMaxRows);
+    REQUIRE_PTR(x, "x");
+    if (!logits_in) REQUIRE_PTR(w_gate, "w_gate");
+    OPT_PTR(logits_in, "logits_in");
+    OPT_PTR(logits_out, "logits_out");
+    if (d->has_bias) REQUIRE_PTR(bias, "bias");
+    REQUIRE_PTR(topk_idx, "topk_idx");
+    REQUIRE_PTR(topk_w, "topk_w");
+    REQUIRE_PTR(xq, "xq");
+    REQUIRE_PTR(xq_scales, "xq_scales");
+    if (separate_shared_input(d)) {
+        REQUIRE_PTR(xq_sh, "xq_sh");
+        if (d->shared_fmt != MOE_FMT_BF16) REQUIRE_PTR(xq_sh_scales, "xq_sh_scales");
+    }
+    const size_t need = logits_in ? 0 : (size_t)((d->H + 511) / 512) * d->E * kMaxRows;
+    if (need > kNaPartialFloats)
+        return fail(MOE_ERR_UNSUPPORTED,
+                    "ceil(H/512) * E = %d exceeds the fixed scratch of the no-allocation router (limit 4096)",
+                    (d->H + 511) / 512 * d->E);
+    uint8_t* scratch = noalloc_scratch(&s);
+    if (!scratch) return s;
+    // scratch regions as a workspace layout for the shared launch helpers
+    WsLayout L{};
+    L.header = kNaHeader;
+    L.groups = kNaHeader;  // unused by the top-k-only launch
+    L.rcnt = kNaCounters;
+    L.rpart = kNaPartials;
+    cudaStream_t st = (cudaStream_t)stream;
+    // the arrival counters must start at zero; the array keeps the last call's contents
+    cudaError_t e = cudaMemsetAsync(scratch + kNaCounters, 0, 256, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(noalloc counters)");
+    float* scores = reinterpret_cast<float*>(scratch + kNaScores);
+    s = launch_router(d, L, scratch, x, w_gate, logits_in, M, logits_out, scores, xq, xq_scales, xq_sh, xq_sh_scales,
+                      st);
+    if (s != MOE_OK) return s;
+    s = launch_topk_route(d, L, scratch, M, scores, bias, topk_idx, topk_w, 1, 0, nullptr, nullptr, nullptr, nullptr,
+                          nullptr, st);
     if (s != MOE_OK) return s;
     return ok();
 }

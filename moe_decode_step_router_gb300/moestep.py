@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 EXPORTS = ("moe_last_error_string", "moe_packed_bytes", "moe_act_bytes", "moe_act_scale_bytes", "moe_hq_bytes",
            "moe_hq_scale_bytes", "moe_workspace_bytes", "moe_workspace_init", "moe_ws_view", "moe_pack_weights",
            "moe_router_topk", "moe_route_tiles", "moe_expert_gate_up", "moe_expert_down", "moe_finalize_norm",
-           "moe_step", "moe_get_status")
+           "moe_step", "moe_get_status", "moe_router_topk_noalloc")
 
 
 class MoeError(RuntimeError):
@@ -90,6 +90,7 @@ def lib():
             "moe_finalize_norm": (I32, [D, P, P, P, I32, P, P, P, P, P, P, P]),
             "moe_step": (I32, [D, ctypes.POINTER(StepArgs), I32, P, P]),
             "moe_get_status": (I32, [P, P, ctypes.POINTER(ctypes.c_int)]),
+            "moe_router_topk_noalloc": (I32, [D, P, P, P, P, I32, P, P, P, P, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -177,6 +178,13 @@ def moe_router_topk(d, x, w_gate, bias, logits_in, M, logits_out, topk_idx, topk
     _check(lib().moe_router_topk(ctypes.byref(d), _ptr(x), _ptr(w_gate), _ptr(bias), _ptr(logits_in), M,
                                  _ptr(logits_out), _ptr(topk_idx), _ptr(topk_w), _ptr(xq), _ptr(xq_scales),
                                  _ptr(xq_sh), _ptr(xq_sh_scales), _ptr(ws), _stream(stream)))
+
+
+def moe_router_topk_noalloc(d, x, w_gate, bias, logits_in, M, logits_out, topk_idx, topk_w, xq, xq_scales, xq_sh,
+                            xq_sh_scales, stream=None):
+    _check(lib().moe_router_topk_noalloc(ctypes.byref(d), _ptr(x), _ptr(w_gate), _ptr(bias), _ptr(logits_in), M,
+                                         _ptr(logits_out), _ptr(topk_idx), _ptr(topk_w), _ptr(xq), _ptr(xq_scales),
+                                         _ptr(xq_sh), _ptr(xq_sh_scales), _stream(stream)))
 
 
 def moe_route_tiles(d, topk_idx, M, tiles, num_tiles, perm, inv_perm, expert_counts, ws, stream=None):

@@ -1,0 +1,94 @@
+"""The allocation-free router entry point against the workspace one.
+
+moe_router_topk_noalloc is for callers that cannot hand the library device memory (a
+framework that owns every allocation, or a loop that must not allocate while running):
+its scratch is a fixed array inside the library. Called twice in a row, each time on new
+inputs, it must give what moe_router_topk gives on the same inputs: the same expert ids,
+weights, logits and quantised FC1 inputs (these are the same kernels, so the comparison is
+exact, which is within every tolerance the other tests use). Layers beyond its fixed
+scratch are refused before any launch.
+"""
+import numpy as np
+import pytest
+import torch
+
+from moe_decode_step_router_gb300 import moestep as ms
+from moe_decode_step_router_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    # 8 H-slices x 512 experts: exactly the scratch limit (ceil(H/512) * E = 4096)
+    "nvfp4_e512_limit": synth.config("nvfp4_h4096_e512_k10", M=8),
+    "mxfp8_bias": synth.config("mxfp8_h7168_e256_k8_8rows", M=13),
+    "nvfp4_bf16_shared": synth.config("nvfp4_h6144_e256_k8_16rows", M=16),
+}
+
+
+def _outputs(cfg, M):
+    d = "cuda"
+    E, k, H = cfg["E"], cfg["k"], cfg["H"]
+    fr, fs = cfg["w_fmt"], cfg["sh_fmt"]
+    return dict(
+        logits=torch.full((M, E), -1.0, dtype=torch.float32, device=d),
+        idx=torch.full((M, k), -1, dtype=torch.int32, device=d),
+        w=torch.full((M, k), -1.0, dtype=torch.float32, device=d),
+        xq=torch.zeros(ms.moe_act_bytes(fr, M, H), dtype=torch.uint8, device=d),
+        xs=torch.zeros(max(16, ms.moe_act_scale_bytes(fr, M, H)), dtype=torch.uint8, device=d),
+        xq_sh=torch.zeros(ms.moe_act_bytes(fs, M, H), dtype=torch.uint8, device=d),
+        xs_sh=torch.zeros(max(16, ms.moe_act_scale_bytes(fs, M, H)), dtype=torch.uint8, device=d))
+
+
+def _same(a, b):
+    for name in ("idx", "w", "logits", "xq", "xs", "xq_sh", "xs_sh"):
+        assert torch.equal(a[name], b[name]), name
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_noalloc_matches_workspace_entry_point_twice(name):
+    cfg = CASES[name]
+    M = cfg["M"]
+    d = ms.layer_desc(cfg, synth.act_global_scales(cfg))
+    ws = torch.empty(ms.moe_workspace_bytes(d), dtype=torch.uint8, device="cuda")
+    ms.moe_workspace_init(d, ws)
+    for seed in (3, 4):  # two calls in a row, on different inputs
+        inp = synth.make_inputs(cfg, seed, device="cuda", weights=False)
+        ref, got = _outputs(cfg, M), _outputs(cfg, M)
+        ms.moe_router_topk(d, inp["x"], inp["wg"], inp["bias"], None, M, ref["logits"], ref["idx"], ref["w"],
+                           ref["xq"], ref["xs"], ref["xq_sh"], ref["xs_sh"], ws)
+        ms.moe_router_topk_noalloc(d, inp["x"], inp["wg"], inp["bias"], None, M, got["logits"], got["idx"],
+                                   got["w"], got["xq"], got["xs"], got["xq_sh"], got["xs_sh"])
+        torch.cuda.synchronize()
+        assert (ref["idx"] >= 0).all() and (ref["w"] > 0).all()
+        _same(ref, got)
+
+
+def test_noalloc_with_given_logits_twice():
+    cfg = CASES["mxfp8_bias"]
+    M, E = cfg["M"], cfg["E"]
+    d = ms.layer_desc(cfg, synth.act_global_scales(cfg))
+    ws = torch.empty(ms.moe_workspace_bytes(d), dtype=torch.uint8, device="cuda")
+    ms.moe_workspace_init(d, ws)
+    inp = synth.make_inputs(cfg, 5, device="cuda", weights=False)
+    for seed in (11, 12):
+        li = torch.from_numpy(np.random.default_rng(seed).standard_normal((M, E)).astype(np.float32) * 2).cuda()
+        ref, got = _outputs(cfg, M), _outputs(cfg, M)
+        ms.moe_router_topk(d, inp["x"], inp["wg"], inp["bias"], li, M, ref["logits"], ref["idx"], ref["w"],
+                           ref["xq"], ref["xs"], ref["xq_sh"], ref["xs_sh"], ws)
+        ms.moe_router_topk_noalloc(d, inp["x"], inp["wg"], inp["bias"], li, M, got["logits"], got["idx"], got["w"],
+                                   got["xq"], got["xs"], got["xq_sh"], got["xs_sh"])
+        torch.cuda.synchronize()
+        _same(ref, got)
+
+
+def test_noalloc_refuses_layers_beyond_its_scratch():
+    cfg = synth.config("nvfp4_h4096_e512_k10", M=4, H=8192)  # 16 slices x 512 experts > 4096
+    d = ms.layer_desc(cfg, synth.act_global_scales(cfg))
+    o = _outputs(cfg, 4)
+    x = torch.zeros(4, cfg["H"], dtype=torch.bfloat16, device="cuda")
+    wg = torch.zeros(cfg["E"], cfg["H"], dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ms.MoeError) as err:
+        ms.moe_router_topk_noalloc(d, x, wg, None, None, 4, o["logits"], o["idx"], o["w"], o["xq"], o["xs"],
+                                   o["xq_sh"], o["xs_sh"])
+    assert err.value.status == ms.MOE_ERR_UNSUPPORTED and "scratch" in str(err.value)
+    assert (o["idx"] == -1).all()  # nothing was launched
