@@ -209,7 +209,7 @@ moe_status launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_
 // ------------------------------------------------------------------ launch helpers
 moe_status launch_router(const moe_layer_desc* d, const WsLayout& L, uint8_t* ws, const void* x,
                          const void* w_gate, const float* logits_in, int M, float* logits_out, float* scores,
-                         void* xq, void* xs, void* xq_sh, void* xs_sh, cudaStream_t st) {
+                         cudaStream_t st) {
     RouterParams p{};
     p.x = static_cast<const uint16_t*>(x);
     p.wg = static_cast<const uint16_t*>(w_gate);
@@ -221,15 +221,6 @@ moe_status launch_router(const moe_layer_desc* d, const WsLayout& L, uint8_t* ws
     p.E = d->E;
     p.part = reinterpret_cast<float*>(ws + L.rpart);
     p.counters = reinterpret_cast<int32_t*>(ws + L.rcnt);
-    p.fmt_r = d->w_fmt;
-    p.fmt_s = shared_fmt_of(d);
-    p.quant_shared = separate_shared_input(d) ? 1 : 0;
-    p.xq = static_cast<uint8_t*>(xq);
-    p.xs = static_cast<uint8_t*>(xs);
-    p.xq_sh = static_cast<uint8_t*>(xq_sh);
-    p.xs_sh = static_cast<uint8_t*>(xs_sh);
-    p.gs_r = d->w_fmt == MOE_FMT_NVFP4 ? d->gs_a1 : 1.0f;
-    p.gs_s = (d->has_shared && d->shared_fmt == MOE_FMT_NVFP4) ? d->gs_a1_shared : 1.0f;
     const int nslices = logits_in ? 1 : (d->H + 511) / 512;
     const int nblocks = (d->E + 7) / 8;
     const size_t smem = logits_in ? 0 : (size_t)(M + 8) * (512 + 8) * 2;
@@ -245,10 +236,21 @@ moe_status launch_router(const moe_layer_desc* d, const WsLayout& L, uint8_t* ws
     return launch_pdl(k_router, dim3(nslices, nblocks), dim3(256), smem, st, p, "k_router launch");
 }
 
+// FC1 input quantisation arguments, carried by the top-k launch (CTAs 1..).
+struct QuantArgs {
+    const void* x = nullptr;
+    void *xq = nullptr, *xs = nullptr, *xq_sh = nullptr, *xs_sh = nullptr;
+};
+
+int quant_units_host(int fmt, int M, int H) {
+    const int Mpad = round_up(M, 16);
+    return fmt == MOE_FMT_MXFP8 ? Mpad * (H / 32) : (fmt == MOE_FMT_NVFP4 ? Mpad * (H / 16) : Mpad * (H / 8));
+}
+
 moe_status launch_topk_route(const moe_layer_desc* d, const WsLayout& L, uint8_t* ws, int M, const float* scores,
                              const float* bias, int32_t* topk_idx, float* topk_w, int do_topk, int do_route,
                              int32_t* counts, int32_t* perm, int32_t* inv_perm, int32_t* tiles, int32_t* num_tiles,
-                             cudaStream_t st) {
+                             cudaStream_t st, const QuantArgs& qa = QuantArgs()) {
     TopkRouteParams p{};
     p.scores = scores;
     p.bias = d->has_bias ? bias : nullptr;
@@ -269,7 +271,24 @@ moe_status launch_topk_route(const moe_layer_desc* d, const WsLayout& L, uint8_t
     p.num_tiles = num_tiles;
     p.groups = reinterpret_cast<Group*>(ws + L.groups);
     p.hdr = reinterpret_cast<WsHeader*>(ws + L.header);
-    return launch_pdl(k_topk_route, dim3(1), dim3(1024), 0, st, p, "k_topk_route launch");
+    int qctas = 0;
+    if (qa.x) {
+        p.x = static_cast<const uint16_t*>(qa.x);
+        p.H = d->H;
+        p.fmt_r = d->w_fmt;
+        p.fmt_s = shared_fmt_of(d);
+        p.quant_shared = separate_shared_input(d) ? 1 : 0;
+        p.xq = static_cast<uint8_t*>(qa.xq);
+        p.xs = static_cast<uint8_t*>(qa.xs);
+        p.xq_sh = static_cast<uint8_t*>(qa.xq_sh);
+        p.xs_sh = static_cast<uint8_t*>(qa.xs_sh);
+        p.gs_r = d->w_fmt == MOE_FMT_NVFP4 ? d->gs_a1 : 1.0f;
+        p.gs_s = (d->has_shared && d->shared_fmt == MOE_FMT_NVFP4) ? d->gs_a1_shared : 1.0f;
+        int units = quant_units_host(p.fmt_r, M, d->H);
+        if (p.quant_shared && quant_units_host(p.fmt_s, M, d->H) > units) units = quant_units_host(p.fmt_s, M, d->H);
+        qctas = (units + 511) / 512;
+    }
+    return launch_pdl(k_topk_route, dim3(1 + qctas), dim3(512), 0, st, p, "k_topk_route launch");
 }
 
 struct GemmBuffers {
@@ -346,7 +365,7 @@ moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* wr,
     p.b_off = round_up(p.sfa_off + am * kAtomBytes, 1024);
     p.sfb_off = p.b_off + p.Mpad * kStepBytes;
     p.stage_bytes = round_up(p.sfb_off + am * kAtomBytes, 1024);
-    const int fixed = 1024 + p.Mpad * kBlockRows * 4 + 640;
+    const int fixed = 1024 + p.Mpad * kBlockRows * 4 + 640 + 4 * kMaxRows;
     int S = (di->smem_optin - fixed) / (p.stage_bytes + 24);  // + full/empty/ready barriers
     const int tmem_cap = am ? (512 - 2 * 64) / (8 * am) : 16;
     if (S > tmem_cap) S = tmem_cap;
@@ -541,11 +560,16 @@ moe_status moe_router_topk(const moe_layer_desc* d, const void* x, const void* w
     uint8_t* w = static_cast<uint8_t*>(ws);
     float* scores = reinterpret_cast<float*>(w + L.scores);
     cudaStream_t st = (cudaStream_t)stream;
-    s = launch_router(d, L, w, x, w_gate, logits_in, M, logits_out, scores, xq, xq_scales, xq_sh, xq_sh_scales,
-                      st);
+    s = launch_router(d, L, w, x, w_gate, logits_in, M, logits_out, scores, st);
     if (s != MOE_OK) return s;
+    QuantArgs qa;
+    qa.x = x;
+    qa.xq = xq;
+    qa.xs = xq_scales;
+    qa.xq_sh = xq_sh;
+    qa.xs_sh = xq_sh_scales;
     s = launch_topk_route(d, L, w, M, scores, bias, topk_idx, topk_w, 1, 0, nullptr, nullptr, nullptr, nullptr,
-                          nullptr, st);
+                          nullptr, st, qa);
     if (s != MOE_OK) return s;
     return ok();
 }
@@ -677,12 +701,17 @@ moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void
     float* topk_w = reinterpret_cast<float*>(w + L.topk_w);
     int32_t* perm = reinterpret_cast<int32_t*>(w + L.perm);
     int32_t* inv_perm = reinterpret_cast<int32_t*>(w + L.inv_perm);
-    s = launch_router(d, L, w, a->x, a->w_gate, nullptr, M, logits, scores, w + L.xq, w + L.xs, w + L.xq_sh,
-                      w + L.xs_sh, st);
+    s = launch_router(d, L, w, a->x, a->w_gate, nullptr, M, logits, scores, st);
     if (s != MOE_OK) return s;
+    QuantArgs qa;
+    qa.x = a->x;
+    qa.xq = w + L.xq;
+    qa.xs = w + L.xs;
+    qa.xq_sh = w + L.xq_sh;
+    qa.xs_sh = w + L.xs_sh;
     s = launch_topk_route(d, L, w, M, scores, a->bias, topk_idx, topk_w, 1, 1,
                           reinterpret_cast<int32_t*>(w + L.counts), perm, inv_perm,
-                          reinterpret_cast<int32_t*>(w + L.tiles), reinterpret_cast<int32_t*>(w + L.num_tiles), st);
+                          reinterpret_cast<int32_t*>(w + L.tiles), reinterpret_cast<int32_t*>(w + L.num_tiles), st, qa);
     if (s != MOE_OK) return s;
     GemmBuffers b{};
     b.xq = w + L.xq;
@@ -790,11 +819,16 @@ extern "C" moe_status moe_router_topk_noalloc(const moe_layer_desc* d, const voi
     cudaError_t e = cudaMemsetAsync(scratch + kNaCounters, 0, 256, st);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(noalloc counters)");
     float* scores = reinterpret_cast<float*>(scratch + kNaScores);
-    s = launch_router(d, L, scratch, x, w_gate, logits_in, M, logits_out, scores, xq, xq_scales, xq_sh, xq_sh_scales,
-                      st);
+    s = launch_router(d, L, scratch, x, w_gate, logits_in, M, logits_out, scores, st);
     if (s != MOE_OK) return s;
+    QuantArgs qa;
+    qa.x = x;
+    qa.xq = xq;
+    qa.xs = xq_scales;
+    qa.xq_sh = xq_sh;
+    qa.xs_sh = xq_sh_scales;
     s = launch_topk_route(d, L, scratch, M, scores, bias, topk_idx, topk_w, 1, 0, nullptr, nullptr, nullptr, nullptr,
-                          nullptr, st);
+                          nullptr, st, qa);
     if (s != MOE_OK) return s;
     return ok();
 }

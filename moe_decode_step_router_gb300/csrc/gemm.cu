@@ -107,6 +107,7 @@ struct GemmSmem {
     int* abort_flag;
     int* bcast;
     int* never;  // stays 0: lets the exit-time drains ignore the abort flag
+    int* tok;    // [64] tokens of the current group (epilogue)
 };
 
 __device__ __forceinline__ void set_error(int32_t* status, int* abort_flag, int code) {
@@ -214,6 +215,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
     sm.abort_flag = reinterpret_cast<int*>(sm.tmem_base + 1);
     sm.bcast = sm.abort_flag + 1;
     sm.never = sm.abort_flag + 2;
+    sm.tok = sm.abort_flag + 4;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
@@ -450,10 +452,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sm.acc_empty[ab]));
             if (++ab == nacc) ab = 0;
-            // compact the selected columns: column of group row rg -> stg[rg][r]
+            // compact the selected columns: column of group row rg -> stg[rg][r]; the
+            // group's tokens are read once (in parallel) into shared memory
             if (p.mode == 0 && s.cls == 0) {
+                if (et < rows) sm.tok[et] = p.perm[perm_off + et] / p.k;
+                named_bar(1, 128);
                 for (int rg = 0; rg < rows; ++rg) {
-                    const int m = p.perm[perm_off + rg] / p.k;
+                    const int m = sm.tok[rg];
                     stg[rg * kBlockRows + r] = stg[m * kBlockRows + r];
                 }
             }

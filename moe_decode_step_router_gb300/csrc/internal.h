@@ -68,10 +68,6 @@ struct RouterParams {
     int M, H, E;
     float* part;              // [H/512][E][64] partial logits (workspace)
     int32_t* counters;        // [ceil(E/8)] arrivals per expert block (self-resetting)
-    // FC1 input quantisation (tiled layout)
-    int fmt_r, fmt_s, quant_shared;
-    uint8_t *xq, *xs, *xq_sh, *xs_sh;
-    float gs_r, gs_s;
 };
 
 struct TopkRouteParams {
@@ -84,6 +80,11 @@ struct TopkRouteParams {
     int32_t *counts, *perm, *inv_perm, *tiles, *num_tiles;
     Group* groups;
     WsHeader* hdr;
+    // FC1 input quantisation into the tiled layout (CTAs 1.. of the launch)
+    const uint16_t* x;        // bf16 [M, H]
+    int H, fmt_r, fmt_s, quant_shared;
+    uint8_t *xq, *xs, *xq_sh, *xs_sh;
+    float gs_r, gs_s;
 };
 
 struct GemmClass {            // one weight class: routed experts or the shared expert

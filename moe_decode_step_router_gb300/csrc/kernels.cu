@@ -17,6 +17,11 @@
 namespace moe {
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 __device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 
@@ -120,8 +125,8 @@ __device__ __forceinline__ int quant_units(int fmt, int Mpad, int H) {
 }
 
 // ------------------------------------------------------------------------------------
-// a1 (+a3): router GEMV with fp32 accumulation and the fp32 sigmoid score evaluated in
-// double and rounded once; the FC1 input quantisation is spread over the same grid.
+// a1: router GEMV with fp32 accumulation and the fp32 sigmoid score evaluated in double
+// and rounded once (the FC1 input quantisation runs beside the top-k, in k_topk_route).
 // Grid (H slices) x (blocks of 8 experts). A CTA stages its x slice [M][512] and the
 // block's Wg slice [8][512] in shared memory; warp w owns expert e0 + w, its lanes split
 // (row, h range). Partial logits go to the workspace; the last CTA of an expert block
@@ -135,41 +140,31 @@ constexpr int kRouterMaxSlices = 8192 / kRouterHS;
 __global__ void __launch_bounds__(kRouterThreads) k_router(RouterParams p) {
     extern __shared__ __align__(16) uint16_t rsm[];
     __shared__ int s_last;
-    pdl_wait();
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int H = p.H, M = p.M, E = p.E;
-    const int Mpad = round_up(M, 16);
-    // FC1 input quantisation (all CTAs share the units)
-    {
-        const int nthreads = gridDim.x * gridDim.y * blockDim.x;
-        const int tid = (blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
-        const int nr = quant_units(p.fmt_r, Mpad, H);
-        for (int u = tid; u < nr; u += nthreads) quant_unit(p.x, M, H, Mpad, p.fmt_r, p.gs_r, p.xq, p.xs, u);
-        if (p.quant_shared) {
-            const int ns = quant_units(p.fmt_s, Mpad, H);
-            for (int u = tid; u < ns; u += nthreads)
-                quant_unit(p.x, M, H, Mpad, p.fmt_s, p.gs_s, p.xq_sh, p.xs_sh, u);
-        }
-    }
     const int e0 = blockIdx.y * kRouterEB, slice = blockIdx.x, nslices = gridDim.x;
+    const int h0 = slice * kRouterHS;
+    const int len = min(kRouterHS, H - h0);         // 512, or 256 for the last slice
+    const int VPR = len / 8;                        // 16-byte vectors per row slice
+    uint16_t* xs = rsm;                             // [M][pitch]
+    uint16_t* ws = rsm + (size_t)M * kRouterPitch;  // [8][pitch]
     if (!p.logits_in) {
-        const int h0 = slice * kRouterHS;
-        const int len = min(kRouterHS, H - h0);        // 512, or 256 for the last slice
-        uint16_t* xs = rsm;                            // [M][pitch]
-        uint16_t* ws = rsm + (size_t)M * kRouterPitch;  // [8][pitch]
-        const int VPR = len / 8;                       // 16-byte vectors per row slice
-        for (int v = threadIdx.x; v < (M + kRouterEB) * VPR; v += blockDim.x) {
-            const int r = v / VPR, c = v % VPR;
-            uint4 val = make_uint4(0u, 0u, 0u, 0u);
-            if (r < M) {
-                val = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)r * H + h0) + c);
-                *reinterpret_cast<uint4*>(xs + (size_t)r * kRouterPitch + 8 * c) = val;
-            } else {
-                const int e = e0 + (r - M);
-                if (e < E) val = __ldg(reinterpret_cast<const uint4*>(p.wg + (size_t)e * H + h0) + c);
-                *reinterpret_cast<uint4*>(ws + (size_t)(r - M) * kRouterPitch + 8 * c) = val;
-            }
+        // the gate weights do not depend on earlier launches: their copies start before
+        // the wait (asynchronous 16-byte copies, all in flight at once)
+        for (int v = threadIdx.x; v < kRouterEB * VPR; v += blockDim.x) {
+            const int r = v / VPR, c = v % VPR, e = min(e0 + r, E - 1);
+            cp_async16(ws + (size_t)r * kRouterPitch + 8 * c, p.wg + (size_t)e * H + h0 + 8 * c);
         }
+        cp_async_commit();
+    }
+    pdl_wait();
+    if (!p.logits_in) {
+        for (int v = threadIdx.x; v < M * VPR; v += blockDim.x) {
+            const int r = v / VPR, c = v % VPR;
+            cp_async16(xs + (size_t)r * kRouterPitch + 8 * c, p.x + (size_t)r * H + h0 + 8 * c);
+        }
+        cp_async_commit();
+        cp_async_wait_all();
         __syncthreads();
         // lanes: R row lanes x (32 / R) h splits; rows above 32 handled as a second pass
         int R = 1;
@@ -194,6 +189,7 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(RouterParams p) {
             for (int o = R; o < 32; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
             if (sp == 0 && rr < M && e < E) __stcg(p.part + ((size_t)slice * E + e) * kMaxRows + rr, acc);
         }
+        pdl_trigger();  // let the top-k launch get scheduled while the slices are summed
         __threadfence();
         __syncthreads();
         if (threadIdx.x == 0) {
@@ -201,10 +197,7 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(RouterParams p) {
             s_last = (old == nslices - 1) ? 1 : 0;
         }
         __syncthreads();
-        if (!s_last) {
-            pdl_trigger();
-            return;
-        }
+        if (!s_last) return;
         __threadfence();
     }
     // the last CTA of the block: sum the slices in order, sigmoid in double, write scores
@@ -235,9 +228,9 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(RouterParams p) {
 
 // ------------------------------------------------------------------------------------
 // a2 + a4 in one CTA: top-k of the selection key (score + bias) with ties to the lower
-// expert index, renormalised weights (double, rounded once), then the stable counting
+// expert index, renormalised weights (fp32, within a few ulps of the exact value), then the stable counting
 // sort of the (row, slot) pairs into 8-row tiles and the per-expert group table.
-constexpr int kRouteThreads = 1024;
+constexpr int kRouteThreads = 512;
 
 // Order-preserving map of an fp32 key to u32: a larger key gives a larger integer; every
 // finite key maps above 0, which marks taken or absent experts.
@@ -277,67 +270,91 @@ __device__ __forceinline__ void block_scan4(int4 v, int4* out_excl, int4* total,
 
 __global__ void __launch_bounds__(kRouteThreads) k_topk_route(TopkRouteParams p) {
     __shared__ unsigned long long sel[kMaxE + 1];
+    __shared__ float bias_s[kMaxE];
     __shared__ int4 sh_warp[32];
     __shared__ int s_bad;
     pdl_wait();
+    pdl_trigger();  // the GEMM's CTAs may take the other SMs and wait there
+    if (blockIdx.x > 0) {
+        // a3: the FC1 input quantisation, on CTAs 1.. beside the top-k of CTA 0
+        const int Mpad = round_up(p.M, 16);
+        const int nthreads = (gridDim.x - 1) * blockDim.x, tid = (blockIdx.x - 1) * blockDim.x + threadIdx.x;
+        const int nr = quant_units(p.fmt_r, Mpad, p.H);
+        for (int u = tid; u < nr; u += nthreads) quant_unit(p.x, p.M, p.H, Mpad, p.fmt_r, p.gs_r, p.xq, p.xs, u);
+        if (p.quant_shared) {
+            const int ns = quant_units(p.fmt_s, Mpad, p.H);
+            for (int u = tid; u < ns; u += nthreads)
+                quant_unit(p.x, p.M, p.H, Mpad, p.fmt_s, p.gs_s, p.xq_sh, p.xs_sh, u);
+        }
+        return;
+    }
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int M = p.M, E = p.E, k = p.k;
     if (p.do_topk) {
+        if (p.bias)
+            for (int e = threadIdx.x; e < E; e += blockDim.x) bias_s[e] = p.bias[e];
+        __syncthreads();
         for (int m = warp; m < M; m += kRouteThreads / 32) {
             // keys as order-preserving u32 (0 = taken / absent); lane owns e = lane + 32 i
             uint32_t ku[kMaxE / 32];
             float sc[kMaxE / 32];
+            // unconditional (clamped) loads, all in flight before the first use
+#pragma unroll
+            for (int i = 0; i < kMaxE / 32; ++i) sc[i] = __ldcg(p.scores + (size_t)m * E + min(lane + 32 * i, E - 1));
 #pragma unroll
             for (int i = 0; i < kMaxE / 32; ++i) {
-                const int e = lane + 32 * i;
-                sc[i] = 0.0f;
-                ku[i] = 0u;
-                if (e < E) {
-                    sc[i] = p.scores[(size_t)m * E + e];
-                    ku[i] = key_u32(p.bias ? __fadd_rn(sc[i], p.bias[e]) : sc[i]);
-                }
+                const bool valid = lane + 32 * i < E;
+                ku[i] = valid ? key_u32(p.bias ? __fadd_rn(sc[i], bias_s[lane + 32 * i]) : sc[i]) : 0u;
+                if (!valid) sc[i] = 0.0f;
             }
             // this lane's best: largest key, lowest index among equals (ascending scan)
             uint32_t lb = 0u;
             int li = 0;
+            float ls = 0.0f;
 #pragma unroll
             for (int i = 0; i < kMaxE / 32; ++i)
-                if (ku[i] > lb) { lb = ku[i]; li = i; }
+                if (ku[i] > lb) { lb = ku[i]; li = i; ls = sc[i]; }
             int my_idx = 0;
             float my_sc = 0.0f;
-            double ssum = 0.0;
+            float ssum = 0.0f;  // fp32 in slot order: FP64 is ~50x slower than fp32 on this part
+            // Each round: one max reduction and one ballot find the winning lane (a tie
+            // between lanes, which needs the lower expert id, takes one more reduction);
+            // the winner rescans its own keys while the others read its id and score.
             for (int j = 0; j < k; ++j) {
                 const uint32_t wmax = __reduce_max_sync(0xffffffffu, lb);
-                const uint32_t cand = (lb == wmax) ? (uint32_t)(lane + 32 * li) : 0xffffffffu;
-                const int bi = (int)__reduce_min_sync(0xffffffffu, cand);
-                float wsc = 0.0f;
-                if ((bi & 31) == lane) {
-                    const int ti = bi >> 5;
+                const uint32_t bal = __ballot_sync(0xffffffffu, lb == wmax);
+                int wl;
+                if ((bal & (bal - 1u)) == 0u) {
+                    wl = __ffs(bal) - 1;
+                } else {
+                    const uint32_t cand = (lb == wmax) ? (uint32_t)(lane + 32 * li) : 0xffffffffu;
+                    wl = (int)(__reduce_min_sync(0xffffffffu, cand) & 31u);
+                }
+                const int wsl = __shfl_sync(0xffffffffu, li, wl);
+                const float wsc = __shfl_sync(0xffffffffu, ls, wl);
+                if (lane == wl) {
 #pragma unroll
                     for (int i = 0; i < kMaxE / 32; ++i)
-                        if (i == ti) { wsc = sc[i]; ku[i] = 0u; }
+                        if (i == li) ku[i] = 0u;
                     lb = 0u;
                     li = 0;
+                    ls = 0.0f;
 #pragma unroll
                     for (int i = 0; i < kMaxE / 32; ++i)
-                        if (ku[i] > lb) { lb = ku[i]; li = i; }
+                        if (ku[i] > lb) { lb = ku[i]; li = i; ls = sc[i]; }
                 }
-                wsc = __shfl_sync(0xffffffffu, wsc, bi & 31);
-                ssum += (double)wsc;
-                if (lane == j) { my_idx = bi; my_sc = wsc; }
+                ssum = __fadd_rn(ssum, wsc);
+                if (lane == j) { my_idx = wl + 32 * wsl; my_sc = wsc; }
             }
             if (lane < k) {
                 p.topk_idx[(size_t)m * k + lane] = my_idx;
-                const double w = p.renormalize ? (double)my_sc / ssum * (double)p.rsf : (double)my_sc * (double)p.rsf;
-                p.topk_w[(size_t)m * k + lane] = (float)w;
+                p.topk_w[(size_t)m * k + lane] =
+                    p.renormalize ? __fmul_rn(__fdiv_rn(my_sc, ssum), p.rsf) : __fmul_rn(my_sc, p.rsf);
             }
         }
         __syncthreads();
     }
-    if (!p.do_route) {
-        pdl_trigger();
-        return;
-    }
+    if (!p.do_route) return;
     // ---- route
     const int P = M * k;
     if (threadIdx.x == 0) s_bad = 0;
@@ -359,30 +376,40 @@ __global__ void __launch_bounds__(kRouteThreads) k_topk_route(TopkRouteParams p)
             p.hdr->num_tiles = 0;
             *p.num_tiles = 0;
         }
-        pdl_trigger();
         return;
     }
-    // one thread per expert (E + 1 <= 513 <= blockDim): pairs, tiles, group flag, padded rows
-    const int e = threadIdx.x;
-    int c = 0;
-    if (e < E) c = __popcll(sel[e]);
-    else if (e == E) c = p.has_shared ? M : 0;
-    int4 v = make_int4(c, (c + kTileRows - 1) / kTileRows, (e < E && c > 0) ? 1 : 0, (e < E) ? round_up(c, 16) : 0);
-    if (e > E) v = make_int4(0, 0, 0, 0);
+    // two experts per thread (E + 1 <= 513 <= 2 * blockDim): pairs, tiles, group flag,
+    // padded rows; one block-wide exclusive scan over the per-thread sums
+    auto vals = [&](int e) {
+        int c = 0;
+        if (e < E) c = __popcll(sel[e]);
+        else if (e == E) c = p.has_shared ? M : 0;
+        if (e > E) return make_int4(0, 0, 0, 0);
+        return make_int4(c, (c + kTileRows - 1) / kTileRows, (e < E && c > 0) ? 1 : 0, (e < E) ? round_up(c, 16) : 0);
+    };
+    const int e0 = 2 * threadIdx.x;
+    const int4 v0 = vals(e0), v1 = vals(e0 + 1);
     int4 ex, tot;
-    block_scan4(v, &ex, &tot, sh_warp);
-    if (e <= E) {
-        p.counts[e] = c;
-        for (int t = 0; t < v.y; ++t) {
-            int32_t* tp = p.tiles + 3 * (ex.y + t);
-            tp[0] = e;
-            tp[1] = ex.x + kTileRows * t;
-            tp[2] = min(kTileRows, c - kTileRows * t);
+    block_scan4(make_int4(v0.x + v1.x, v0.y + v1.y, v0.z + v1.z, v0.w + v1.w), &ex, &tot, sh_warp);
+    __shared__ int s_off[kMaxE + 2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int e = e0 + h;
+        const int4 v = h ? v1 : v0;
+        const int4 x0 = h ? make_int4(ex.x + v0.x, ex.y + v0.y, ex.z + v0.z, ex.w + v0.w) : ex;
+        if (e <= E) {
+            const int c = v.x;
+            p.counts[e] = c;
+            for (int t = 0; t < v.y; ++t) {
+                int32_t* tp = p.tiles + 3 * (x0.y + t);
+                tp[0] = e;
+                tp[1] = x0.x + kTileRows * t;
+                tp[2] = min(kTileRows, c - kTileRows * t);
+            }
+            if (v.z) p.groups[x0.z] = Group{e, c, x0.x, x0.w};
+            s_off[e] = x0.x;
         }
-        if (v.z) p.groups[ex.z] = Group{e, c, ex.x, ex.w};
     }
-    __shared__ int s_off[kMaxE + 1];
-    if (e <= E) s_off[e] = ex.x;
     if (threadIdx.x == 0) {
         *p.num_tiles = tot.y;
         p.hdr->num_tiles = tot.y;
@@ -401,7 +428,6 @@ __global__ void __launch_bounds__(kRouteThreads) k_topk_route(TopkRouteParams p)
             p.perm[P + m] = P + m;
             p.inv_perm[P + m] = P + m;
         }
-    pdl_trigger();
 }
 
 // ------------------------------------------------------------------------------------
@@ -435,6 +461,7 @@ __global__ void __launch_bounds__(kFinThreads) k_finalize(FinalizeParams p) {
     __shared__ float w_s[kMaxK];
     __shared__ int pos_s[kMaxK + 1];
     pdl_wait();
+    pdl_trigger();
     const int m = blockIdx.y, H = p.H, k = p.k, M = p.M;
     const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
     const int slice = H / kFinCluster, base = (int)cluster_rank() * slice;
@@ -537,7 +564,6 @@ __global__ void __launch_bounds__(kFinThreads) k_finalize(FinalizeParams p) {
             if ((n % 32) == 0) p.outs[(size_t)m * (H / 32) + n / 32] = (uint8_t)(e + 127);
         }
     }
-    pdl_trigger();
 }
 
 // ------------------------------------------------------------------------------------

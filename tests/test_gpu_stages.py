@@ -129,7 +129,8 @@ def test_stages_against_oracle(name, M):
     torch.cuda.synchronize()
     _, _, oidx, ow, _ = oracle.router(L, x16, wg16, bias=bias, logits_in=li)
     assert (npy(t["idx"]) == oidx).all()
-    assert (npy(t["w"]) == ow.astype(np.float32)).all()
+    # weights: fp32 sum and division on the GPU (a few ulps) vs the oracle's double
+    assert np.allclose(npy(t["w"]), ow, rtol=2 ** -20, atol=0)
     fr, fs = cfg["w_fmt"], cfg["sh_fmt"]
     gs_a1, gs_a2, gs_a1s, gs_a2s = inp["gs_a"]
     oq, osc = oracle.quant_x(fr, x16, gs_a1)
