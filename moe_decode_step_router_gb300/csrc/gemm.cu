@@ -234,6 +234,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
         *sm.never = 0;
         fence_mbar_init();
     }
+    // The shared expert's weights do not depend on the routing: while the earlier kernels
+    // of the step still run (HBM is otherwise idle then), every CTA prefetches its 1/G
+    // share of them into L2. They are consumed at the end of the step space; the routed
+    // weights streamed meanwhile carry an evict-first hint.
+    if (threadIdx.x == 32 && p.has_shared) {
+        const GemmClass& C1 = p.cls[1];
+        const size_t total = (size_t)C1.MB * C1.KS * record_bytes(C1.fmt);
+        const size_t share = (total / gridDim.x + 15) & ~(size_t)15;
+        const size_t b0 = (size_t)blockIdx.x * share;
+        const size_t b1 = b0 + share < total ? b0 + share : total;
+        for (size_t o = b0; o < b1; o += 65536) {
+            const size_t n = b1 - o < 65536 ? b1 - o : 65536;
+            prefetch_l2(C1.w + o, (uint32_t)n);
+        }
+    }
     // Everything below reads the previous launches' outputs.
     pdl_wait();
     if (warp == 1) {

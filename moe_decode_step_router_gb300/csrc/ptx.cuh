@@ -72,6 +72,10 @@ __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uin
         "l"(src), "r"(bytes), "r"(bar), "l"(policy)
         : "memory");
 }
+// Prefetch a 16-byte-aligned range (size a multiple of 16) into L2, no destination.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
