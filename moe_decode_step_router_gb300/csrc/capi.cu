@@ -358,7 +358,7 @@ moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* wr,
                                                                                 : atoms_per_step(p.cls[1].fmt);
     p.atoms_max = am;
     // NVFP4 stages carry 8 scale copies; issuing them from two extra warps keeps the MMA
-    // thread's issue stream short. MXFP8-only launches copy in the MMA thread (one hop less).
+    // issuers' streams short. MXFP8-only launches copy in the issuers (one hop less).
     p.sf_warps = am == 4 ? 1 : 0;
     p.a_off = 0;
     p.sfa_off = kBlockRows * kStepBytes;
@@ -367,7 +367,7 @@ moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* wr,
     p.stage_bytes = round_up(p.sfb_off + am * kAtomBytes, 1024);
     const int fixed = 1024 + p.Mpad * kBlockRows * 4 + 640 + 4 * kMaxRows;
     int S = (di->smem_optin - fixed) / (p.stage_bytes + 24);  // + full/empty/ready barriers
-    const int tmem_cap = am ? (512 - 2 * 64) / (8 * am) : 16;
+    const int tmem_cap = am ? (512 - 2 * acc_bank_cols(am, p.Mpad)) / (8 * am) : 16;
     if (S > tmem_cap) S = tmem_cap;
     if (S > 16) S = 16;
     if (S < 2) return fail(MOE_ERR_UNSUPPORTED, "not enough shared memory for the GEMM pipeline");
@@ -381,7 +381,7 @@ moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* wr,
     }
     int grid = di->sms;
     if (grid > kMaxGemmCtas) grid = kMaxGemmCtas;
-    return launch_pdl(k_expert_gemm, dim3(grid), dim3(256), smem, st, p,
+    return launch_pdl(k_expert_gemm, dim3(grid), dim3(kGemmThreads), smem, st, p,
                       mode == 0 ? "k_expert_gemm(gate_up) launch" : "k_expert_gemm(down) launch");
 }
 

@@ -15,11 +15,15 @@
 // by the last CTA to finish a piece, in piece order (deterministic).
 //
 // Roles: warp 0 lane 0 issues the bulk copies (weight record + activation tile + its
-// scales) into a ring of shared-memory stages; in launches with NVFP4 weights warps 6
-// and 7 copy each stage's A and B block scales into tensor memory (otherwise the MMA
-// thread does it); warp 1 lane 0 issues the MMAs into one of two TMEM
-// accumulators; warps 2..5 drain the accumulator and run the epilogue (gate_up: SwiGLU
-// + requantisation into the tiled FC2 input; down: fp32 rows in perm order).
+// scales) into a ring of shared-memory stages. Two MMA issuers (lane 0 of warps 1 and 6)
+// consume the even and the odd ring slots, each accumulating into its own TMEM bank: at
+// 8-64 rows one thread's tcgen05 issue rate, not the tensor pipe, caps the bytes a CTA
+// can consume, and two issuers double that cap. In launches with NVFP4 weights (4 scale
+// atoms per operand and step) warps 7..10 copy the stages' A and B block scales into
+// tensor memory, two atoms each; otherwise each issuer copies the scales of its slots.
+// Either way a slot's scale columns always have the same writer. Warps 2..5 add the two
+// banks and run the epilogue (gate_up: SwiGLU + requantisation into the tiled FC2 input;
+// down: fp32 rows in perm order).
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -28,65 +32,112 @@
 
 namespace moe {
 
-constexpr int kGemmThreads = 256;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint32_t kTmemCols = 512;
-constexpr int kAccCols = 64;   // two buffers of 64 columns = the 128-column accumulator region
-constexpr int kMaxAcc = 8;    // up to 8 buffers of round_up(M,16) columns in that region
+constexpr int kMaxAcc = 8;  // up to 8 accumulator buffers per bank
 
+// One segment: the steps [ka, kb) of unit (cls, g, b) that fall in this CTA's range, with
+// the facts of the unit's group.
 struct Seg {
     int cls, g, b, ka, kb, KS;
     long long unit, us;  // global unit id, first global step of the unit
+    int expert, rows, perm_off, row_off, gidx;
 };
 
+__device__ __forceinline__ int4 ld_group(const Group* gp) {
+    int4 v;
+    asm volatile("ld.global.nc.v4.s32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(gp));
+    return v;
+}
+
+// Walks this CTA's contiguous range of the step space (routed units in group order, then
+// the shared expert's units). The position is advanced incrementally (no divisions after
+// the start) and each group record is loaded one group ahead, so a segment boundary costs
+// a few instructions instead of dependent divisions and a load round trip.
 struct Walker {
+    const Group* groups;
     long long T_r, T, t, t1;
-    int MB0, KS0, MB1, KS1;
-    long long NR_units;
+    int ngroups, MB0, KS0, MB1, KS1, M, ktop;
+    int cls, g, b, k;  // position of step t
+    int4 cur, nxt;     // records of groups g and g + 1
     // Effective grid: never more CTAs than steps, so every working CTA owns at least one
     // step and the CTAs whose ranges meet a unit are exactly its pieces.
     __device__ static long long total_steps(const GemmParams& p, int ngroups) {
         return (long long)ngroups * p.cls[0].MB * p.cls[0].KS + (p.has_shared ? (long long)p.cls[1].MB * p.cls[1].KS : 0);
     }
-    __device__ void init(const GemmParams& p, int ngroups, int G, int c) {
+    __device__ void init(const GemmParams& p, int ngroups_, int G, int c) {
+        groups = p.groups;
+        ngroups = ngroups_;
         MB0 = p.cls[0].MB;
         KS0 = p.cls[0].KS;
         MB1 = p.cls[1].MB;
         KS1 = p.cls[1].KS;
-        NR_units = (long long)ngroups * MB0;
-        T_r = NR_units * KS0;
+        M = p.M;
+        ktop = p.k;
+        T_r = (long long)ngroups * MB0 * KS0;
         T = T_r + (p.has_shared ? (long long)MB1 * KS1 : 0);
-        if (c >= G || T == 0) {
-            t = t1 = 0;
-            return;
-        }
+        t = t1 = 0;
+        if (c >= G || T == 0) return;
         t = (long long)c * T / G;
         t1 = (long long)(c + 1) * T / G;
-    }
-    __device__ bool next(Seg& s) {
-        if (t >= t1) return false;
         if (t < T_r) {
             const long long u = t / KS0;
-            s.cls = 0;
-            s.KS = KS0;
-            s.g = (int)(u / MB0);
-            s.b = (int)(u % MB0);
-            s.ka = (int)(t - u * KS0);
-            s.unit = u;
-            s.us = u * KS0;
+            cls = 0;
+            g = (int)(u / MB0);
+            b = (int)(u - (long long)g * MB0);
+            k = (int)(t - u * KS0);
+            cur = ld_group(groups + g);
+            nxt = ld_group(groups + (g + 1 < ngroups ? g + 1 : g));
         } else {
-            const long long tt = t - T_r, u = tt / KS1;
-            s.cls = 1;
-            s.KS = KS1;
-            s.g = -1;
-            s.b = (int)u;
-            s.ka = (int)(tt - u * KS1);
-            s.unit = NR_units + u;
-            s.us = T_r + u * KS1;
+            const long long tt = t - T_r;
+            cls = 1;
+            g = ngroups;
+            b = (int)(tt / KS1);
+            k = (int)(tt - (long long)b * KS1);
         }
+    }
+    __device__ __forceinline__ bool next(Seg& s) {
+        if (t >= t1) return false;
+        const int KS = cls ? KS1 : KS0;
+        s.cls = cls;
+        s.g = cls ? -1 : g;
+        s.b = b;
+        s.KS = KS;
+        s.ka = k;
         const long long room = t1 - t;
-        s.kb = (int)((long long)s.ka + room < (long long)s.KS ? s.ka + room : s.KS);
+        s.kb = room < (long long)(KS - k) ? k + (int)room : KS;
+        s.us = t - k;
+        if (cls == 0) {
+            s.unit = (long long)g * MB0 + b;
+            s.expert = cur.x;
+            s.rows = cur.y;
+            s.perm_off = cur.z;
+            s.row_off = cur.w;
+            s.gidx = g;
+        } else {
+            s.unit = (long long)ngroups * MB0 + b;
+            s.expert = 0;
+            s.rows = M;
+            s.perm_off = M * ktop;
+            s.row_off = 0;
+            s.gidx = 0;
+        }
         t += s.kb - s.ka;
+        k = s.kb;
+        if (k == KS) {
+            k = 0;
+            if (++b == (cls ? MB1 : MB0)) {
+                b = 0;
+                if (cls == 0) {
+                    if (++g == ngroups) {
+                        cls = 1;
+                    } else {
+                        cur = nxt;
+                        nxt = ld_group(groups + (g + 1 < ngroups ? g + 1 : g));
+                    }
+                }
+            }
+        }
         return true;
     }
     __device__ long long start(long long c, int G) const { return c * T / G; }
@@ -95,12 +146,12 @@ struct Walker {
 
 struct GemmSmem {
     uint8_t* ring;
-    float* stg;  // [kAccCols][128] fp32 epilogue staging
+    float* stg;  // [Mpad][128] fp32 epilogue staging
     uint64_t* full;
     uint64_t* empty;
     uint64_t* acc_full;
     uint64_t* acc_empty;
-    uint64_t* drain;
+    uint64_t* drain;     // [2] per MMA issuer
     uint64_t* sf_ready;  // [S] scale factors of the stage are in tensor memory
     uint64_t* sf_drain;
     uint32_t* tmem_base;
@@ -121,46 +172,58 @@ __device__ __forceinline__ float warp_max_f(float v) {
     return v;
 }
 
-// Group facts of a segment.
-__device__ __forceinline__ void seg_group(const GemmParams& p, const Seg& s, int& expert, int& rows, int& perm_off,
-                                          int& row_off, int& gidx) {
-    if (s.cls == 0) {
-        const Group gr = p.groups[s.g];
-        expert = gr.expert;
-        rows = gr.rows;
-        perm_off = gr.perm_off;
-        row_off = gr.row_off;
-        gidx = s.g;
-    } else {
-        expert = 0;
-        rows = p.M;
-        perm_off = p.M * p.k;
-        row_off = 0;
-        gidx = 0;
+// Position in the ring of shared-memory stages: slot and the parity of its lap.
+struct Ring {
+    int st;
+    uint32_t ph;
+    int S;  // >= 2
+    __device__ __forceinline__ void adv1() {
+        if (++st == S) {
+            st = 0;
+            ph ^= 1u;
+        }
     }
+};
+
+// Accumulator banks written by a segment of n steps whose first step sits in ring slot
+// st0 (bit b: some step sits in a slot of parity b, consumed by issuer b). Any three
+// consecutive slots include both parities.
+__device__ __forceinline__ uint32_t bank_mask(int st0, int n, int S) {
+    uint32_t m = 0;
+    for (int i = 0; i < n && i < 3; ++i) {
+        m |= 1u << (st0 & 1);
+        if (++st0 == S) st0 = 0;
+    }
+    return m;
 }
 
-// Issues the MMAs of one segment from the single MMA thread. At small N the issue stream
-// of that thread, not the tensor pipe, limits the rate, so the scale-factor copies run
-// on their own warp and every descriptor is precomputed and advanced with integer adds
-// (a shared-memory descriptor holds address >> 4 in its low 14 bits: +16 bytes is +1);
-// the format branch is taken once per segment.
+// Issues this issuer's MMAs of one segment: the steps of [ka, kb) that sit in ring slots
+// of parity par, accumulated into d_tmem (the first of them overwrites it); the ring
+// position advances over every step. Returns -1 on a timeout, else the number of steps
+// issued. At small N the issue stream of a thread, not the tensor pipe, limits the rate,
+// so every descriptor is precomputed and advanced with integer adds (a shared-memory
+// descriptor holds address >> 4 in its low 14 bits: +16 bytes is +1) and the format
+// branch is taken once per segment.
 template <int FMT, bool CP>
-__device__ __forceinline__ bool mma_segment(uint32_t ready0, uint32_t empty0, int& st, uint32_t& ph, int S, int ka,
-                                            int kb, uint64_t adesc0, uint64_t bdesc0, uint64_t sfadesc0,
-                                            uint64_t sfbdesc0, uint32_t stage16, uint32_t d_tmem, uint32_t sf_t0,
-                                            uint32_t sf_stride, uint32_t sfb_cols, uint32_t N, volatile int* abort) {
+__device__ __forceinline__ int mma_segment(uint32_t ready0, uint32_t empty0, Ring& rg, int ka, int kb, int par,
+                                           uint64_t adesc0, uint64_t bdesc0, uint64_t sfadesc0, uint64_t sfbdesc0,
+                                           uint32_t stage16, uint32_t d_tmem, uint32_t sf_t0, uint32_t sf_stride,
+                                           uint32_t sfb_cols, uint32_t N, volatile int* abort) {
+    static_assert(!(CP && FMT == MOE_FMT_NVFP4), "NVFP4 scales are copied by the copy warps");
     uint32_t id[4];
 #pragma unroll
     for (int sub = 0; sub < 4; ++sub)
         id[sub] = FMT == MOE_FMT_MXFP8 ? idesc_mxf8(N, sub) : (FMT == MOE_FMT_NVFP4 ? idesc_nvf4(N) : idesc_bf16(N));
-    for (int kk = ka; kk < kb; ++kk) {
-        if (!mbar_wait_bounded(ready0 + 8u * st, ph, abort, kWaitLimitNs)) return false;
+    int issued = 0;
+    for (int kk = ka; kk < kb; ++kk, rg.adv1()) {
+        const int st = rg.st;
+        if ((st & 1) != par) continue;
+        if (!mbar_wait_bounded(ready0 + 8u * st, rg.ph, abort, kWaitLimitNs)) return -1;
         tc_fence_after();
         const uint64_t so = (uint64_t)st * stage16;
         const uint64_t ad = adesc0 + so, bd = bdesc0 + so;
         const uint32_t sfa = sf_t0 + (uint32_t)st * sf_stride, sfb = sfa + sfb_cols;
-        const uint32_t acc0 = kk > ka ? 1u : 0u;
+        const uint32_t acc0 = issued ? 1u : 0u;
         if (FMT == MOE_FMT_MXFP8) {
             if (CP) {
                 tc_cp_sf(sfa, sfadesc0 + so);
@@ -170,13 +233,6 @@ __device__ __forceinline__ bool mma_segment(uint32_t ready0, uint32_t empty0, in
             for (int sub = 0; sub < 4; ++sub)
                 mma_mxf8(d_tmem, ad + 2 * sub, bd + 2 * sub, id[sub], sfa, sfb, sub ? 1u : acc0);
         } else if (FMT == MOE_FMT_NVFP4) {
-            if (CP) {
-#pragma unroll
-                for (int a = 0; a < 4; ++a) {
-                    tc_cp_sf(sfa + 4 * a, sfadesc0 + so + 32 * a);
-                    tc_cp_sf(sfb + 4 * a, sfbdesc0 + so + 32 * a);
-                }
-            }
 #pragma unroll
             for (int sub = 0; sub < 4; ++sub)
                 mma_nvf4(d_tmem, ad + 2 * sub, bd + 2 * sub, id[sub], sfa + 4 * sub, sfb + 4 * sub, sub ? 1u : acc0);
@@ -185,12 +241,9 @@ __device__ __forceinline__ bool mma_segment(uint32_t ready0, uint32_t empty0, in
             for (int sub = 0; sub < 4; ++sub) mma_bf16(d_tmem, ad + 2 * sub, bd + 2 * sub, id[sub], sub ? 1u : acc0);
         }
         tc_commit(empty0 + 8u * st);
-        if (++st == S) {
-            st = 0;
-            ph ^= 1u;
-        }
+        ++issued;
     }
-    return true;
+    return issued;
 }
 
 __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_constant__ GemmParams p) {
@@ -209,9 +262,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
     sm.acc_full = sm.empty + S;
     sm.acc_empty = sm.acc_full + kMaxAcc;
     sm.drain = sm.acc_empty + kMaxAcc;
-    sm.sf_ready = sm.drain + 1;
+    sm.sf_ready = sm.drain + 2;
     sm.sf_drain = sm.sf_ready + S;
-    sm.tmem_base = reinterpret_cast<uint32_t*>(sm.sf_drain + 2);
+    sm.tmem_base = reinterpret_cast<uint32_t*>(sm.sf_drain + 4);
     sm.abort_flag = reinterpret_cast<int*>(sm.tmem_base + 1);
     sm.bcast = sm.abort_flag + 1;
     sm.never = sm.abort_flag + 2;
@@ -223,13 +276,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             mbar_init(smem_u32(&sm.empty[i]), 1);
         }
         for (int i = 0; i < kMaxAcc; ++i) {
-            mbar_init(smem_u32(&sm.acc_full[i]), 1);
+            mbar_init(smem_u32(&sm.acc_full[i]), 2);  // one arrival per MMA issuer
             mbar_init(smem_u32(&sm.acc_empty[i]), 4);
         }
-        mbar_init(smem_u32(sm.drain), 1);
-        for (int i = 0; i < S; ++i) mbar_init(smem_u32(&sm.sf_ready[i]), 2);
-        mbar_init(smem_u32(&sm.sf_drain[0]), 1);
-        mbar_init(smem_u32(&sm.sf_drain[1]), 1);
+        mbar_init(smem_u32(&sm.drain[0]), 1);
+        mbar_init(smem_u32(&sm.drain[1]), 1);
+        for (int i = 0; i < S; ++i) mbar_init(smem_u32(&sm.sf_ready[i]), 4);  // one per copy warp
+        for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&sm.sf_drain[i]), 1);
         *sm.abort_flag = 0;
         *sm.never = 0;
         fence_mbar_init();
@@ -258,9 +311,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *sm.tmem_base;
-    // accumulator buffers of Mpad columns each in the 128-column region: the MMA thread
-    // runs up to nacc - 1 units ahead of the epilogue
-    const int nacc = min(kMaxAcc, 2 * kAccCols / p.Mpad);
+    // two accumulator banks of nacc buffers (Mpad columns each): the MMA issuers run up to
+    // nacc - 1 units ahead of the epilogue
+    const int bank = acc_bank_cols(p.atoms_max, p.Mpad);
+    const int nacc = min(kMaxAcc, bank / p.Mpad);
     pdl_trigger();
 
     const int ngroups = p.hdr->num_groups;
@@ -281,8 +335,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             bool ok = true;
             while (ok && wk.next(s)) {
                 const GemmClass& C = p.cls[s.cls];
-                int expert, rows, perm_off, row_off, gidx;
-                seg_group(p, s, expert, rows, perm_off, row_off, gidx);
                 const int A = atoms_per_step(C.fmt);
                 const uint32_t REC = record_bytes(C.fmt);
                 int Rpad;
@@ -292,11 +344,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                     bsrc = C.b;
                     bssrc = C.bs;
                 } else {
-                    Rpad = (s.cls == 0) ? round_up(rows, 16) : p.Mpad;
-                    bsrc = C.b + (size_t)row_off * C.KS * kStepBytes;
-                    bssrc = C.bs + (size_t)gidx * C.KS * A * kAtomBytes;
+                    Rpad = (s.cls == 0) ? round_up(s.rows, 16) : p.Mpad;
+                    bsrc = C.b + (size_t)s.row_off * C.KS * kStepBytes;
+                    bssrc = C.bs + (size_t)s.gidx * C.KS * A * kAtomBytes;
                 }
-                const uint8_t* wrec = C.w + ((size_t)((size_t)expert * C.MB + s.b) * C.KS + s.ka) * REC;
+                const uint8_t* wrec = C.w + ((size_t)((size_t)s.expert * C.MB + s.b) * C.KS + s.ka) * REC;
                 const uint32_t bbytes = (uint32_t)Rpad * kStepBytes;
                 for (int kk = s.ka; kk < s.kb; ++kk) {
                     if (!mbar_wait_bounded(smem_u32(&sm.empty[st]), ph ^ 1u, abort_flag, kWaitLimitNs)) {
@@ -327,19 +379,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                 mbar_wait_bounded(smem_u32(&sm.full[i]), par, sm.never, kWaitLimitNs / 2);
             }
         }
-    } else if (warp == 1) {
-        // ================================================================ MMA issuer
+    } else if (warp == 1 || warp == 6) {
+        // ================================================================ MMA issuers
+        // warp 1 consumes the even ring slots (bank 0), warp 6 the odd ones (bank 1)
         if (lane == 0) {
+            const int par = warp == 6 ? 1 : 0;
             Walker wk;
             wk.init(p, ngroups, G, c);
             Seg s;
-            int st = 0;
-            uint32_t ph = 0;
+            Ring rg{0, 0u, S};
             int ab = 0;
             uint32_t acc_ph = 0u;  // bit b: phase of accumulator buffer b
-            bool ok = true;
             const int am = p.atoms_max;
-            // with copy warps the MMA thread waits for the stage's scales, else for its data
+            // with copy warps the issuers wait for the stage's scales, else for its data
             const uint32_t wait0 = p.sf_warps ? smem_u32(&sm.sf_ready[0]) : smem_u32(&sm.full[0]);
             const uint32_t empty0 = smem_u32(&sm.empty[0]);
             const uint32_t ring = smem_u32(sm.ring);
@@ -348,90 +400,97 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             const uint64_t sfadesc0 = smem_desc(ring + p.sfa_off, 0, 128, 0);
             const uint64_t sfbdesc0 = smem_desc(ring + p.sfb_off, 0, 128, 0);
             const uint32_t stage16 = (uint32_t)p.stage_bytes >> 4;
-            const uint32_t sf_t0 = tmem + 2 * kAccCols;
-            while (ok && wk.next(s)) {
+            const uint32_t sf_t0 = tmem + 2 * bank;
+            const uint32_t bank_t = tmem + (uint32_t)(par * bank);
+            while (wk.next(s)) {
                 const GemmClass& C = p.cls[s.cls];
-                int expert, rows, perm_off, row_off, gidx;
-                seg_group(p, s, expert, rows, perm_off, row_off, gidx);
-                const uint32_t N = (p.mode == 0) ? (uint32_t)p.Mpad : (uint32_t)((s.cls == 0) ? round_up(rows, 16) : p.Mpad);
+                const uint32_t N =
+                    (p.mode == 0) ? (uint32_t)p.Mpad : (uint32_t)((s.cls == 0) ? round_up(s.rows, 16) : p.Mpad);
                 if (!mbar_wait_bounded(smem_u32(&sm.acc_empty[ab]), ((acc_ph >> ab) & 1u) ^ 1u, abort_flag,
                                        kWaitLimitNs)) {
                     set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem + (uint32_t)(ab * p.Mpad);
-#define MOE_SEG(F, CPV)                                                                                   \
-    mma_segment<F, CPV>(wait0, empty0, st, ph, S, s.ka, s.kb, adesc0, bdesc0, sfadesc0, sfbdesc0, stage16, d_tmem, \
+                const uint32_t d_tmem = bank_t + (uint32_t)(ab * p.Mpad);
+#define MOE_SEG(F, CPV)                                                                                      \
+    mma_segment<F, CPV>(wait0, empty0, rg, s.ka, s.kb, par, adesc0, bdesc0, sfadesc0, sfbdesc0, stage16, d_tmem, \
                         sf_t0, 8 * am, 4 * am, N, abort_flag)
+                // launches with NVFP4 weights always have the copy warps (host invariant)
+                int n;
                 if (p.sf_warps) {
-                    if (C.fmt == MOE_FMT_MXFP8) ok = MOE_SEG(MOE_FMT_MXFP8, false);
-                    else if (C.fmt == MOE_FMT_NVFP4) ok = MOE_SEG(MOE_FMT_NVFP4, false);
-                    else ok = MOE_SEG(MOE_FMT_BF16, false);
+                    if (C.fmt == MOE_FMT_MXFP8) n = MOE_SEG(MOE_FMT_MXFP8, false);
+                    else if (C.fmt == MOE_FMT_NVFP4) n = MOE_SEG(MOE_FMT_NVFP4, false);
+                    else n = MOE_SEG(MOE_FMT_BF16, false);
                 } else {
-                    if (C.fmt == MOE_FMT_MXFP8) ok = MOE_SEG(MOE_FMT_MXFP8, true);
-                    else if (C.fmt == MOE_FMT_NVFP4) ok = MOE_SEG(MOE_FMT_NVFP4, true);
-                    else ok = MOE_SEG(MOE_FMT_BF16, true);
+                    if (C.fmt == MOE_FMT_MXFP8) n = MOE_SEG(MOE_FMT_MXFP8, true);
+                    else if (C.fmt == MOE_FMT_BF16) n = MOE_SEG(MOE_FMT_BF16, true);
+                    else {
+                        set_error(p.status, sm.abort_flag, MOE_ERR_UNSUPPORTED);
+                        break;
+                    }
                 }
 #undef MOE_SEG
-                if (!ok) set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
-                if (!ok) break;
-                tc_commit(smem_u32(&sm.acc_full[ab]));
+                if (n < 0) {
+                    set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
+                    break;
+                }
+                // a segment with no step in this issuer's slots leaves its bank untouched
+                // (the epilogue skips it) and only reports the buffer done
+                if (n > 0) tc_commit(smem_u32(&sm.acc_full[ab]));
+                else mbar_arrive(smem_u32(&sm.acc_full[ab]));
                 acc_ph ^= 1u << ab;
                 if (++ab == nacc) ab = 0;
             }
             // wait until every issued MMA has completed before the TMEM is released
-            tc_commit(smem_u32(sm.drain));
-            mbar_wait_bounded(smem_u32(sm.drain), 0u, sm.never, kWaitLimitNs / 2);
+            tc_commit(smem_u32(&sm.drain[par]));
+            mbar_wait_bounded(smem_u32(&sm.drain[par]), 0u, sm.never, kWaitLimitNs / 2);
         }
-    } else if (warp >= 6) {
+    } else if (warp >= 7) {
         // ================================================================ scale-factor copies
-        // (launches with NVFP4 weights): warp 6 copies the A scales, warp 7 the B scales
+        // (launches with NVFP4 weights): warp 7 + j copies scale atoms 2 (j % 2) and
+        // 2 (j % 2) + 1 of every stage, of the A operand for j < 2 and of B otherwise. Each
+        // warp walks all steps in ring order, so a stage's scale columns are always written
+        // by the same warp.
         if (lane == 0 && p.sf_warps) {
-            const bool is_b = warp == 7;
+            const int j = warp - 7;
+            const bool is_b = j >= 2;
+            const int a0 = 2 * (j & 1);
             Walker wk;
             wk.init(p, ngroups, G, c);
             Seg s;
-            int st = 0;
-            uint32_t ph = 0;
+            Ring rg{0, 0u, S};
             const int am = p.atoms_max;
             const uint32_t full0 = smem_u32(&sm.full[0]), ready0 = smem_u32(&sm.sf_ready[0]);
             const uint32_t ring = smem_u32(sm.ring);
-            const uint64_t sfadesc0 = smem_desc(ring + p.sfa_off, 0, 128, 0);
-            const uint64_t sfbdesc0 = smem_desc(ring + p.sfb_off, 0, 128, 0);
+            const uint64_t desc0 = smem_desc(ring + (is_b ? p.sfb_off : p.sfa_off), 0, 128, 0);
             const uint32_t stage16 = (uint32_t)p.stage_bytes >> 4;
-            const uint32_t sf_t0 = tmem + 2 * kAccCols;
+            const uint32_t sf_t0 = tmem + 2 * bank + (is_b ? 4u * am : 0u);
             bool ok = true;
             while (ok && wk.next(s)) {
-                const int fmt = p.cls[s.cls].fmt;
-                const int A = atoms_per_step(fmt);
+                const int A = atoms_per_step(p.cls[s.cls].fmt);
+                const int a1 = A < a0 + 2 ? A : a0 + 2;
                 for (int kk = s.ka; kk < s.kb; ++kk) {
-                    if (!mbar_wait_bounded(full0 + 8u * st, ph, abort_flag, kWaitLimitNs)) {
+                    const int st = rg.st;
+                    if (!mbar_wait_bounded(full0 + 8u * st, rg.ph, abort_flag, kWaitLimitNs)) {
                         set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
                         ok = false;
                         break;
                     }
-                    if (A) {
+                    if (a1 > a0) {
                         tc_fence_after();
-                        const uint64_t so = (uint64_t)st * stage16;
-                        const uint32_t sfa = sf_t0 + (uint32_t)st * 8 * am, sfb = sfa + 4 * am;
-                        if (is_b) {
-                            for (int a = 0; a < A; ++a) tc_cp_sf(sfb + 4 * a, sfbdesc0 + so + 32 * a);
-                        } else {
-                            for (int a = 0; a < A; ++a) tc_cp_sf(sfa + 4 * a, sfadesc0 + so + 32 * a);
-                        }
+                        const uint64_t sd = desc0 + (uint64_t)st * stage16;
+                        const uint32_t sf = sf_t0 + (uint32_t)st * 8 * am;
+                        for (int a = a0; a < a1; ++a) tc_cp_sf(sf + 4 * a, sd + 32 * a);
                         tc_commit(ready0 + 8u * st);
                     } else {
                         mbar_arrive(ready0 + 8u * st);
                     }
-                    if (++st == S) {
-                        st = 0;
-                        ph ^= 1u;
-                    }
+                    rg.adv1();
                 }
             }
-            tc_commit(smem_u32(&sm.sf_drain[warp - 6]));
-            mbar_wait_bounded(smem_u32(&sm.sf_drain[warp - 6]), 0u, sm.never, kWaitLimitNs / 2);
+            tc_commit(smem_u32(&sm.sf_drain[j]));
+            mbar_wait_bounded(smem_u32(&sm.sf_drain[j]), 0u, sm.never, kWaitLimitNs / 2);
         }
     } else {
         // ================================================================ epilogue
@@ -444,11 +503,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
         Seg s;
         int ab = 0;
         uint32_t acc_ph = 0u;
+        int est = 0;  // ring slot of the segment's first step
         float* stg = sm.stg;
         while (wk.next(s)) {
             const GemmClass& C = p.cls[s.cls];
-            int expert, rows, perm_off, row_off, gidx;
-            seg_group(p, s, expert, rows, perm_off, row_off, gidx);
+            const int expert = s.expert, rows = s.rows, perm_off = s.perm_off, row_off = s.row_off, gidx = s.gidx;
             const int N = (p.mode == 0) ? p.Mpad : ((s.cls == 0) ? round_up(rows, 16) : p.Mpad);
             if (!mbar_wait_bounded(smem_u32(&sm.acc_full[ab]), (acc_ph >> ab) & 1u, abort_flag, kWaitLimitNs)) {
                 set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
@@ -456,12 +515,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             }
             acc_ph ^= 1u << ab;
             tc_fence_after();
+            // bank b holds the steps in slots of parity b; a bank with no step of this
+            // segment is not read (the sum is bank 0 + bank 1, in that order)
+            const int nst = s.kb - s.ka;
+            const uint32_t bm = bank_mask(est, nst, S);
+            est = (est + nst) % S;
             const uint32_t t_row = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(ab * p.Mpad);
+            const bool two = bm == 3u;
+            const uint32_t t_one = t_row + (bm == 2u ? (uint32_t)bank : 0u);
             for (int c0 = 0; c0 < N; c0 += 16) {
-                float v[16];
-                tmem_ld16(t_row + (uint32_t)c0, v);
+                uint32_t v0[16], v1[16];
+                if (two) {
+                    tmem_ld16_nowait(t_row + (uint32_t)c0, v0);
+                    tmem_ld16_nowait(t_row + (uint32_t)bank + (uint32_t)c0, v1);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) stg[(c0 + i) * kBlockRows + r] = v[i];
+                    for (int i = 0; i < 16; ++i)
+                        stg[(c0 + i) * kBlockRows + r] = __uint_as_float(v0[i]) + __uint_as_float(v1[i]);
+                } else {
+                    tmem_ld16_nowait(t_one + (uint32_t)c0, v0);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) stg[(c0 + i) * kBlockRows + r] = __uint_as_float(v0[i]);
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -478,10 +554,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                 }
             }
             // stream-K: pieces of a unit cut between CTAs
-            const long long ue = s.us + s.KS - 1;
-            const int c_first = wk.cta_of(s.us, G), c_last = wk.cta_of(ue, G);
-            const int npieces = c_last - c_first + 1;
-            if (npieces > 1) {
+            if (s.ka != 0 || s.kb != s.KS) {
+                const int c_first = wk.cta_of(s.us, G), c_last = wk.cta_of(s.us + s.KS - 1, G);
+                const int npieces = c_last - c_first + 1;
                 const int my_slot = (c == c_first && wk.start(c, G) < s.us) ? 1 : 0;
                 float* part = p.partials + ((size_t)c * 2 + my_slot) * kPartialFloats;
                 for (int rg = 0; rg < rows; ++rg) __stcg(part + rg * kBlockRows + r, stg[rg * kBlockRows + r]);

@@ -36,6 +36,14 @@ __host__ __device__ inline int record_bytes(int fmt) {
     return kBlockRows * kStepBytes + atoms_per_step(fmt) * kAtomBytes;
 }
 
+// GEMM tensor-memory layout: two accumulator banks (one per MMA issuer), each holding
+// nacc buffers of Mpad columns, then the scale factors of every pipeline stage
+// (8 columns per scale atom). NVFP4 stages carry 4 atoms, so their banks are kept small.
+constexpr int kGemmThreads = 352;  // 11 warps: copies, 2 MMA issuers, 4 epilogue, 4 scale copies
+__host__ __device__ inline int acc_bank_cols(int atoms_max, int Mpad) {
+    return atoms_max == 4 ? (2 * Mpad > 64 ? 2 * Mpad : 64) : 128;
+}
+
 // Group table entry written by the route kernel, one per selected routed expert.
 struct Group {
     int32_t expert, rows, perm_off, row_off;  // row_off: padded rows before this group
