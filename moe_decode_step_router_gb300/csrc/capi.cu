@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdarg>
+#include <cstdlib>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -148,7 +149,8 @@ WsLayout layout(const moe_layer_desc* d) {
     L.y = take(4ull * L.P_max * d->H);
     L.cnt_gu = take(4ull * L.U_gu);
     L.cnt_dn = take(4ull * L.U_dn);
-    L.partials = take(4ull * kMaxGemmCtas * 2 * kPartialFloats);
+    L.partials = take(4ull * kPartialSlots * kPartialFloats);
+    L.sched = take(4ull * 4);  // gate_up and down: next work item, CTAs finished
     L.rpart = take(4ull * ((d->H + 511) / 512) * d->E * kMaxRows);
     L.rcnt = take(4ull * ((d->E + 7) / 8));
     L.total = o;
@@ -298,6 +300,21 @@ struct GemmBuffers {
     const int32_t* perm;
 };
 
+// Units at the end of a GEMM launch's list that CTAs take from a shared counter once they
+// have finished their equal static range. The default is none: on GB300 the counter-fed
+// items stream measurably slower than the static ranges, which wins everywhere except the
+// largest units. The environment variable MOE_GEMM_SCHEDULE (read at each launch; a
+// captured graph keeps the schedule it was captured with) selects =static (the default),
+// =hybrid (2 units per CTA in the pool) or =dynamic (all units from the counter). Every
+// schedule agrees with the definition of the step within the tolerance of the fp32
+// accumulation, and each is deterministic.
+int gemm_pool_units(int grid) {
+    const char* e = getenv("MOE_GEMM_SCHEDULE");
+    if (e && strcmp(e, "dynamic") == 0) return -1;
+    if (e && strcmp(e, "hybrid") == 0) return 2 * grid;
+    return 0;
+}
+
 moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* wr, const moe_qweight* ws_,
                        const GemmBuffers& b, int M, const WsLayout& L, uint8_t* ws, cudaStream_t st) {
     DevInfo* di;
@@ -317,6 +334,8 @@ moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* wr,
     p.y = b.y;
     p.counters = reinterpret_cast<int32_t*>(ws + (mode == 0 ? L.cnt_gu : L.cnt_dn));
     p.partials = reinterpret_cast<float*>(ws + L.partials);
+    p.sched = reinterpret_cast<int32_t*>(ws + L.sched) + 2 * mode;
+    p.pool_units = gemm_pool_units(di->sms < kMaxGemmCtas ? di->sms : kMaxGemmCtas);
     p.status = reinterpret_cast<int32_t*>(ws + L.header);
     const size_t hqr = hq_routed(d, M), hsr = hs_routed(d, M);
     for (int c = 0; c < 2; ++c) {
@@ -365,11 +384,14 @@ moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* wr,
     p.b_off = round_up(p.sfa_off + am * kAtomBytes, 1024);
     p.sfb_off = p.b_off + p.Mpad * kStepBytes;
     p.stage_bytes = round_up(p.sfb_off + am * kAtomBytes, 1024);
-    const int fixed = 1024 + p.Mpad * kBlockRows * 4 + 640 + 4 * kMaxRows;
+    // alignment, epilogue staging, work-item queue, barriers and flags (1 KB covers those
+    // not counted per stage)
+    const int fixed = 1024 + p.Mpad * kBlockRows * 4 + kGemmQueue * 64 + 1024;
     int S = (di->smem_optin - fixed) / (p.stage_bytes + 24);  // + full/empty/ready barriers
     const int tmem_cap = am ? (512 - 2 * acc_bank_cols(am, p.Mpad)) / (8 * am) : 16;
     if (S > tmem_cap) S = tmem_cap;
     if (S > 16) S = 16;
+    S &= ~1;  // even ring: items start on even slots
     if (S < 2) return fail(MOE_ERR_UNSUPPORTED, "not enough shared memory for the GEMM pipeline");
     p.stages = S;
     const size_t smem = (size_t)fixed + (size_t)S * p.stage_bytes + 24 * S;

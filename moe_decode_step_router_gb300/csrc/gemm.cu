@@ -9,12 +9,19 @@
 //
 // Design (swap-AB): the expert weight is the MMA's A operand (M = 128 weight rows), the
 // step's rows are N (padded to a multiple of 16). A unit is one (expert group, 128-row
-// weight block); its K loop runs over 128-byte steps. All units of one launch form a
-// single step space that is cut into equal contiguous ranges, one per CTA (stream-K),
-// so every SM streams the same number of weight bytes. A unit cut between CTAs is summed
-// by the last CTA to finish a piece, in piece order (deterministic).
+// weight block); its K loop runs over 128-byte steps. The launch is persistent (one CTA
+// per SM). The units, in order, are handed out as work items in two parts:
+//  - static: the steps of all but the last units are cut into equal contiguous ranges, one
+//    per CTA (stream-K), so every SM streams the same number of bytes;
+//  - pool (none by default): a CTA that has finished its range takes items of the last
+//    units from an atomic counter (whole units first, the final ones cut into up to four
+//    pieces), so SMs that get more memory bandwidth than others take more of the pool.
+// A unit cut into pieces is summed by the CTA that finishes the last piece, in piece order.
+// Item boundaries depend only on the routing and every item starts on an even ring slot,
+// so the arithmetic of each output is fixed whichever CTA computes it.
 //
-// Roles: warp 0 lane 0 issues the bulk copies (weight record + activation tile + its
+// Roles: warp 0 lane 0 takes the work items, publishes them to the other roles through a
+// shared-memory queue and issues the bulk copies (weight record + activation tile + its
 // scales) into a ring of shared-memory stages. Two MMA issuers (lane 0 of warps 1 and 6)
 // consume the even and the odd ring slots, each accumulating into its own TMEM bank: at
 // 8-64 rows one thread's tcgen05 issue rate, not the tensor pipe, caps the bytes a CTA
@@ -36,13 +43,18 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxAcc = 8;  // up to 8 accumulator buffers per bank
 
-// One segment: the steps [ka, kb) of unit (cls, g, b) that fall in this CTA's range, with
-// the facts of the unit's group.
-struct Seg {
-    int cls, g, b, ka, kb, KS;
-    long long unit, us;  // global unit id, first global step of the unit
+// One work item as published to the CTA's roles: the steps [ka, kb) of one unit with the
+// facts of its group, and where its partial sum goes when the unit is cut into pieces.
+struct WorkItem {
+    int cls;  // 0 routed, 1 shared, -1 end of the CTA's work
+    int b, ka, kb;
+    int rot;  // the steps are taken in the order ka + (rot + j) % (kb - ka), j = 0, 1, ...
     int expert, rows, perm_off, row_off, gidx;
+    int unit;                     // unit id (piece counter index)
+    int np;                       // pieces of the unit (1: the item is the whole unit)
+    int s0, sb, sstride, myslot;  // partial slots: piece 0 in s0, piece pc > 0 in sb + pc * sstride
 };
+static_assert(sizeof(WorkItem) == 64, "queue entries are 64 bytes");
 
 __device__ __forceinline__ int4 ld_group(const Group* gp) {
     int4 v;
@@ -50,22 +62,37 @@ __device__ __forceinline__ int4 ld_group(const Group* gp) {
     return v;
 }
 
-// Walks this CTA's contiguous range of the step space (routed units in group order, then
-// the shared expert's units). The position is advanced incrementally (no divisions after
-// the start) and each group record is loaded one group ahead, so a segment boundary costs
-// a few instructions instead of dependent divisions and a load round trip.
+// Position in the ring of shared-memory stages: slot and the parity of its lap. The ring
+// length is even and every item starts on an even slot (an item of odd length is followed
+// by one empty "bubble" slot), so step j of an item always sits in a slot of parity j % 2.
+struct Ring {
+    int st;
+    uint32_t ph;
+    int S;  // even, >= 2
+    __device__ __forceinline__ void adv1() {
+        if (++st == S) {
+            st = 0;
+            ph ^= 1u;
+        }
+    }
+};
+
+// Static part: this CTA's contiguous range of the steps of units [0, U0) (routed units in
+// group order, then the shared expert's units). The position is advanced incrementally (no
+// divisions after the start) and each group record is loaded one group ahead.
 struct Walker {
     const Group* groups;
     long long T_r, T, t, t1;
     int ngroups, MB0, KS0, MB1, KS1, M, ktop;
     int cls, g, b, k;  // position of step t
     int4 cur, nxt;     // records of groups g and g + 1
-    // Effective grid: never more CTAs than steps, so every working CTA owns at least one
-    // step and the CTAs whose ranges meet a unit are exactly its pieces.
-    __device__ static long long total_steps(const GemmParams& p, int ngroups) {
-        return (long long)ngroups * p.cls[0].MB * p.cls[0].KS + (p.has_shared ? (long long)p.cls[1].MB * p.cls[1].KS : 0);
+    // Steps of units [0, U0).
+    __device__ static long long steps_before(const GemmParams& p, int ngroups, int U0) {
+        const int NRU = ngroups * p.cls[0].MB;
+        return U0 <= NRU ? (long long)U0 * p.cls[0].KS
+                         : (long long)NRU * p.cls[0].KS + (long long)(U0 - NRU) * p.cls[1].KS;
     }
-    __device__ void init(const GemmParams& p, int ngroups_, int G, int c) {
+    __device__ void init(const GemmParams& p, int ngroups_, int G, int c, int U0) {
         groups = p.groups;
         ngroups = ngroups_;
         MB0 = p.cls[0].MB;
@@ -75,7 +102,7 @@ struct Walker {
         M = p.M;
         ktop = p.k;
         T_r = (long long)ngroups * MB0 * KS0;
-        T = T_r + (p.has_shared ? (long long)MB1 * KS1 : 0);
+        T = steps_before(p, ngroups, U0);
         t = t1 = 0;
         if (c >= G || T == 0) return;
         t = (long long)c * T / G;
@@ -96,34 +123,47 @@ struct Walker {
             k = (int)(tt - (long long)b * KS1);
         }
     }
-    __device__ __forceinline__ bool next(Seg& s) {
+    __device__ long long start(long long c, int G) const { return c * T / G; }
+    __device__ int cta_of(long long step, int G) const { return (int)(((step + 1) * G - 1) / T); }
+    // The next segment of the range (with its stream-K piece facts), or false at its end.
+    __device__ __forceinline__ bool next(WorkItem& w, int G, int c) {
         if (t >= t1) return false;
         const int KS = cls ? KS1 : KS0;
-        s.cls = cls;
-        s.g = cls ? -1 : g;
-        s.b = b;
-        s.KS = KS;
-        s.ka = k;
+        w.cls = cls;
+        w.b = b;
+        w.rot = 0;
+        w.ka = k;
         const long long room = t1 - t;
-        s.kb = room < (long long)(KS - k) ? k + (int)room : KS;
-        s.us = t - k;
+        w.kb = room < (long long)(KS - k) ? k + (int)room : KS;
+        const long long us = t - k;  // first step of the unit
         if (cls == 0) {
-            s.unit = (long long)g * MB0 + b;
-            s.expert = cur.x;
-            s.rows = cur.y;
-            s.perm_off = cur.z;
-            s.row_off = cur.w;
-            s.gidx = g;
+            w.unit = g * MB0 + b;
+            w.expert = cur.x;
+            w.rows = cur.y;
+            w.perm_off = cur.z;
+            w.row_off = cur.w;
+            w.gidx = g;
         } else {
-            s.unit = (long long)ngroups * MB0 + b;
-            s.expert = 0;
-            s.rows = M;
-            s.perm_off = M * ktop;
-            s.row_off = 0;
-            s.gidx = 0;
+            w.unit = ngroups * MB0 + b;
+            w.expert = 0;
+            w.rows = M;
+            w.perm_off = M * ktop;
+            w.row_off = 0;
+            w.gidx = 0;
         }
-        t += s.kb - s.ka;
-        k = s.kb;
+        w.np = 1;
+        if (w.ka != 0 || w.kb != KS) {
+            // the unit is cut between CTAs c_first..c_last; each CTA has two slots (for
+            // the unit its range starts in and the one it ends in)
+            const int c_first = cta_of(us, G), c_last = cta_of(us + KS - 1, G);
+            w.np = c_last - c_first + 1;
+            w.s0 = 2 * c_first + (start(c_first, G) < us ? 1 : 0);
+            w.sb = 2 * c_first;
+            w.sstride = 2;
+            w.myslot = 2 * c + ((c == c_first && start(c, G) < us) ? 1 : 0);
+        }
+        t += w.kb - w.ka;
+        k = w.kb;
         if (k == KS) {
             k = 0;
             if (++b == (cls ? MB1 : MB0)) {
@@ -140,20 +180,125 @@ struct Walker {
         }
         return true;
     }
-    __device__ long long start(long long c, int G) const { return c * T / G; }
-    __device__ int cta_of(long long step, int G) const { return (int)(((step + 1) * G - 1) / T); }
+};
+
+// Dynamic schedule: the units in order (routed units in group order, then the shared
+// expert's) are handed out by a counter. The first Uh units go whole, Cu consecutive units
+// per grab (at least 32 steps, so the counter's round trip hides behind the copies); the
+// last Ut = min(U, CTAs) units go one per grab, cut into P = clamp(KS / 8, 1, 4) pieces.
+// Head grab w takes chunk (w % G) * R + w / G (R = ceil(Nh / G); indices past the head
+// are skipped): the G grabs in flight at any time read G regions spread over the weights,
+// each region in order, as the static ranges do, which HBM serves faster than G
+// neighbouring chunks.
+struct DynList {
+    int NRU, U, U0, Uh, Urt, Ust, P0, P1, Cu, Nh, R, Wh, W, G;
+    int MB0, KS0, KS1, M, ktop;
+    // The pool: units [U0_, U).
+    __device__ void init(const GemmParams& p, int ngroups, int G_, int U0_) {
+        G = G_;
+        U0 = U0_;
+        MB0 = p.cls[0].MB;
+        KS0 = p.cls[0].KS;
+        KS1 = p.cls[1].KS;
+        M = p.M;
+        ktop = p.k;
+        NRU = ngroups * MB0;
+        const int Ush = p.has_shared ? p.cls[1].MB : 0;
+        U = NRU + Ush;
+        const int Up = U - U0;
+        const int Ut = Up < G ? Up : G;
+        Uh = Up - Ut;
+        Ust = Ut < Ush ? Ut : Ush;
+        Urt = Ut - Ust;
+        P0 = min(max(KS0 / 8, 1), kMaxPieces);
+        P1 = min(max(KS1 / 8, 1), kMaxPieces);
+        Cu = (32 + KS0 - 1) / KS0;
+        Nh = (Uh + Cu - 1) / Cu;
+        R = (Nh + G - 1) / G;
+        Wh = R * G;
+        W = Wh + Urt * P0 + Ust * P1;
+    }
+    // Grab w < W: units [ub, ue), whole (P = 1, ti = -1) or piece pc of P of tail unit ti;
+    // ub == ue for a skipped head index.
+    __device__ __forceinline__ void grab(int w, int& ub, int& ue, int& pc, int& P, int& ti) const {
+        if (w < Wh) {
+            const int ch = (w % G) * R + w / G;
+            ub = ch * Cu;
+            if (ub > Uh) ub = Uh;
+            ue = ub + Cu < Uh ? ub + Cu : Uh;
+            ub += U0;
+            ue += U0;
+            pc = 0;
+            P = 1;
+            ti = -1;
+            return;
+        }
+        const int i = w - Wh;
+        if (i < Urt * P0) {
+            ti = i / P0;
+            pc = i - ti * P0;
+            P = P0;
+        } else {
+            const int j = i - Urt * P0;
+            const int q = j / P1;
+            ti = Urt + q;
+            pc = j - q * P1;
+            P = P1;
+        }
+        ub = U0 + Uh + ti;
+        ue = ub + 1;
+    }
+    __device__ __forceinline__ int group_of(int u) const { return u < NRU ? u / MB0 : -1; }
+    // Item of unit u (piece pc of P, tail index ti) with the record grp of its group
+    // (ignored for the shared expert).
+    __device__ __forceinline__ void item(int u, int pc, int P, int ti, int4 grp, WorkItem& it) const {
+        const bool routed = u < NRU;
+        const int KS = routed ? KS0 : KS1;
+        it.cls = routed ? 0 : 1;
+        it.unit = u;
+        if (routed) {
+            const int g = u / MB0;
+            it.b = u - g * MB0;
+            it.expert = grp.x;
+            it.rows = grp.y;
+            it.perm_off = grp.z;
+            it.row_off = grp.w;
+            it.gidx = g;
+        } else {
+            it.b = u - NRU;
+            it.expert = 0;
+            it.rows = M;
+            it.perm_off = M * ktop;
+            it.row_off = 0;
+            it.gidx = 0;
+        }
+        it.np = P;
+        it.ka = pc * KS / P;
+        it.kb = (pc + 1) * KS / P;
+        // CTAs that run at the same time work on neighbouring units; starting each unit's
+        // K loop at a different step keeps them off the same activation tile (one L2 slice)
+        it.rot = u % (it.kb - it.ka);
+        if (P > 1) {
+            it.s0 = it.sb = kPoolSlot0 + kMaxPieces * ti;
+            it.sstride = 1;
+            it.myslot = kPoolSlot0 + kMaxPieces * ti + pc;
+        }
+    }
 };
 
 struct GemmSmem {
     uint8_t* ring;
-    float* stg;  // [Mpad][128] fp32 epilogue staging
+    float* stg;          // [Mpad][128] fp32 epilogue staging
+    WorkItem* queue;     // [kGemmQueue]
     uint64_t* full;
     uint64_t* empty;
     uint64_t* acc_full;
     uint64_t* acc_empty;
     uint64_t* drain;     // [2] per MMA issuer
     uint64_t* sf_ready;  // [S] scale factors of the stage are in tensor memory
-    uint64_t* sf_drain;
+    uint64_t* sf_drain;  // [4] per copy warp
+    uint64_t* q_full;    // [kGemmQueue] item published
+    uint64_t* q_empty;   // [kGemmQueue] item read by every consuming role
     uint32_t* tmem_base;
     int* abort_flag;
     int* bcast;
@@ -172,38 +317,22 @@ __device__ __forceinline__ float warp_max_f(float v) {
     return v;
 }
 
-// Position in the ring of shared-memory stages: slot and the parity of its lap.
-struct Ring {
-    int st;
-    uint32_t ph;
-    int S;  // >= 2
-    __device__ __forceinline__ void adv1() {
-        if (++st == S) {
-            st = 0;
-            ph ^= 1u;
-        }
-    }
-};
-
-// Accumulator banks written by a segment of n steps whose first step sits in ring slot
-// st0 (bit b: some step sits in a slot of parity b, consumed by issuer b). Any three
-// consecutive slots include both parities.
-__device__ __forceinline__ uint32_t bank_mask(int st0, int n, int S) {
-    uint32_t m = 0;
-    for (int i = 0; i < n && i < 3; ++i) {
-        m |= 1u << (st0 & 1);
-        if (++st0 == S) st0 = 0;
-    }
-    return m;
+// Reads queue entry i, waiting until it is published; false on a timeout.
+__device__ __forceinline__ bool q_read(const GemmSmem& sm, int i, WorkItem& w, volatile int* abort) {
+    const int qi = i % kGemmQueue;
+    if (!mbar_wait_bounded(smem_u32(&sm.q_full[qi]), (uint32_t)(i / kGemmQueue) & 1u, abort, kWaitLimitNs))
+        return false;
+    w = sm.queue[qi];
+    return true;
 }
 
-// Issues this issuer's MMAs of one segment: the steps of [ka, kb) that sit in ring slots
-// of parity par, accumulated into d_tmem (the first of them overwrites it); the ring
-// position advances over every step. Returns -1 on a timeout, else the number of steps
-// issued. At small N the issue stream of a thread, not the tensor pipe, limits the rate,
-// so every descriptor is precomputed and advanced with integer adds (a shared-memory
-// descriptor holds address >> 4 in its low 14 bits: +16 bytes is +1) and the format
-// branch is taken once per segment.
+// Issues this issuer's MMAs of one item: the steps of [ka, kb) that sit in ring slots of
+// parity par (step j = kk - ka of the item with j % 2 == par), accumulated into d_tmem
+// (the first of them overwrites it); the ring position advances over every step. Returns
+// -1 on a timeout, else the number of steps issued. At small N the issue stream of a
+// thread, not the tensor pipe, limits the rate, so every descriptor is precomputed and
+// advanced with integer adds (a shared-memory descriptor holds address >> 4 in its low 14
+// bits: +16 bytes is +1) and the format branch is taken once per item.
 template <int FMT, bool CP>
 __device__ __forceinline__ int mma_segment(uint32_t ready0, uint32_t empty0, Ring& rg, int ka, int kb, int par,
                                            uint64_t adesc0, uint64_t bdesc0, uint64_t sfadesc0, uint64_t sfbdesc0,
@@ -250,21 +379,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int S = p.stages;
+    // roles that read every queue entry: 2 issuers, 4 epilogue warps, 4 copy warps
+    const uint32_t n_cons = 6u + (p.sf_warps ? 4u : 0u);
 
     // ---- shared-memory carve-up
     GemmSmem sm;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     sm.ring = base;
     sm.stg = reinterpret_cast<float*>(base + (size_t)S * p.stage_bytes);
-    uint8_t* misc = reinterpret_cast<uint8_t*>(sm.stg + p.Mpad * kBlockRows);
-    sm.full = reinterpret_cast<uint64_t*>(misc);
+    sm.queue = reinterpret_cast<WorkItem*>(sm.stg + p.Mpad * kBlockRows);
+    sm.full = reinterpret_cast<uint64_t*>(sm.queue + kGemmQueue);
     sm.empty = sm.full + S;
     sm.acc_full = sm.empty + S;
     sm.acc_empty = sm.acc_full + kMaxAcc;
     sm.drain = sm.acc_empty + kMaxAcc;
     sm.sf_ready = sm.drain + 2;
     sm.sf_drain = sm.sf_ready + S;
-    sm.tmem_base = reinterpret_cast<uint32_t*>(sm.sf_drain + 4);
+    sm.q_full = sm.sf_drain + 4;
+    sm.q_empty = sm.q_full + kGemmQueue;
+    sm.tmem_base = reinterpret_cast<uint32_t*>(sm.q_empty + kGemmQueue);
     sm.abort_flag = reinterpret_cast<int*>(sm.tmem_base + 1);
     sm.bcast = sm.abort_flag + 1;
     sm.never = sm.abort_flag + 2;
@@ -274,22 +407,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
         for (int i = 0; i < S; ++i) {
             mbar_init(smem_u32(&sm.full[i]), 1);
             mbar_init(smem_u32(&sm.empty[i]), 1);
+            mbar_init(smem_u32(&sm.sf_ready[i]), 4);  // one per copy warp
         }
         for (int i = 0; i < kMaxAcc; ++i) {
-            mbar_init(smem_u32(&sm.acc_full[i]), 2);  // one arrival per MMA issuer
-            mbar_init(smem_u32(&sm.acc_empty[i]), 4);
+            mbar_init(smem_u32(&sm.acc_full[i]), 2);  // one per MMA issuer
+            mbar_init(smem_u32(&sm.acc_empty[i]), 4);  // one per epilogue warp
         }
-        mbar_init(smem_u32(&sm.drain[0]), 1);
-        mbar_init(smem_u32(&sm.drain[1]), 1);
-        for (int i = 0; i < S; ++i) mbar_init(smem_u32(&sm.sf_ready[i]), 4);  // one per copy warp
+        for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&sm.drain[i]), 1);
         for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&sm.sf_drain[i]), 1);
+        for (int i = 0; i < kGemmQueue; ++i) {
+            mbar_init(smem_u32(&sm.q_full[i]), 1);
+            mbar_init(smem_u32(&sm.q_empty[i]), n_cons);
+        }
         *sm.abort_flag = 0;
         *sm.never = 0;
         fence_mbar_init();
     }
     // The shared expert's weights do not depend on the routing: while the earlier kernels
     // of the step still run (HBM is otherwise idle then), every CTA prefetches its 1/G
-    // share of them into L2. They are consumed at the end of the step space; the routed
+    // share of them into L2. They are consumed at the end of the item list; the routed
     // weights streamed meanwhile carry an evict-first hint.
     if (threadIdx.x == 32 && p.has_shared) {
         const GemmClass& C1 = p.cls[1];
@@ -312,29 +448,40 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
     tc_fence_after();
     const uint32_t tmem = *sm.tmem_base;
     // two accumulator banks of nacc buffers (Mpad columns each): the MMA issuers run up to
-    // nacc - 1 units ahead of the epilogue
+    // nacc - 1 items ahead of the epilogue
     const int bank = acc_bank_cols(p.atoms_max, p.Mpad);
     const int nacc = min(kMaxAcc, bank / p.Mpad);
     pdl_trigger();
 
     const int ngroups = p.hdr->num_groups;
-    const long long T_all = Walker::total_steps(p, ngroups);
-    const int G = (int)((long long)gridDim.x < T_all ? (long long)gridDim.x : T_all), c = blockIdx.x;
+    const int U_all = ngroups * p.cls[0].MB + (p.has_shared ? p.cls[1].MB : 0);
+    const int U_pool = p.pool_units < 0 || p.pool_units > U_all ? U_all : p.pool_units;
+    const int U0 = U_all - U_pool;  // units [0, U0) in static ranges, [U0, U_all) in the pool
+    const bool dyn = U_pool > 0;
+    const long long T_st = Walker::steps_before(p, ngroups, U0);
+    // static part: never more CTAs than steps, so every working CTA owns at least one step
+    // and the CTAs whose ranges meet a unit are exactly its pieces
+    const int G = (int)((long long)gridDim.x < T_st ? (long long)gridDim.x : T_st), c = blockIdx.x;
     volatile int* abort_flag = sm.abort_flag;
 
     if (warp == 0) {
         // ================================================================ producer
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            Walker wk;
-            wk.init(p, ngroups, G, c);
-            Seg s;
-            int st = 0;
-            uint32_t ph = 0;
+            Ring rg{0, 0u, S};
             uint32_t issued_mask = 0;  // stages with a copy in flight at least once
             bool ok = true;
-            while (ok && wk.next(s)) {
-                const GemmClass& C = p.cls[s.cls];
+            int qn = 0;  // items published
+            // Publishes one item and issues its copies (plus the bubble after an odd count).
+            auto issue = [&](const WorkItem& it) -> bool {
+                const int qi = qn % kGemmQueue;
+                if (!mbar_wait_bounded(smem_u32(&sm.q_empty[qi]), ((uint32_t)(qn / kGemmQueue) & 1u) ^ 1u, abort_flag,
+                                       kWaitLimitNs))
+                    return false;
+                sm.queue[qi] = it;
+                mbar_arrive(smem_u32(&sm.q_full[qi]));
+                ++qn;
+                const GemmClass& C = p.cls[it.cls];
                 const int A = atoms_per_step(C.fmt);
                 const uint32_t REC = record_bytes(C.fmt);
                 int Rpad;
@@ -344,30 +491,97 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                     bsrc = C.b;
                     bssrc = C.bs;
                 } else {
-                    Rpad = (s.cls == 0) ? round_up(s.rows, 16) : p.Mpad;
-                    bsrc = C.b + (size_t)s.row_off * C.KS * kStepBytes;
-                    bssrc = C.bs + (size_t)s.gidx * C.KS * A * kAtomBytes;
+                    Rpad = (it.cls == 0) ? round_up(it.rows, 16) : p.Mpad;
+                    bsrc = C.b + (size_t)it.row_off * C.KS * kStepBytes;
+                    bssrc = C.bs + (size_t)it.gidx * C.KS * A * kAtomBytes;
                 }
-                const uint8_t* wrec = C.w + ((size_t)((size_t)s.expert * C.MB + s.b) * C.KS + s.ka) * REC;
+                const uint8_t* wrec0 = C.w + ((size_t)((size_t)it.expert * C.MB + it.b) * C.KS + it.ka) * REC;
                 const uint32_t bbytes = (uint32_t)Rpad * kStepBytes;
-                for (int kk = s.ka; kk < s.kb; ++kk) {
-                    if (!mbar_wait_bounded(smem_u32(&sm.empty[st]), ph ^ 1u, abort_flag, kWaitLimitNs)) {
-                        set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
-                        ok = false;
-                        break;
-                    }
-                    uint8_t* stage = sm.ring + (size_t)st * p.stage_bytes;
+                const int nst = it.kb - it.ka;
+                int jr = it.rot;  // step of the item at position j
+                for (int j = 0; j < nst + (nst & 1); ++j, rg.adv1()) {
+                    const int st = rg.st;
+                    if (!mbar_wait_bounded(smem_u32(&sm.empty[st]), rg.ph ^ 1u, abort_flag, kWaitLimitNs))
+                        return false;
                     const uint32_t fb = smem_u32(&sm.full[st]);
+                    issued_mask |= 1u << st;
+                    if (j == nst) {  // bubble: the slot completes with no data
+                        mbar_arrive(fb);
+                        continue;
+                    }
+                    const int kk = it.ka + jr;
+                    if (++jr == nst) jr = 0;
+                    uint8_t* stage = sm.ring + (size_t)st * p.stage_bytes;
                     mbar_arrive_expect_tx(fb, REC + bbytes + (uint32_t)A * kAtomBytes);
-                    bulk_g2s_hint(smem_u32(stage + p.a_off), wrec, REC, fb, pol);
+                    bulk_g2s_hint(smem_u32(stage + p.a_off), wrec0 + (size_t)(kk - it.ka) * REC, REC, fb, pol);
                     bulk_g2s(smem_u32(stage + p.b_off), bsrc + (size_t)kk * bbytes, bbytes, fb);
                     if (A) bulk_g2s(smem_u32(stage + p.sfb_off), bssrc + (size_t)kk * A * kAtomBytes, A * kAtomBytes, fb);
-                    issued_mask |= 1u << st;
-                    wrec += REC;
-                    if (++st == S) {
-                        st = 0;
-                        ph ^= 1u;
+                }
+                return true;
+            };
+            WorkItem it;
+            {
+                Walker wk;
+                wk.init(p, ngroups, G, c, U0);
+                while (ok && wk.next(it, G, c)) ok = issue(it);
+            }
+            if (ok && dyn) {
+                DynList dl;
+                dl.init(p, ngroups, gridDim.x, U0);
+                // grab w0 in hand with the records of its first unit's group ga0 and ga0 + 1;
+                // w1 taken; w2 requested while w0's copies go out
+                auto preload = [&](int w, int& ga, int4& ra, int4& rb) {
+                    int ub, ue, pc, P, ti;
+                    dl.grab(w, ub, ue, pc, P, ti);
+                    ga = dl.group_of(ub);
+                    if (ga >= 0) {
+                        ra = ld_group(p.groups + ga);
+                        rb = ld_group(p.groups + (ga + 1 < ngroups ? ga + 1 : ga));
                     }
+                };
+                int ga0 = -1;
+                int4 r0a = make_int4(0, 0, 0, 0), r0b = r0a;
+                int w0 = atomicAdd(p.sched, 1), w1 = dl.W;
+                if (w0 < dl.W) {
+                    preload(w0, ga0, r0a, r0b);
+                    w1 = atomicAdd(p.sched, 1);
+                }
+                while (ok && w0 < dl.W) {
+                    int w2 = dl.W, ga1 = -1;
+                    int4 r1a = make_int4(0, 0, 0, 0), r1b = r1a;
+                    if (w1 < dl.W) {
+                        w2 = atomicAdd(p.sched, 1);  // used one grab later
+                        preload(w1, ga1, r1a, r1b);
+                    }
+                    int ub, ue, pc, P, ti;
+                    dl.grab(w0, ub, ue, pc, P, ti);
+                    for (int u = ub; u < ue; ++u) {
+                        const int g = dl.group_of(u);
+                        int4 rec = r0a;
+                        if (g >= 0 && g != ga0) rec = (g == ga0 + 1) ? r0b : ld_group(p.groups + g);
+                        dl.item(u, pc, P, ti, rec, it);
+                        if (!issue(it)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    w0 = w1;
+                    w1 = w2;
+                    ga0 = ga1;
+                    r0a = r1a;
+                    r0b = r1b;
+                }
+            }
+            if (!ok) set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
+            // the end marker
+            if (ok) {
+                const int qi = qn % kGemmQueue;
+                if (mbar_wait_bounded(smem_u32(&sm.q_empty[qi]), ((uint32_t)(qn / kGemmQueue) & 1u) ^ 1u, abort_flag,
+                                      kWaitLimitNs)) {
+                    sm.queue[qi].cls = -1;
+                    mbar_arrive(smem_u32(&sm.q_full[qi]));
+                } else {
+                    set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
                 }
             }
             // make sure no copy is still writing shared memory when the CTA exits: wait for
@@ -375,7 +589,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             // the others in lap ph ^ 1)
             for (int i = 0; i < S; ++i) {
                 if (!(issued_mask >> i & 1u)) continue;
-                const uint32_t par = (i < st) ? ph : (ph ^ 1u);
+                const uint32_t par = (i < rg.st) ? rg.ph : (rg.ph ^ 1u);
                 mbar_wait_bounded(smem_u32(&sm.full[i]), par, sm.never, kWaitLimitNs / 2);
             }
         }
@@ -384,9 +598,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
         // warp 1 consumes the even ring slots (bank 0), warp 6 the odd ones (bank 1)
         if (lane == 0) {
             const int par = warp == 6 ? 1 : 0;
-            Walker wk;
-            wk.init(p, ngroups, G, c);
-            Seg s;
             Ring rg{0, 0u, S};
             int ab = 0;
             uint32_t acc_ph = 0u;  // bit b: phase of accumulator buffer b
@@ -402,10 +613,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             const uint32_t stage16 = (uint32_t)p.stage_bytes >> 4;
             const uint32_t sf_t0 = tmem + 2 * bank;
             const uint32_t bank_t = tmem + (uint32_t)(par * bank);
-            while (wk.next(s)) {
-                const GemmClass& C = p.cls[s.cls];
+            for (int qn = 0;; ++qn) {
+                WorkItem it;
+                if (!q_read(sm, qn, it, abort_flag)) {
+                    set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
+                    break;
+                }
+                mbar_arrive(smem_u32(&sm.q_empty[qn % kGemmQueue]));
+                if (it.cls < 0) break;
+                const GemmClass& C = p.cls[it.cls];
                 const uint32_t N =
-                    (p.mode == 0) ? (uint32_t)p.Mpad : (uint32_t)((s.cls == 0) ? round_up(s.rows, 16) : p.Mpad);
+                    (p.mode == 0) ? (uint32_t)p.Mpad : (uint32_t)((it.cls == 0) ? round_up(it.rows, 16) : p.Mpad);
                 if (!mbar_wait_bounded(smem_u32(&sm.acc_empty[ab]), ((acc_ph >> ab) & 1u) ^ 1u, abort_flag,
                                        kWaitLimitNs)) {
                     set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
@@ -413,8 +631,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = bank_t + (uint32_t)(ab * p.Mpad);
-#define MOE_SEG(F, CPV)                                                                                      \
-    mma_segment<F, CPV>(wait0, empty0, rg, s.ka, s.kb, par, adesc0, bdesc0, sfadesc0, sfbdesc0, stage16, d_tmem, \
+#define MOE_SEG(F, CPV)                                                                                        \
+    mma_segment<F, CPV>(wait0, empty0, rg, it.ka, it.kb, par, adesc0, bdesc0, sfadesc0, sfbdesc0, stage16, d_tmem, \
                         sf_t0, 8 * am, 4 * am, N, abort_flag)
                 // launches with NVFP4 weights always have the copy warps (host invariant)
                 int n;
@@ -435,8 +653,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                     set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
                     break;
                 }
-                // a segment with no step in this issuer's slots leaves its bank untouched
-                // (the epilogue skips it) and only reports the buffer done
+                // after an item of odd length the next slot is a bubble: its owner hands it
+                // back to the producer
+                if ((it.kb - it.ka) & 1) {
+                    if ((rg.st & 1) == par) {
+                        if (!mbar_wait_bounded(wait0 + 8u * rg.st, rg.ph, abort_flag, kWaitLimitNs)) {
+                            set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
+                            break;
+                        }
+                        mbar_arrive(empty0 + 8u * rg.st);
+                    }
+                    rg.adv1();
+                }
+                // an item with no step in this issuer's slots (a single step) leaves its bank
+                // untouched (the epilogue skips it) and only reports the buffer done
                 if (n > 0) tc_commit(smem_u32(&sm.acc_full[ab]));
                 else mbar_arrive(smem_u32(&sm.acc_full[ab]));
                 acc_ph ^= 1u << ab;
@@ -456,9 +686,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             const int j = warp - 7;
             const bool is_b = j >= 2;
             const int a0 = 2 * (j & 1);
-            Walker wk;
-            wk.init(p, ngroups, G, c);
-            Seg s;
             Ring rg{0, 0u, S};
             const int am = p.atoms_max;
             const uint32_t full0 = smem_u32(&sm.full[0]), ready0 = smem_u32(&sm.sf_ready[0]);
@@ -467,17 +694,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             const uint32_t stage16 = (uint32_t)p.stage_bytes >> 4;
             const uint32_t sf_t0 = tmem + 2 * bank + (is_b ? 4u * am : 0u);
             bool ok = true;
-            while (ok && wk.next(s)) {
-                const int A = atoms_per_step(p.cls[s.cls].fmt);
+            for (int qn = 0; ok; ++qn) {
+                WorkItem it;
+                if (!q_read(sm, qn, it, abort_flag)) {
+                    set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
+                    break;
+                }
+                mbar_arrive(smem_u32(&sm.q_empty[qn % kGemmQueue]));
+                if (it.cls < 0) break;
+                const int A = atoms_per_step(p.cls[it.cls].fmt);
                 const int a1 = A < a0 + 2 ? A : a0 + 2;
-                for (int kk = s.ka; kk < s.kb; ++kk) {
+                const int nst = it.kb - it.ka;
+                for (int s = 0; s < nst + (nst & 1); ++s, rg.adv1()) {
                     const int st = rg.st;
                     if (!mbar_wait_bounded(full0 + 8u * st, rg.ph, abort_flag, kWaitLimitNs)) {
                         set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
                         ok = false;
                         break;
                     }
-                    if (a1 > a0) {
+                    if (s < nst && a1 > a0) {
                         tc_fence_after();
                         const uint64_t sd = desc0 + (uint64_t)st * stage16;
                         const uint32_t sf = sf_t0 + (uint32_t)st * 8 * am;
@@ -486,7 +721,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                     } else {
                         mbar_arrive(ready0 + 8u * st);
                     }
-                    rg.adv1();
                 }
             }
             tc_commit(smem_u32(&sm.sf_drain[j]));
@@ -498,31 +732,38 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
         const int r = 32 * q + lane;      // accumulator row (weight row of the block)
         const int et = threadIdx.x - 64;  // 0..127
         const int ew = et / 32;
-        Walker wk;
-        wk.init(p, ngroups, G, c);
-        Seg s;
         int ab = 0;
         uint32_t acc_ph = 0u;
-        int est = 0;  // ring slot of the segment's first step
         float* stg = sm.stg;
-        while (wk.next(s)) {
-            const GemmClass& C = p.cls[s.cls];
-            const int expert = s.expert, rows = s.rows, perm_off = s.perm_off, row_off = s.row_off, gidx = s.gidx;
-            const int N = (p.mode == 0) ? p.Mpad : ((s.cls == 0) ? round_up(rows, 16) : p.Mpad);
-            if (!mbar_wait_bounded(smem_u32(&sm.acc_full[ab]), (acc_ph >> ab) & 1u, abort_flag, kWaitLimitNs)) {
-                set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
+        for (int qn = 0;; ++qn) {
+            // one thread waits for each event and the barrier's AND tells the others, so
+            // the 128 threads always leave the loop together
+            bool ok = et == 0 ? mbar_wait_bounded(smem_u32(&sm.q_full[qn % kGemmQueue]),
+                                                  (uint32_t)(qn / kGemmQueue) & 1u, abort_flag, kWaitLimitNs)
+                              : true;
+            if (!named_bar_and(1, 128, ok)) {
+                if (et == 0) set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
+                break;
+            }
+            const WorkItem it = sm.queue[qn % kGemmQueue];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sm.q_empty[qn % kGemmQueue]));
+            if (it.cls < 0) break;
+            const GemmClass& C = p.cls[it.cls];
+            const int expert = it.expert, rows = it.rows, perm_off = it.perm_off, row_off = it.row_off, gidx = it.gidx;
+            const int N = (p.mode == 0) ? p.Mpad : ((it.cls == 0) ? round_up(rows, 16) : p.Mpad);
+            ok = et == 0 ? mbar_wait_bounded(smem_u32(&sm.acc_full[ab]), (acc_ph >> ab) & 1u, abort_flag, kWaitLimitNs)
+                         : true;
+            if (!named_bar_and(1, 128, ok)) {
+                if (et == 0) set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
                 break;
             }
             acc_ph ^= 1u << ab;
             tc_fence_after();
-            // bank b holds the steps in slots of parity b; a bank with no step of this
-            // segment is not read (the sum is bank 0 + bank 1, in that order)
-            const int nst = s.kb - s.ka;
-            const uint32_t bm = bank_mask(est, nst, S);
-            est = (est + nst) % S;
+            // bank b holds the item's steps j with j % 2 == b; a single-step item wrote bank
+            // 0 only (the sum is bank 0 + bank 1, in that order)
             const uint32_t t_row = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(ab * p.Mpad);
-            const bool two = bm == 3u;
-            const uint32_t t_one = t_row + (bm == 2u ? (uint32_t)bank : 0u);
+            const bool two = it.kb - it.ka >= 2;
             for (int c0 = 0; c0 < N; c0 += 16) {
                 uint32_t v0[16], v1[16];
                 if (two) {
@@ -533,7 +774,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                     for (int i = 0; i < 16; ++i)
                         stg[(c0 + i) * kBlockRows + r] = __uint_as_float(v0[i]) + __uint_as_float(v1[i]);
                 } else {
-                    tmem_ld16_nowait(t_one + (uint32_t)c0, v0);
+                    tmem_ld16_nowait(t_row + (uint32_t)c0, v0);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 16; ++i) stg[(c0 + i) * kBlockRows + r] = __uint_as_float(v0[i]);
@@ -545,7 +786,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             if (++ab == nacc) ab = 0;
             // compact the selected columns: column of group row rg -> stg[rg][r]; the
             // group's tokens are read once (in parallel) into shared memory
-            if (p.mode == 0 && s.cls == 0) {
+            if (p.mode == 0 && it.cls == 0) {
                 if (et < rows) sm.tok[et] = p.perm[perm_off + et] / p.k;
                 named_bar(1, 128);
                 for (int rg = 0; rg < rows; ++rg) {
@@ -553,17 +794,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                     stg[rg * kBlockRows + r] = stg[m * kBlockRows + r];
                 }
             }
-            // stream-K: pieces of a unit cut between CTAs
-            if (s.ka != 0 || s.kb != s.KS) {
-                const int c_first = wk.cta_of(s.us, G), c_last = wk.cta_of(s.us + s.KS - 1, G);
-                const int npieces = c_last - c_first + 1;
-                const int my_slot = (c == c_first && wk.start(c, G) < s.us) ? 1 : 0;
-                float* part = p.partials + ((size_t)c * 2 + my_slot) * kPartialFloats;
+            // a unit cut into pieces: store this piece's partial sum; the CTA finishing the
+            // last piece adds them all, in piece order
+            if (it.np > 1) {
+                const int npieces = it.np;
+                float* part = p.partials + (size_t)it.myslot * kPartialFloats;
                 for (int rg = 0; rg < rows; ++rg) __stcg(part + rg * kBlockRows + r, stg[rg * kBlockRows + r]);
                 __threadfence();
                 named_bar(1, 128);
                 if (et == 0) {
-                    const int old = atomicAdd(p.counters + s.unit, 1);
+                    const int old = atomicAdd(p.counters + it.unit, 1);
                     *sm.bcast = (old == npieces - 1) ? 1 : 0;
                 }
                 named_bar(1, 128);
@@ -571,9 +811,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                 named_bar(1, 128);
                 if (!last) continue;
                 __threadfence();
-                // sum the pieces in piece order; loads of 8 rows x 4 pieces are issued
-                // before their adds (clamped addresses keep them unconditional)
-                const int sl0 = (wk.start(c_first, G) < s.us) ? 1 : 0;
+                // loads of 8 rows x 4 pieces are issued before their adds (clamped
+                // addresses keep them unconditional)
                 for (int rg0 = 0; rg0 < rows; rg0 += 8) {
                     float sum[8];
 #pragma unroll
@@ -581,24 +820,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                     for (int pc0 = 0; pc0 < npieces; pc0 += 4) {
                         float v[4][8];
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int pc = min(pc0 + q, npieces - 1);
-                            const float* src = p.partials + ((size_t)(c_first + pc) * 2 + (pc == 0 ? sl0 : 0)) *
-                                                                kPartialFloats + r;
+                        for (int qq = 0; qq < 4; ++qq) {
+                            const int pc = min(pc0 + qq, npieces - 1);
+                            const int slot = pc == 0 ? it.s0 : it.sb + pc * it.sstride;
+                            const float* src = p.partials + (size_t)slot * kPartialFloats + r;
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) v[q][i] = __ldcg(src + min(rg0 + i, rows - 1) * kBlockRows);
+                            for (int i = 0; i < 8; ++i) v[qq][i] = __ldcg(src + min(rg0 + i, rows - 1) * kBlockRows);
                         }
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            if (pc0 + q < npieces)
+                        for (int qq = 0; qq < 4; ++qq)
+                            if (pc0 + qq < npieces)
 #pragma unroll
-                                for (int i = 0; i < 8; ++i) sum[i] += v[q][i];
+                                for (int i = 0; i < 8; ++i) sum[i] += v[qq][i];
                     }
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
                         if (rg0 + i < rows) stg[(rg0 + i) * kBlockRows + r] = sum[i];
                 }
-                if (et == 0) p.counters[s.unit] = 0;
+                if (et == 0) p.counters[it.unit] = 0;
             }
             named_bar(1, 128);
             // ---- final epilogue
@@ -606,12 +845,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             if (p.mode == 0) {
                 // SwiGLU on (gate, up) = rows (fi, fi + 64); warps take 32 features each
                 const int fi = 32 * (ew & 1) + lane;
-                const int f = 64 * s.b + fi;  // feature in [0, I)
-                const int Rp = (s.cls == 0) ? round_up(rows, 16) : p.Mpad;
-                uint8_t* hq_g = C.hq + (s.cls == 0 ? (size_t)row_off * row_bytes(C.out_fmt, C.I) : 0);
+                const int f = 64 * it.b + fi;  // feature in [0, I)
+                const int Rp = (it.cls == 0) ? round_up(rows, 16) : p.Mpad;
+                uint8_t* hq_g = C.hq + (it.cls == 0 ? (size_t)row_off * row_bytes(C.out_fmt, C.I) : 0);
                 const int Aout = atoms_per_step(C.out_fmt);
                 const int KSo = steps_of(C.out_fmt, C.I);
-                uint8_t* hs_g = C.hs + (s.cls == 0 ? (size_t)gidx * KSo * Aout * kAtomBytes : 0);
+                uint8_t* hs_g = C.hs + (it.cls == 0 ? (size_t)gidx * KSo * Aout * kAtomBytes : 0);
                 for (int rg = (ew >> 1); rg < rows; rg += 2) {
                     const float g = stg[rg * kBlockRows + fi] * alpha;
                     const float u = stg[rg * kBlockRows + fi + 64] * alpha;
@@ -669,7 +908,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                     }
                 }
             } else {
-                const int n = kBlockRows * s.b + et;
+                const int n = kBlockRows * it.b + et;
                 for (int rg = 0; rg < rows; ++rg) {
                     const int pos = perm_off + rg;
                     p.y[(size_t)pos * p.H + n] = stg[rg * kBlockRows + et] * alpha;
@@ -682,6 +921,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
+    }
+    // pool: the last CTA to finish resets the item counter for the next launch
+    if (dyn && threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1) == (int)gridDim.x - 1) {
+            p.sched[0] = 0;
+            p.sched[1] = 0;
+            __threadfence();
+        }
     }
 }
 

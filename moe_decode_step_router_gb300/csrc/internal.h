@@ -16,7 +16,11 @@ constexpr int kStepBytes = 128;      // K bytes per pipeline step (one 128-byte 
 constexpr int kBlockRows = 128;      // weight rows per MMA block (the MMA's M)
 constexpr int kAtomBytes = 512;      // scale atom: 128 rows x 4 bytes
 constexpr int kMaxGemmCtas = 256;    // partial-sum slots are sized for this many CTAs
-constexpr int kPartialFloats = kMaxRows * kBlockRows;  // one stream-K partial
+constexpr int kPartialFloats = kMaxRows * kBlockRows;  // one partial sum of a unit piece
+constexpr int kMaxPieces = 4;        // pieces of a unit cut in the dynamic pool
+constexpr int kPoolSlot0 = 2 * kMaxGemmCtas;  // static ranges: 2 slots per CTA; then the pool's
+constexpr int kPartialSlots = kPoolSlot0 + kMaxPieces * kMaxGemmCtas;
+constexpr int kGemmQueue = 16;       // work items in flight between a CTA's roles
 
 __host__ __device__ inline int round_up(int a, int b) { return (a + b - 1) / b * b; }
 
@@ -61,7 +65,7 @@ struct WsHeader {
 // Byte offsets of the workspace regions for a layer and a maximum row count.
 struct WsLayout {
     size_t header, groups, logits, scores, topk_idx, topk_w, counts, perm, inv_perm, tiles, num_tiles;
-    size_t xq, xs, xq_sh, xs_sh, hq, hs, y, cnt_gu, cnt_dn, partials, rpart, rcnt, total;
+    size_t xq, xs, xq_sh, xs_sh, hq, hs, y, cnt_gu, cnt_dn, partials, sched, rpart, rcnt, total;
     int max_rows, P_max, G_max, T_max, U_gu, U_dn;
     size_t hq_routed_bytes, hs_routed_bytes;  // shared group's data / scales start here
 };
@@ -119,10 +123,12 @@ struct GemmParams {
     const Group* groups;
     const WsHeader* hdr;
     float* y;                 // down output [P, H]
-    int32_t* counters;
-    float* partials;
+    int32_t* counters;        // per unit: pieces finished (self-resetting)
+    float* partials;          // [kPartialSlots][kPartialFloats]
+    int32_t* sched;           // [2]: next work item, CTAs finished (dynamic schedule, self-resetting)
     int32_t* status;
     int stages, stage_bytes, a_off, sfa_off, b_off, sfb_off, atoms_max, sf_warps;
+    int pool_units;           // units at the end of the list taken from the counter (-1: all)
 };
 
 struct FinalizeParams {

@@ -67,9 +67,14 @@ def _check_rows(layer, inp, rows, out, res, oq, os_, ref):
             assert (np.abs(s.astype(int) - ref["outs"][keep].astype(int)) <= 1).all()
 
 
+@pytest.mark.parametrize("sched", ["static", "dynamic"])
 @pytest.mark.parametrize("name", list(SMALL))
 @pytest.mark.parametrize("M", [1, 8, 23, 64])
-def test_step_matches_oracle(name, M):
+def test_step_matches_oracle(name, M, sched, monkeypatch):
+    # the GEMMs' work schedule (equal static ranges, items taken from a counter, or both)
+    # changes only how units are cut between CTAs, never the result beyond fp32 summation
+    # order
+    monkeypatch.setenv("MOE_GEMM_SCHEDULE", sched)
     cfg = SMALL[name]
     inp, layer = make(cfg, seed=10 + M, M=M)
     out, res, oq, os_ = _run(layer, inp, M)
@@ -80,7 +85,11 @@ def test_step_matches_oracle(name, M):
         assert (npy(oq)[M:] == 0).all() and (npy(os_)[M:] == 0).all()
 
 
-def test_graph_replay_equals_eager_and_is_deterministic():
+@pytest.mark.parametrize("sched", ["static", "dynamic", "hybrid"])
+def test_graph_replay_equals_eager_and_is_deterministic(sched, monkeypatch):
+    # when items come from a counter the CTA that computes one changes from run to run;
+    # the bytes must not
+    monkeypatch.setenv("MOE_GEMM_SCHEDULE", sched)
     cfg = SMALL["nv_mx"]
     M = 19
     inp, layer = make(cfg, seed=5, M=M)
@@ -116,13 +125,19 @@ def test_row_map_invariance():
     assert torch.equal(out1[p], out2) and torch.equal(res1[p], res2)
 
 
-FULL = [("tiny_mxfp8", None), ("mxfp8_h7168_e256_k8_8rows", None), ("nvfp4_h6144_e256_k8_16rows", None),
-        ("mxfp8_skew_48rows", None), ("nvfp4_h4096_e512_k10", 1), ("nvfp4_h4096_e512_k10", 8),
-        ("nvfp4_h4096_e512_k10", 64)]
+# (workload, rows, GEMM schedule); "auto" is the default (static ranges)
+FULL = [("tiny_mxfp8", None, "auto"), ("mxfp8_h7168_e256_k8_8rows", None, "auto"),
+        ("nvfp4_h6144_e256_k8_16rows", None, "auto"), ("mxfp8_skew_48rows", None, "auto"),
+        ("nvfp4_h4096_e512_k10", 1, "auto"), ("nvfp4_h4096_e512_k10", 8, "auto"),
+        ("nvfp4_h4096_e512_k10", 64, "auto"), ("mxfp8_h7168_e256_k8_8rows", None, "hybrid"),
+        ("nvfp4_h6144_e256_k8_16rows", None, "dynamic"), ("nvfp4_h4096_e512_k10", 1, "dynamic"),
+        ("nvfp4_h4096_e512_k10", 32, "hybrid"), ("mxfp8_h7168_e256_k8_8rows", None, "dynamic")]
 
 
-@pytest.mark.parametrize("name,M", FULL, ids=["%s-%s" % (n, m) for n, m in FULL])
-def test_full_size_sampled_rows(name, M):
+@pytest.mark.parametrize("name,M,sched", FULL, ids=["%s-%s-%s" % f for f in FULL])
+def test_full_size_sampled_rows(name, M, sched, monkeypatch):
+    if sched != "auto":
+        monkeypatch.setenv("MOE_GEMM_SCHEDULE", sched)
     cfg = synth.config(name) if M is None else synth.config(name, M=M)
     M = cfg["M"]
     inp, layer = make(cfg, seed=0, M=M)
@@ -138,3 +153,17 @@ def test_full_size_sampled_rows(name, M):
         assert (counts[:cfg["E"]] > 8).any()
         idle = (counts[:cfg["E"]] == 0).mean()
         assert 0.25 < idle < 0.55
+
+
+@pytest.mark.parametrize("sched", ["hybrid", "dynamic"])
+def test_full_size_counter_schedules_are_deterministic(sched, monkeypatch):
+    # these schedules hand units to whichever CTA is free first
+    monkeypatch.setenv("MOE_GEMM_SCHEDULE", sched)
+    cfg = synth.config("mxfp8_h7168_e256_k8_8rows")
+    M = cfg["M"]
+    inp, layer = make(cfg, seed=1, M=M)
+    runs = []
+    for _ in range(3):
+        out, res, _, _ = _run(layer, inp, M)
+        runs.append((u16(out).tobytes(), u16(res).tobytes()))
+    assert runs[0] == runs[1] == runs[2]
