@@ -736,28 +736,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
         uint32_t acc_ph = 0u;
         float* stg = sm.stg;
         for (int qn = 0;; ++qn) {
-            // one thread waits for each event and the barrier's AND tells the others, so
-            // the 128 threads always leave the loop together
-            bool ok = et == 0 ? mbar_wait_bounded(smem_u32(&sm.q_full[qn % kGemmQueue]),
-                                                  (uint32_t)(qn / kGemmQueue) & 1u, abort_flag, kWaitLimitNs)
-                              : true;
+            // one thread waits for the next item and for its accumulator; the barrier's AND
+            // tells the others, so the 128 threads always leave the loop together. The
+            // barrier also keeps the staging buffer from being refilled while any thread
+            // still reads the previous item from it.
+            const int qi = qn % kGemmQueue;
+            bool ok = true;
+            if (et == 0) {
+                ok = mbar_wait_bounded(smem_u32(&sm.q_full[qi]), (uint32_t)(qn / kGemmQueue) & 1u, abort_flag,
+                                       kWaitLimitNs);
+                if (ok && sm.queue[qi].cls >= 0)
+                    ok = mbar_wait_bounded(smem_u32(&sm.acc_full[ab]), (acc_ph >> ab) & 1u, abort_flag, kWaitLimitNs);
+            }
             if (!named_bar_and(1, 128, ok)) {
                 if (et == 0) set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
                 break;
             }
-            const WorkItem it = sm.queue[qn % kGemmQueue];
+            const WorkItem it = sm.queue[qi];
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sm.q_empty[qn % kGemmQueue]));
+            if (lane == 0) mbar_arrive(smem_u32(&sm.q_empty[qi]));
             if (it.cls < 0) break;
             const GemmClass& C = p.cls[it.cls];
             const int expert = it.expert, rows = it.rows, perm_off = it.perm_off, row_off = it.row_off, gidx = it.gidx;
             const int N = (p.mode == 0) ? p.Mpad : ((it.cls == 0) ? round_up(rows, 16) : p.Mpad);
-            ok = et == 0 ? mbar_wait_bounded(smem_u32(&sm.acc_full[ab]), (acc_ph >> ab) & 1u, abort_flag, kWaitLimitNs)
-                         : true;
-            if (!named_bar_and(1, 128, ok)) {
-                if (et == 0) set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
-                break;
-            }
             acc_ph ^= 1u << ab;
             tc_fence_after();
             // bank b holds the item's steps j with j % 2 == b; a single-step item wrote bank
@@ -914,7 +915,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                     p.y[(size_t)pos * p.H + n] = stg[rg * kBlockRows + et] * alpha;
                 }
             }
-            named_bar(1, 128);
         }
     }
     __syncthreads();
