@@ -44,7 +44,8 @@ class Layer(ctypes.Structure):
                 ("renormalize", ctypes.c_int32), ("emit_next", ctypes.c_int32),
                 ("rsf", ctypes.c_double), ("eps", ctypes.c_double),
                 ("gs_a1", ctypes.c_float), ("gs_a2", ctypes.c_float),
-                ("gs_a1_sh", ctypes.c_float), ("gs_a2_sh", ctypes.c_float)]
+                ("gs_a1_sh", ctypes.c_float), ("gs_a2_sh", ctypes.c_float),
+                ("swiglu_limit", ctypes.c_double)]
 
 
 class Proj(ctypes.Structure):
@@ -82,7 +83,7 @@ def lib():
             L.or_quant_x.argtypes = [ctypes.c_int, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_float, P, P]
             L.or_expert_row.restype = None
             L.or_expert_row.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(Proj),
-                                        ctypes.POINTER(Proj), P, ctypes.c_float, P, P, P, P]
+                                        ctypes.POINTER(Proj), P, ctypes.c_float, ctypes.c_double, P, P, P, P]
             L.or_finalize_row.restype = None
             L.or_finalize_row.argtypes = [ctypes.POINTER(Layer), P, P, P, P, P, P, P]
             L.or_step_rows.restype = ctypes.c_int
@@ -155,7 +156,8 @@ def make_layer(cfg, gs_a=(1.0, 1.0, 1.0, 1.0)):
     return Layer(cfg["H"], cfg["E"], cfg["k"], cfg["I"], cfg["I_sh"], cfg["w_fmt"], cfg["sh_fmt"],
                  int(cfg.get("has_shared", True)), int(cfg["has_bias"]), int(cfg.get("renormalize", True)),
                  int(cfg.get("emit_next", False)), float(cfg["rsf"]), float(cfg["eps"]),
-                 float(gs_a[0]), float(gs_a[1]), float(gs_a[2]), float(gs_a[3]))
+                 float(gs_a[0]), float(gs_a[1]), float(gs_a[2]), float(gs_a[3]),
+                 float(cfg.get("swiglu_limit", 0.0)))
 
 
 def router(layer, x_bf16, wg_bf16, bias=None, logits_in=None):
@@ -205,7 +207,7 @@ def _proj(vals, scales, gs):
     return Proj(vals.ctypes.data, None if scales is None or scales.size == 0 else scales.ctypes.data, float(gs))
 
 
-def expert_row(fmt, H, I, w13, w2, xdq, gs_a2=1.0):
+def expert_row(fmt, H, I, w13, w2, xdq, gs_a2=1.0, limit=0.0):
     """One expert on one dequantised input row.
 
     w13 = (vals [2I, rb], scales [2I, rs] | None, gs), w2 = (vals [H, rb], scales, gs).
@@ -219,8 +221,8 @@ def expert_row(fmt, H, I, w13, w2, xdq, gs_a2=1.0):
     hs = np.zeros(max(row_scales(fmt, I), 1), np.uint8)
     h = np.zeros(I, np.float64)
     y = np.zeros(H, np.float64)
-    lib().or_expert_row(fmt, H, I, ctypes.byref(p13), ctypes.byref(p2), _p(xdq), gs_a2, _p(hq), _p(hs), _p(h),
-                        _p(y))
+    lib().or_expert_row(fmt, H, I, ctypes.byref(p13), ctypes.byref(p2), _p(xdq), gs_a2, limit, _p(hq), _p(hs),
+                        _p(h), _p(y))
     return hq, hs[:row_scales(fmt, I)], h, y
 
 

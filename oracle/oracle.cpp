@@ -26,7 +26,9 @@
 //  A2 the per-expert bias enters the selection key only; weights use the raw score.
 //  A3 MXFP8 scale exponent = smallest e in [-127,127] with amax <= 448*2^e.
 //  A4 NVFP4 activation global scales are static per layer (inputs here).
-//  A5 SwiGLU is unclamped.   A6 one bf16 rounding of the residual, RMSNorm reads it.
+//  A5 SwiGLU is unclamped unless the layer gives a limit L > 0: then g -> min(g, L) and
+//     u -> clamp(u, -L, L) before silu(g) u.
+//  A6 one bf16 rounding of the residual, RMSNorm reads it.
 //  A8 W13 rows: gate rows 0..I-1, then up rows I..2I-1.  A9 shared output unscaled.
 
 #include <cmath>
@@ -221,6 +223,7 @@ typedef struct {
     double rsf, eps;
     float gs_a1, gs_a2;         // routed NVFP4 static activation scales (FC1 in, FC2 in)
     float gs_a1_sh, gs_a2_sh;   // shared-expert NVFP4 static activation scales
+    double swiglu_limit;        // > 0: clamped SwiGLU (routed and shared experts); <= 0: plain
 } or_layer;
 
 // One projection of one expert in canonical layout.
@@ -343,12 +346,14 @@ void or_quant_x(int fmt, const uint16_t* x, int64_t rows, int64_t H, float gs, u
 // [README] moe row: a pair of block-scaled GEMMs (gate_up then down); shared_ll row:
 // SwiGLU between them; Qwen3.5 mkm row: FC1, SwiGLU, NVFP4 requantisation, FC2.
 // g_i = sum_h deq(W13[i,h]) deq(xq[h]); u_i the same over row I+i (double sums);
-// h_i = silu(g_i) u_i with silu(z) = z/(1+exp(-z)) (A5: unclamped);
+// h_i = silu(g_i) u_i with silu(z) = z/(1+exp(-z)); with a limit L > 0 ("SGLang-NVIDIA-
+// Mega" README, shared_ll row: clamped SwiGLU), g_i -> min(g_i, L) and u_i -> clamp(u_i,
+// -L, L) first;
 // hq = quant(fp32(h)) along I in `fmt` (BF16: one bf16 rounding);
 // y_n = sum_i deq(W2[n,i]) deq(hq[i]).
 // Outputs: hq (row_bytes(fmt, I)), hs (row_scales(fmt, I)), h_out (double, I) and y (double, H).
 void or_expert_row(int fmt, int H, int I, const or_proj* w13, const or_proj* w2, const double* xdq,
-                   float gs_a2, uint8_t* hq, uint8_t* hs, double* h_out, double* y) {
+                   float gs_a2, double limit, uint8_t* hq, uint8_t* hs, double* h_out, double* y) {
     std::vector<double> wrow(std::max(H, I)), hv(I), hdq(I);
     std::vector<float> hf(I);
     const int64_t rb13 = row_bytes(fmt, H), rs13 = row_scales(fmt, H);
@@ -360,6 +365,10 @@ void or_expert_row(int fmt, int H, int I, const or_proj* w13, const or_proj* w2,
         dequant_row(fmt, w13->vals + (int64_t)(I + i) * rb13,
                     w13->scales ? w13->scales + (int64_t)(I + i) * rs13 : nullptr, w13->gs, H, wrow.data());
         for (int h = 0; h < H; ++h) u += wrow[h] * xdq[h];
+        if (limit > 0.0) {
+            g = std::min(g, limit);
+            u = std::max(-limit, std::min(u, limit));
+        }
         double silu = g / (1.0 + std::exp(-g));
         hv[i] = silu * u;
         hf[i] = (float)hv[i];
@@ -430,8 +439,8 @@ int or_step_rows(const or_layer* L, int M, const int32_t* rows, int nrows, const
         for (int j = 0; j < k; ++j) {
             int e = topk_idx[(int64_t)i * k + j];
             if (!w13[e].vals || !w2[e].vals) return -(e + 1);
-            or_expert_row(L->w_fmt, H, L->I, &w13[e], &w2[e], xdq.data(), L->gs_a2, hq.data(), hs.data(),
-                          hbuf.data(), y.data());
+            or_expert_row(L->w_fmt, H, L->I, &w13[e], &w2[e], xdq.data(), L->gs_a2, L->swiglu_limit, hq.data(),
+                          hs.data(), hbuf.data(), y.data());
             double w = topk_w[(int64_t)i * k + j];
             for (int n = 0; n < H; ++n) {
                 if (y_pairs) y_pairs[((int64_t)i * k + j) * H + n] = y[n];
@@ -441,8 +450,8 @@ int or_step_rows(const or_layer* L, int M, const int32_t* rows, int nrows, const
         if (L->has_shared) {
             or_quant_x(L->sh_fmt, xr, 1, H, L->gs_a1_sh, xq.data(), xs.data());
             dequant_row(L->sh_fmt, xq.data(), xs.data(), L->gs_a1_sh, H, xdq_sh.data());
-            or_expert_row(L->sh_fmt, H, L->I_sh, sh13, sh2, xdq_sh.data(), L->gs_a2_sh, hq.data(), hs.data(),
-                          hbuf.data(), y.data());
+            or_expert_row(L->sh_fmt, H, L->I_sh, sh13, sh2, xdq_sh.data(), L->gs_a2_sh, L->swiglu_limit, hq.data(),
+                          hs.data(), hbuf.data(), y.data());
             for (int n = 0; n < H; ++n) {
                 if (y_shared) y_shared[(int64_t)i * H + n] = y[n];
                 moe[n] += y[n];

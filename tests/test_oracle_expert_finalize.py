@@ -54,6 +54,43 @@ def test_expert_closed_form_mxfp8():
     assert np.allclose(y, I * hd[0])              # W2 == 1 everywhere: y_n = sum_i hq_i
 
 
+@pytest.mark.parametrize("gsign,usign", [(1, 1), (-1, 1), (1, -1), (-1, -1)])
+def test_expert_clamped_swiglu_closed_form(gsign, usign):
+    # Clamped SwiGLU ("SGLang-NVIDIA-Mega" README, shared_ll row): g -> min(g, L),
+    # u -> clamp(u, -L, L), then silu(g) u. |g| = 0.5, |u| = 1.0 and L = 0.25: a positive
+    # gate is cut to L, a negative one is left alone (upper bound only), u is cut either way.
+    H, I, L = 64, 32, 0.25
+    gcode, ucode = (0x38 if gsign > 0 else 0xB8), (0x38 if usign > 0 else 0xB8)   # +-1.0 in E4M3
+    v13 = np.concatenate([np.full((I, H), gcode, np.uint8), np.full((I, H), ucode, np.uint8)])
+    s13 = np.concatenate([np.full((I, H // 32), 120, np.uint8), np.full((I, H // 32), 121, np.uint8)])
+    v2, s2 = _mx_const(H, I, 0x38, 127)
+    _, _, h, _ = oracle.expert_row(FMT_MXFP8, H, I, (v13, s13, 1.0), (v2, s2, 1.0), np.ones(H), limit=L)
+    g = 0.5 * gsign
+    g = L if g > L else g
+    u = L * usign
+    assert np.all(h == g / (1 + math.exp(-g)) * u)
+    # a limit above every |g| and |u| changes nothing; a limit <= 0 means unclamped
+    _, _, h_off, _ = oracle.expert_row(FMT_MXFP8, H, I, (v13, s13, 1.0), (v2, s2, 1.0), np.ones(H), limit=0.0)
+    _, _, h_big, _ = oracle.expert_row(FMT_MXFP8, H, I, (v13, s13, 1.0), (v2, s2, 1.0), np.ones(H), limit=4.0)
+    g0, u0 = 0.5 * gsign, 1.0 * usign
+    assert np.all(h_off == g0 / (1 + math.exp(-g0)) * u0) and np.all(h_big == h_off)
+
+
+def test_expert_clamped_swiglu_brute_force():
+    H, I = 128, 64
+    g = synth._gen(7, "cpu")
+    v13, s13, gs13 = [t.numpy() if t is not None else None for t in synth.weight(FMT_MXFP8, 1, 2 * I, H, g, "cpu")]
+    v2, s2, gs2 = [t.numpy() if t is not None else None for t in synth.weight(FMT_MXFP8, 1, H, I, g, "cpu")]
+    xdq = np.random.default_rng(17).standard_normal(H) * 8.0
+    W13 = _deq_indep(FMT_MXFP8, v13[0], s13[0], 1.0, H)
+    gg, uu = W13[:I] @ xdq, W13[I:] @ xdq
+    L = float(np.median(np.abs(np.concatenate([gg, uu]))))   # about half the values are cut
+    _, _, h, _ = oracle.expert_row(FMT_MXFP8, H, I, (v13[0], s13[0], 1.0), (v2[0], s2[0], 1.0), xdq, limit=L)
+    gc, uc = np.minimum(gg, L), np.clip(uu, -L, L)
+    assert (gg > L).any() and (np.abs(uu) > L).any() and (gg < -L).any()
+    assert np.allclose(h, gc / (1 + np.exp(-gc)) * uc, rtol=1e-12, atol=1e-12)
+
+
 def test_expert_fc2_one_hot_rows():
     rng = np.random.default_rng(12)
     H, I = 64, 64
