@@ -37,6 +37,7 @@ def _args():
     ap.add_argument("--rows", type=int, default=None)
     ap.add_argument("--experts", type=int, default=None, help="override E (smaller profiling cases)")
     ap.add_argument("--inter", type=int, default=None, help="override I and shared I (smaller profiling cases)")
+    ap.add_argument("--swiglu-limit", type=float, default=None, help="clamped SwiGLU limit (default: plain SwiGLU)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
     return ap.parse_args()
@@ -104,6 +105,8 @@ def _cfg(a):
         over["E"] = a.experts
     if a.inter is not None:
         over["I"] = over["I_sh"] = a.inter
+    if a.swiglu_limit is not None:
+        over["swiglu_limit"] = a.swiglu_limit
     return synth.config(a.config, **over)
 
 
@@ -409,7 +412,8 @@ def main():
                 "vs_baseline": None, "dtype": "mxfp8" if cfg["w_fmt"] == 1 else "nvfp4",
                 "data": "synthetic (seeded): inputs of the workload's shapes, random weights",
                 "config": {"workload": cfg["name"], "rows": M, "H": H, "E": cfg["E"], "k": cfg["k"], "I": I,
-                           "shared_I": Ish, "unique_experts": n_active, "unique_bytes": ubytes,
+                           "shared_I": Ish, "swiglu_limit": cfg.get("swiglu_limit", 0.0),
+                           "unique_experts": n_active, "unique_bytes": ubytes,
                            "us_per_step": ms_step * 1e3, "rows_per_s": M / (ms_step * 1e-3),
                            "frac_of_measured_peak": gbs / peak, "frac_of_8000": gbs / 8000.0,
                            "l2": "512 MiB buffer written, then another 512 MiB read, between timed steps (untimed)",

@@ -89,13 +89,17 @@ typedef enum { MOE_W13 = 0, MOE_W2 = 1, MOE_SH13 = 2, MOE_SH2 = 3 } moe_proj;
  * I, I_shared % 256 == 0 and 256 <= I <= 4096. w_fmt is MXFP8 or NVFP4; shared_fmt is
  * BF16, MXFP8 or NVFP4. gs_a1 / gs_a2 are the static NVFP4 global scales of the routed
  * experts' FC1 and FC2 inputs (gs_a1_shared / gs_a2_shared for the shared expert);
- * they are ignored for other formats. */
+ * they are ignored for other formats. swiglu_limit > 0 selects the clamped SwiGLU of the
+ * routed and the shared experts ("SGLang-NVIDIA-Mega" README, shared_ll row): the gate
+ * is cut to min(g, L) and the up projection to clamp(u, -L, L) before silu(g) * u, with
+ * L = swiglu_limit; 0 (or any value <= 0) is the plain SwiGLU; NaN is rejected. */
 typedef struct {
     int32_t H, E, k, I, I_shared;
     int32_t w_fmt, shared_fmt;
     int32_t has_shared, has_bias, renormalize, emit_next_mxfp8;
     float routed_scaling_factor, rms_eps;
     float gs_a1, gs_a2, gs_a1_shared, gs_a2_shared;
+    float swiglu_limit;
 } moe_layer_desc;
 
 /* A packed projection: the moe_pack_weights output and, for NVFP4, the fp32 global

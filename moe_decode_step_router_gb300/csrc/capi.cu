@@ -76,6 +76,7 @@ moe_status check_desc(const moe_layer_desc* d) {
     }
     REQUIRE(d->routed_scaling_factor == d->routed_scaling_factor, "routed_scaling_factor is NaN");
     REQUIRE(d->rms_eps >= 0.0f, "rms_eps must be >= 0");
+    REQUIRE(d->swiglu_limit == d->swiglu_limit, "swiglu_limit must not be NaN");
     if (d->w_fmt == MOE_FMT_NVFP4) REQUIRE(d->gs_a1 > 0.0f && d->gs_a2 > 0.0f, "NVFP4 needs gs_a1, gs_a2 > 0");
     if (d->has_shared && d->shared_fmt == MOE_FMT_NVFP4)
         REQUIRE(d->gs_a1_shared > 0.0f && d->gs_a2_shared > 0.0f, "NVFP4 shared needs gs_a1_shared, gs_a2_shared > 0");
@@ -335,6 +336,7 @@ moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* wr,
     p.counters = reinterpret_cast<int32_t*>(ws + (mode == 0 ? L.cnt_gu : L.cnt_dn));
     p.partials = reinterpret_cast<float*>(ws + L.partials);
     p.sched = reinterpret_cast<int32_t*>(ws + L.sched) + 2 * mode;
+    p.swiglu_limit = d->swiglu_limit > 0.0f ? d->swiglu_limit : 0.0f;
     p.pool_units = gemm_pool_units(di->sms < kMaxGemmCtas ? di->sms : kMaxGemmCtas);
     p.status = reinterpret_cast<int32_t*>(ws + L.header);
     const size_t hqr = hq_routed(d, M), hsr = hs_routed(d, M);

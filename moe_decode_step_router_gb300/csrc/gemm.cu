@@ -852,9 +852,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                 const int Aout = atoms_per_step(C.out_fmt);
                 const int KSo = steps_of(C.out_fmt, C.I);
                 uint8_t* hs_g = C.hs + (it.cls == 0 ? (size_t)gidx * KSo * Aout * kAtomBytes : 0);
+                const float lim = p.swiglu_limit;
                 for (int rg = (ew >> 1); rg < rows; rg += 2) {
-                    const float g = stg[rg * kBlockRows + fi] * alpha;
-                    const float u = stg[rg * kBlockRows + fi + 64] * alpha;
+                    float g = stg[rg * kBlockRows + fi] * alpha;
+                    float u = stg[rg * kBlockRows + fi + 64] * alpha;
+                    if (lim > 0.0f) {  // clamped SwiGLU: gate cut from above, up to [-lim, lim]
+                        g = fminf(g, lim);
+                        u = fminf(fmaxf(u, -lim), lim);
+                    }
                     const float h = g / (1.0f + expf(-g)) * u;
                     if (C.out_fmt == MOE_FMT_MXFP8) {
                         const float amax = warp_max_f(fabsf(h));

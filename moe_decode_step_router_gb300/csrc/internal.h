@@ -129,6 +129,7 @@ struct GemmParams {
     int32_t* status;
     int stages, stage_bytes, a_off, sfa_off, b_off, sfb_off, atoms_max, sf_warps;
     int pool_units;           // units at the end of the list taken from the counter (-1: all)
+    float swiglu_limit;       // > 0: clamped SwiGLU in the gate_up epilogue
 };
 
 struct FinalizeParams {

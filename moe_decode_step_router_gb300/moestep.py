@@ -38,7 +38,8 @@ class LayerDesc(ctypes.Structure):
                 ("has_shared", ctypes.c_int32), ("has_bias", ctypes.c_int32), ("renormalize", ctypes.c_int32),
                 ("emit_next_mxfp8", ctypes.c_int32), ("routed_scaling_factor", ctypes.c_float),
                 ("rms_eps", ctypes.c_float), ("gs_a1", ctypes.c_float), ("gs_a2", ctypes.c_float),
-                ("gs_a1_shared", ctypes.c_float), ("gs_a2_shared", ctypes.c_float)]
+                ("gs_a1_shared", ctypes.c_float), ("gs_a2_shared", ctypes.c_float),
+                ("swiglu_limit", ctypes.c_float)]
 
 
 class QWeight(ctypes.Structure):
@@ -126,7 +127,7 @@ def layer_desc(cfg, gs_a=(1.0, 1.0, 1.0, 1.0)) -> LayerDesc:
     return LayerDesc(cfg["H"], cfg["E"], cfg["k"], cfg["I"], cfg["I_sh"], cfg["w_fmt"], cfg["sh_fmt"],
                      int(cfg.get("has_shared", True)), int(cfg["has_bias"]), int(cfg.get("renormalize", True)),
                      int(cfg.get("emit_next", False)), float(cfg["rsf"]), float(cfg["eps"]), float(gs_a[0]),
-                     float(gs_a[1]), float(gs_a[2]), float(gs_a[3]))
+                     float(gs_a[1]), float(gs_a[2]), float(gs_a[3]), float(cfg.get("swiglu_limit", 0.0)))
 
 
 def qweight(packed, gs=None) -> QWeight:

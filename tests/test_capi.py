@@ -53,7 +53,7 @@ def test_sizes(lib):
 @pytest.mark.parametrize("field,value,status", [
     ("H", 1000, ms.MOE_ERR_INVALID_ARG), ("E", 0, ms.MOE_ERR_INVALID_ARG), ("k", 17, ms.MOE_ERR_INVALID_ARG),
     ("I", 300, ms.MOE_ERR_INVALID_ARG), ("w_fmt", ms.MOE_FMT_BF16, ms.MOE_ERR_UNSUPPORTED),
-    ("shared_fmt", 7, ms.MOE_ERR_UNSUPPORTED)])
+    ("shared_fmt", 7, ms.MOE_ERR_UNSUPPORTED), ("swiglu_limit", float("nan"), ms.MOE_ERR_INVALID_ARG)])
 def test_bad_descriptor_rejected(lib, field, value, status):
     d = _desc()
     setattr(d, field, value)

@@ -167,3 +167,29 @@ def test_full_size_counter_schedules_are_deterministic(sched, monkeypatch):
         out, res, _, _ = _run(layer, inp, M)
         runs.append((u16(out).tobytes(), u16(res).tobytes()))
     assert runs[0] == runs[1] == runs[2]
+
+
+# Clamped SwiGLU ("SGLang-NVIDIA-Mega" README, shared_ll row): the limit is chosen below
+# the typical |gate| so that most gate and up values of every format are cut.
+@pytest.mark.parametrize("name", ["mx_mx", "nv_bf16", "nv_mx"])
+@pytest.mark.parametrize("M", [8, 37])
+def test_clamped_swiglu_step_matches_oracle(name, M):
+    cfg = dict(SMALL[name], swiglu_limit=0.25)
+    inp, layer = make(cfg, seed=40 + M, M=M)
+    out, res, oq, os_ = _run(layer, inp, M)
+    rows = list(range(M))
+    ref = _oracle_rows(cfg, inp, rows)
+    _check_rows(layer, inp, rows, out, res, oq, os_, ref)
+    # the limit does change the step
+    plain = _oracle_rows(dict(cfg, swiglu_limit=0.0), inp, rows)
+    assert np.abs(plain["out"].astype(np.int64) - ref["out"].astype(np.int64)).max() > 0
+
+
+def test_clamped_swiglu_full_size_sampled_rows():
+    cfg = synth.config("mxfp8_h7168_e256_k8_8rows", swiglu_limit=1.0)
+    M = cfg["M"]
+    inp, layer = make(cfg, seed=2, M=M)
+    out, res, oq, os_ = _run(layer, inp, M)
+    rows = [0, M - 1]
+    ref = _oracle_rows(cfg, inp, rows)
+    _check_rows(layer, inp, rows, out, res, oq, os_, ref)
