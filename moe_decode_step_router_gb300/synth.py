@@ -13,6 +13,8 @@ Recipes (all seeded):
   NVFP4 weight E2M1 codes drawn from a fixed magnitude table (random sign); E4M3 block
                scale bytes uniform in [0x30, 0x40] (0.5 .. 2.0); per-expert fp32 global
                scale 2^-8 * (1 + U(0, 1)/4)
+  MXFP4 weight E2M1 codes drawn from the same magnitude table (random sign); E8M0 scale
+               bytes uniform in {119, 120} (2^-8, 2^-7): values up to ~0.05, ~N(0, 0.01)
   BF16 weight  bf16 N(0, 0.02)
   NVFP4 static activation scales: FC1 input 2^-8, FC2 input 2^-6 (plain constants).
   Skewed routing: the selection bias adds beta * r_e^-1.2 over a seeded permutation r of
@@ -23,8 +25,8 @@ from __future__ import annotations
 
 import torch
 
-FMT_BF16, FMT_MXFP8, FMT_NVFP4 = 0, 1, 2
-FMT_NAMES = {FMT_BF16: "bf16", FMT_MXFP8: "mxfp8", FMT_NVFP4: "nvfp4"}
+FMT_BF16, FMT_MXFP8, FMT_NVFP4, FMT_MXFP4 = 0, 1, 2, 3
+FMT_NAMES = {FMT_BF16: "bf16", FMT_MXFP8: "mxfp8", FMT_NVFP4: "nvfp4", FMT_MXFP4: "mxfp4"}
 
 # Magnitude index 0..7 of E2M1 (0, .5, 1, 1.5, 2, 3, 4, 6): draw probabilities.
 NVFP4_MAG_PROBS = (0.10, 0.18, 0.17, 0.15, 0.13, 0.12, 0.09, 0.06)
@@ -48,6 +50,10 @@ CONFIGS = {
     # 48 rows, MXFP8, Zipf-skewed selection, emits the next layer's MXFP8 input.
     "mxfp8_skew_48rows": dict(_BASE, M=48, H=7168, E=256, k=8, I=2048, I_sh=2048, w_fmt=FMT_MXFP8,
                               sh_fmt=FMT_MXFP8, has_bias=True, rsf=2.5, skew=True, emit_next=True),
+    # Packed MXFP4 routed experts (the pages' packed-MXFP4 decode steps of 1-8, 16, 32 and
+    # 64 rows give no shapes: the headline's are used) + MXFP8 shared.
+    "mxfp4_h7168_e256_k8": dict(_BASE, M=8, H=7168, E=256, k=8, I=2048, I_sh=2048, w_fmt=FMT_MXFP4,
+                                sh_fmt=FMT_MXFP8),
     # Row sweep on H 4096, 512 experts, top-10, NVFP4 routed + MXFP8 shared.
     "nvfp4_h4096_e512_k10": dict(_BASE, M=8, H=4096, E=512, k=10, I=1024, I_sh=1024, w_fmt=FMT_NVFP4,
                                  sh_fmt=FMT_MXFP8),
@@ -85,7 +91,7 @@ def _row_bytes(fmt, K):
 
 
 def _row_scales(fmt, K):
-    return K // 32 if fmt == FMT_MXFP8 else (K // 16 if fmt == FMT_NVFP4 else 0)
+    return K // 32 if fmt in (FMT_MXFP8, FMT_MXFP4) else (K // 16 if fmt == FMT_NVFP4 else 0)
 
 
 def weight(fmt, n_exp, rows, K, g, device, chunk_elems=1 << 28):
@@ -113,9 +119,13 @@ def weight(fmt, n_exp, rows, K, g, device, chunk_elems=1 << 28):
             sign = torch.randint(0, 2, (n, rows, K), generator=g, device=device)
             nib = (mag + 8 * sign).to(torch.uint8)
             vals[e0:e1] = nib[..., 0::2] | (nib[..., 1::2] << 4)
-            scales[e0:e1] = torch.randint(0x30, 0x41, (n, rows, K // 16), generator=g,
-                                          device=device).to(torch.uint8)
-            gs[e0:e1] = (2.0 ** -8) * (1.0 + 0.25 * torch.rand(n, generator=g, device=device))
+            if fmt == FMT_MXFP4:
+                scales[e0:e1] = torch.randint(119, 121, (n, rows, K // 32), generator=g,
+                                              device=device).to(torch.uint8)
+            else:
+                scales[e0:e1] = torch.randint(0x30, 0x41, (n, rows, K // 16), generator=g,
+                                              device=device).to(torch.uint8)
+                gs[e0:e1] = (2.0 ** -8) * (1.0 + 0.25 * torch.rand(n, generator=g, device=device))
     return vals, scales, gs
 
 

@@ -23,7 +23,7 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-FMT_BF16, FMT_MXFP8, FMT_NVFP4 = 0, 1, 2
+FMT_BF16, FMT_MXFP8, FMT_NVFP4, FMT_MXFP4 = 0, 1, 2, 3
 
 
 def build(force: bool = False) -> str:
@@ -106,7 +106,7 @@ def row_bytes(fmt, K):
 
 
 def row_scales(fmt, K):
-    return K // 32 if fmt == FMT_MXFP8 else (K // 16 if fmt == FMT_NVFP4 else 0)
+    return K // 32 if fmt in (FMT_MXFP8, FMT_MXFP4) else (K // 16 if fmt == FMT_NVFP4 else 0)
 
 
 def e4m3_decode(b):

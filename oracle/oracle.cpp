@@ -19,7 +19,8 @@
 //  [GB10]    "SGLang Spark GB10 Optimizations", "Key Optimizations 1": the MoE sum
 //            takes a routed_scaling_factor.
 //  Block formats follow the OCP Microscaling (MX) definitions of E4M3, E2M1 and
-//  E8M0; NVFP4 is E2M1 values with an E4M3 scale per 16 and an fp32 global scale.
+//  E8M0 (MXFP8: E4M3 + E8M0 per 32; MXFP4: packed E2M1 + E8M0 per 32); NVFP4 is E2M1
+//  values with an E4M3 scale per 16 and an fp32 global scale.
 //
 // Readings where the pages are silent (named A1..A13 in the design notes):
 //  A1 score = fp32 rounding of the sigmoid evaluated in double.
@@ -40,7 +41,7 @@
 
 namespace {
 
-enum { FMT_BF16 = 0, FMT_MXFP8 = 1, FMT_NVFP4 = 2 };
+enum { FMT_BF16 = 0, FMT_MXFP8 = 1, FMT_NVFP4 = 2, FMT_MXFP4 = 3 };
 
 // ---------------------------------------------------------------- number formats
 // Round a non-negative double to a binary format with `mbits` explicit mantissa
@@ -171,6 +172,23 @@ void quant_nvfp4_block(const float* v, float gs, uint8_t* q /*8 bytes*/, uint8_t
     }
 }
 
+// MXFP4 (OCP MX: E2M1 elements, one E8M0 scale per 32), one block of 32 fp32 values,
+// the rule of A3 with E2M1's largest value: e is the smallest integer in [-127, 127] with
+// amax <= 6 * 2^e (e = -127 when amax = 0); element = E2M1(v * 2^-e); low nibble = even
+// element.
+void quant_mxfp4_block(const float* v, uint8_t* q /*16 bytes*/, uint8_t* s) {
+    float amax = 0.0f;
+    for (int i = 0; i < 32; ++i) amax = std::max(amax, std::fabs(v[i]));
+    int e = -127;
+    if (amax > 0.0f) {
+        while (e < 127 && (double)amax > std::ldexp(6.0, e)) ++e;
+    }
+    *s = (uint8_t)(e + 127);
+    float inv = std::ldexp(1.0f, -e);
+    for (int i = 0; i < 16; ++i)
+        q[i] = (uint8_t)(e2m1_encode(v[2 * i] * inv) | (e2m1_encode(v[2 * i + 1] * inv) << 4));
+}
+
 // Bytes of one K-row of codes for a format.
 int64_t row_bytes(int fmt, int64_t K) {
     if (fmt == FMT_BF16) return 2 * K;
@@ -178,7 +196,7 @@ int64_t row_bytes(int fmt, int64_t K) {
     return K / 2;
 }
 int64_t row_scales(int fmt, int64_t K) {
-    if (fmt == FMT_MXFP8) return K / 32;
+    if (fmt == FMT_MXFP8 || fmt == FMT_MXFP4) return K / 32;
     if (fmt == FMT_NVFP4) return K / 16;
     return 0;
 }
@@ -189,6 +207,8 @@ void quant_row(int fmt, const float* v, int64_t K, float gs, uint8_t* q, uint8_t
         for (int64_t b = 0; b < K / 32; ++b) quant_mxfp8_block(v + 32 * b, q + 32 * b, s + b);
     } else if (fmt == FMT_NVFP4) {
         for (int64_t b = 0; b < K / 16; ++b) quant_nvfp4_block(v + 16 * b, gs, q + 8 * b, s + b);
+    } else if (fmt == FMT_MXFP4) {
+        for (int64_t b = 0; b < K / 32; ++b) quant_mxfp4_block(v + 32 * b, q + 16 * b, s + b);
     } else {
         uint16_t* o = (uint16_t*)q;
         for (int64_t i = 0; i < K; ++i) o[i] = double_to_bf16((double)v[i]);
@@ -204,6 +224,12 @@ void dequant_row(int fmt, const uint8_t* q, const uint8_t* s, double gs, int64_t
             uint8_t byte = q[i / 2];
             uint8_t nib = (i & 1) ? (byte >> 4) : (byte & 15);
             out[i] = e2m1_decode(nib) * e4m3_decode(s[i / 16]) * gs;
+        }
+    } else if (fmt == FMT_MXFP4) {
+        for (int64_t i = 0; i < K; ++i) {
+            uint8_t byte = q[i / 2];
+            uint8_t nib = (i & 1) ? (byte >> 4) : (byte & 15);
+            out[i] = e2m1_decode(nib) * e8m0_decode(s[i / 32]);
         }
     } else {
         const uint16_t* b = (const uint16_t*)q;

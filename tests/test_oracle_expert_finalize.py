@@ -15,7 +15,7 @@ import pytest
 import torch
 
 import oracle
-from oracle import FMT_BF16, FMT_MXFP8, FMT_NVFP4
+from oracle import FMT_BF16, FMT_MXFP4, FMT_MXFP8, FMT_NVFP4
 from moe_decode_step_router_gb300 import synth
 
 E2M1 = np.array([0, .5, 1, 1.5, 2, 3, 4, 6, -0., -.5, -1, -1.5, -2, -3, -4, -6])
@@ -28,9 +28,11 @@ def _deq_indep(fmt, vals, scales, gs, K):
         v = torch.from_numpy(np.ascontiguousarray(vals)).view(torch.float8_e4m3fn).double().numpy()
         s = np.ldexp(1.0, scales.astype(np.int64) - 127)
         return v * np.repeat(s, 32, axis=-1)
-    if fmt == FMT_NVFP4:
+    if fmt in (FMT_NVFP4, FMT_MXFP4):
         lo, hi = vals & 15, vals >> 4
         nib = np.stack([lo, hi], axis=-1).reshape(vals.shape[:-1] + (K,))
+        if fmt == FMT_MXFP4:
+            return E2M1[nib] * np.repeat(np.ldexp(1.0, scales.astype(np.int64) - 127), 32, axis=-1)
         s = torch.from_numpy(np.ascontiguousarray(scales)).view(torch.float8_e4m3fn).double().numpy()
         return E2M1[nib] * np.repeat(s, 16, axis=-1) * float(gs)
     return torch.from_numpy(np.ascontiguousarray(vals)).view(torch.bfloat16).double().numpy()
@@ -106,7 +108,7 @@ def test_expert_fc2_one_hot_rows():
     assert np.all(y == hd[col])
 
 
-@pytest.mark.parametrize("fmt", [FMT_MXFP8, FMT_NVFP4, FMT_BF16])
+@pytest.mark.parametrize("fmt", [FMT_MXFP8, FMT_NVFP4, FMT_MXFP4, FMT_BF16])
 def test_expert_brute_force(fmt):
     H, I = 128, 64
     g = synth._gen(5, "cpu")
@@ -132,6 +134,9 @@ def test_expert_brute_force(fmt):
     elif fmt == FMT_NVFP4:    # largest E2M1 half-gap is 1 (between 4 and 6) of a block max near 6
         blk = np.repeat(np.abs(h_ref).reshape(-1, 16).max(1), 16)
         assert (err <= blk * (1.0 / 6.0) * (1 + 2 ** -3)).all()
+    elif fmt == FMT_MXFP4:    # half-gap 1 at scale 2^e, block max in (3, 6] * 2^e (plus fp32 of h)
+        blk = np.repeat(np.abs(h_ref).reshape(-1, 32).max(1), 32)
+        assert (err <= blk / 3.0 * (1 + 2 ** -20)).all()
     else:
         assert (err <= 2 ** -8 * np.abs(h_ref)).all()
 

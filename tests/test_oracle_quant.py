@@ -11,7 +11,7 @@ import numpy as np
 import torch
 
 import oracle
-from oracle import FMT_MXFP8, FMT_NVFP4
+from oracle import FMT_MXFP4, FMT_MXFP8, FMT_NVFP4
 
 E2M1_GRID = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
 
@@ -141,3 +141,59 @@ def test_quant_x_bf16_input_is_exact_fp32():
     q1, s1 = oracle.quant_x(FMT_MXFP8, x16)
     q2, s2 = oracle.quant(FMT_MXFP8, xf.float().numpy())
     assert (q1 == q2).all() and (s1 == s2).all()
+
+
+# ---- MXFP4 (OCP MX: packed E2M1 + E8M0 per 32; scale rule of A3 with E2M1's maximum 6)
+def test_mxfp4_block_of_ones():
+    q, s = oracle.quant(FMT_MXFP4, np.ones((1, 32), np.float32))
+    assert s[0, 0] == 125          # 6 * 2^-3 < 1 <= 6 * 2^-2
+    assert (q == 0x66).all()       # 1 * 2^2 = 4 = E2M1 0b0110 in both nibbles
+
+
+def test_mxfp4_scale_rule_property():
+    rng = np.random.default_rng(5)
+    for scale in (1e-20, 1e-3, 1.0, 3.0, 1e5, 1e30):
+        v = (rng.standard_normal((64, 32)) * scale).astype(np.float32)
+        q, s = oracle.quant(FMT_MXFP4, v)
+        for r in range(64):
+            t = float(np.abs(v[r]).max()) * 2.0 ** -(int(s[r, 0]) - 127)
+            assert 3.0 < t <= 6.0, (scale, r, t)
+
+
+def test_mxfp4_matches_independent():
+    rng = np.random.default_rng(8)
+    v = (rng.standard_normal((6, 64)) * rng.choice([0.01, 1.0, 20.0], size=(6, 1))).astype(np.float32)
+    v[3, 32:] = 0.0
+    q, s = oracle.quant(FMT_MXFP4, v)
+    for r in range(6):
+        for b in range(2):
+            blk = v[r, 32 * b:32 * b + 32]
+            amax = float(np.abs(blk).max())
+            e = -127
+            while amax > 0 and e < 127 and amax > 6.0 * 2.0 ** e:   # power-of-two search
+                e += 1
+            assert s[r, b] == e + 127
+            for i in range(32):
+                want = _e2m1_brute(float(np.float32(blk[i]) * np.float32(2.0 ** -e)))
+                byte = q[r, 16 * b + i // 2]
+                got = (byte >> 4) if i & 1 else (byte & 15)
+                assert got == want, (r, b, i)
+
+
+def test_mxfp4_grid_roundtrip():
+    # values on the E2M1 grid times a power of two come back exactly
+    rng = np.random.default_rng(9)
+    grid = np.array(E2M1_GRID[1:] + [-g for g in E2M1_GRID[1:]], np.float64)
+    for e in (-20, -3, 0, 5):
+        v = rng.choice(grid, size=(4, 32)) * 2.0 ** e
+        v[:, 0] = 6.0 * 2.0 ** e                      # the block maximum fixes the scale at e
+        q, s = oracle.quant(FMT_MXFP4, v.astype(np.float32))
+        assert (s == e + 127).all()
+        assert np.array_equal(oracle.dequant(FMT_MXFP4, q, s, 32), v)
+
+
+def test_mxfp4_dequant_values():
+    q = np.array([[0x21] * 16], np.uint8)             # even elements 0.5, odd elements 1.0
+    s = np.array([[129]], np.uint8)                   # 2^2
+    d = oracle.dequant(FMT_MXFP4, q, s, 32)
+    assert (d[0, 0::2] == 2.0).all() and (d[0, 1::2] == 4.0).all()
