@@ -352,7 +352,7 @@ def main():
 
     def proj(fmt, rows, K):
         rb = 2 * K if fmt == 0 else (K if fmt == 1 else K // 2)
-        rs = K // 32 if fmt == 1 else (K // 16 if fmt == 2 else 0)
+        rs = K // 32 if fmt in (1, 3) else (K // 16 if fmt == 2 else 0)
         return rows * (rb + rs) + (4 if fmt == 2 else 0)
 
     I, Ish = cfg["I"], cfg["I_sh"]
@@ -409,7 +409,7 @@ def main():
     if rank == 0:
         line = {"metric": METRIC, "value": gbs * world, "unit": "GB/s", "n_gpus": world, "steps": a.steps,
                 "warmup": a.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "mxfp8" if cfg["w_fmt"] == 1 else "nvfp4",
+                "vs_baseline": None, "dtype": synth.FMT_NAMES[cfg["w_fmt"]],
                 "data": "synthetic (seeded): inputs of the workload's shapes, random weights",
                 "config": {"workload": cfg["name"], "rows": M, "H": H, "E": cfg["E"], "k": cfg["k"], "I": I,
                            "shared_I": Ish, "swiglu_limit": cfg.get("swiglu_limit", 0.0),

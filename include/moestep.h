@@ -41,17 +41,18 @@
  *  - bf16 tensors are row-major; x and residual are [M, H]; Wg is [E, H]; gamma is [H].
  *  - Canonical expert weights (inputs of moe_pack_weights), per projection:
  *      codes  [n_exp][rows][row_bytes]  MXFP8: 1 byte/element (E4M3);
- *                                       NVFP4: 2 elements/byte, low nibble = even element;
- *                                       BF16: 2 bytes/element
- *      scales [n_exp][rows][K/32] E8M0 (MXFP8) or [n_exp][rows][K/16] E4M3 (NVFP4)
+ *                                       NVFP4, MXFP4: 2 E2M1 elements/byte, low nibble =
+ *                                       even element; BF16: 2 bytes/element
+ *      scales [n_exp][rows][K/32] E8M0 (MXFP8, MXFP4) or [n_exp][rows][K/16] E4M3 (NVFP4)
  *      W13 rows: gate rows 0..I-1, then up rows I..2I-1, K = H.   W2 rows: H, K = I.
  *      NVFP4 global scales: fp32 [n_exp] per projection (passed to the GEMM calls).
  *  - Packed weights (outputs of moe_pack_weights): one record per (expert, 128-row
  *    block, 128-byte K step), records of one block contiguous. A record holds the
  *    block's 128 x 128 B codes in the 128-byte swizzled shared-memory image (16-byte
  *    chunk c of row r at chunk position c ^ (r & 7)), followed by its block scales as
- *    512-byte atoms (MXFP8: 1 atom of the four E8M0 scales of the step; NVFP4: 4 atoms of
- *    four E4M3 scales each, one per 64-element MMA step), row r's four bytes at
+ *    512-byte atoms (MXFP8: 1 atom of the four E8M0 scales of the step; MXFP4: 2 atoms of
+ *    four E8M0 scales each, one per two 64-element MMA steps; NVFP4: 4 atoms of four E4M3
+ *    scales each, one per 64-element MMA step), row r's four bytes at
  *    offset (r % 32) * 16 + (r / 32) * 4. W13 blocks interleave 64 gate rows and the
  *    64 matching up rows.
  *  - Tiled activations (xq, and the hidden activations of a selected expert): rows are
@@ -81,13 +82,13 @@ typedef enum {
     MOE_ERR_TIMEOUT = 4
 } moe_status;
 
-typedef enum { MOE_FMT_BF16 = 0, MOE_FMT_MXFP8 = 1, MOE_FMT_NVFP4 = 2 } moe_fmt;
+typedef enum { MOE_FMT_BF16 = 0, MOE_FMT_MXFP8 = 1, MOE_FMT_NVFP4 = 2, MOE_FMT_MXFP4 = 3 } moe_fmt;
 
 typedef enum { MOE_W13 = 0, MOE_W2 = 1, MOE_SH13 = 2, MOE_SH2 = 3 } moe_proj;
 
 /* One MoE layer. Limits: 1 <= k <= 16, k <= E <= 512; H % 256 == 0 and 1024 <= H <= 8192;
- * I, I_shared % 256 == 0 and 256 <= I <= 4096. w_fmt is MXFP8 or NVFP4; shared_fmt is
- * BF16, MXFP8 or NVFP4. gs_a1 / gs_a2 are the static NVFP4 global scales of the routed
+ * I, I_shared % 256 == 0 and 256 <= I <= 4096. w_fmt is MXFP8, NVFP4 or MXFP4; shared_fmt is
+ * BF16, MXFP8, NVFP4 or MXFP4. gs_a1 / gs_a2 are the static NVFP4 global scales of the routed
  * experts' FC1 and FC2 inputs (gs_a1_shared / gs_a2_shared for the shared expert);
  * they are ignored for other formats. swiglu_limit > 0 selects the clamped SwiGLU of the
  * routed and the shared experts ("SGLang-NVIDIA-Mega" README, shared_ll row): the gate

@@ -66,12 +66,13 @@ moe_status check_desc(const moe_layer_desc* d) {
     REQUIRE(d->E >= 1 && d->E <= kMaxE, "E=%d: need 1 <= E <= %d", d->E, kMaxE);
     REQUIRE(d->k >= 1 && d->k <= kMaxK && d->k <= d->E, "k=%d: need 1 <= k <= min(16, E)", d->k);
     REQUIRE(d->I >= 256 && d->I <= 4096 && d->I % 256 == 0, "I=%d: need 256 <= I <= 4096, I %% 256 == 0", d->I);
-    if (d->w_fmt != MOE_FMT_MXFP8 && d->w_fmt != MOE_FMT_NVFP4)
-        return fail(MOE_ERR_UNSUPPORTED, "routed weight format %d has no kernel (MXFP8=1, NVFP4=2)", d->w_fmt);
+    if (d->w_fmt != MOE_FMT_MXFP8 && d->w_fmt != MOE_FMT_NVFP4 && d->w_fmt != MOE_FMT_MXFP4)
+        return fail(MOE_ERR_UNSUPPORTED, "routed weight format %d has no kernel (MXFP8=1, NVFP4=2, MXFP4=3)",
+                    d->w_fmt);
     if (d->has_shared) {
         REQUIRE(d->I_shared >= 256 && d->I_shared <= 4096 && d->I_shared % 256 == 0,
                 "I_shared=%d: need 256 <= I_shared <= 4096, %% 256 == 0", d->I_shared);
-        if (d->shared_fmt != MOE_FMT_BF16 && d->shared_fmt != MOE_FMT_MXFP8 && d->shared_fmt != MOE_FMT_NVFP4)
+        if (d->shared_fmt < MOE_FMT_BF16 || d->shared_fmt > MOE_FMT_MXFP4)
             return fail(MOE_ERR_UNSUPPORTED, "shared weight format %d has no kernel", d->shared_fmt);
     }
     REQUIRE(d->routed_scaling_factor == d->routed_scaling_factor, "routed_scaling_factor is NaN");
@@ -247,7 +248,8 @@ struct QuantArgs {
 
 int quant_units_host(int fmt, int M, int H) {
     const int Mpad = round_up(M, 16);
-    return fmt == MOE_FMT_MXFP8 ? Mpad * (H / 32) : (fmt == MOE_FMT_NVFP4 ? Mpad * (H / 16) : Mpad * (H / 8));
+    return (fmt == MOE_FMT_MXFP8 || fmt == MOE_FMT_MXFP4) ? Mpad * (H / 32)
+                                                          : (fmt == MOE_FMT_NVFP4 ? Mpad * (H / 16) : Mpad * (H / 8));
 }
 
 moe_status launch_topk_route(const moe_layer_desc* d, const WsLayout& L, uint8_t* ws, int M, const float* scores,
@@ -475,11 +477,11 @@ size_t moe_packed_bytes(const moe_layer_desc* d, int which) {
 }
 
 size_t moe_act_bytes(int fmt, int rows, int K) {
-    if (fmt < 0 || fmt > 2 || rows < 1 || rows > kMaxRows || K <= 0 || row_bytes(fmt, K) % kStepBytes) return 0;
+    if (fmt < 0 || fmt > 3 || rows < 1 || rows > kMaxRows || K <= 0 || row_bytes(fmt, K) % kStepBytes) return 0;
     return act_bytes(fmt, rows, K);
 }
 size_t moe_act_scale_bytes(int fmt, int rows, int K) {
-    if (fmt < 0 || fmt > 2 || rows < 1 || rows > kMaxRows || K <= 0 || row_bytes(fmt, K) % kStepBytes) return 0;
+    if (fmt < 0 || fmt > 3 || rows < 1 || rows > kMaxRows || K <= 0 || row_bytes(fmt, K) % kStepBytes) return 0;
     return act_scale_bytes(fmt, K);
 }
 size_t moe_hq_bytes(const moe_layer_desc* d, int max_rows) {

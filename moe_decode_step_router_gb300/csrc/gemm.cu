@@ -342,7 +342,10 @@ __device__ __forceinline__ int mma_segment(uint32_t ready0, uint32_t empty0, Rin
     uint32_t id[4];
 #pragma unroll
     for (int sub = 0; sub < 4; ++sub)
-        id[sub] = FMT == MOE_FMT_MXFP8 ? idesc_mxf8(N, sub) : (FMT == MOE_FMT_NVFP4 ? idesc_nvf4(N) : idesc_bf16(N));
+        id[sub] = FMT == MOE_FMT_MXFP8   ? idesc_mxf8(N, sub)
+                  : FMT == MOE_FMT_MXFP4 ? idesc_mxf4(N, 2 * (sub % 2))
+                  : FMT == MOE_FMT_NVFP4 ? idesc_nvf4(N)
+                                         : idesc_bf16(N);
     int issued = 0;
     for (int kk = ka; kk < kb; ++kk, rg.adv1()) {
         const int st = rg.st;
@@ -361,6 +364,19 @@ __device__ __forceinline__ int mma_segment(uint32_t ready0, uint32_t empty0, Rin
 #pragma unroll
             for (int sub = 0; sub < 4; ++sub)
                 mma_mxf8(d_tmem, ad + 2 * sub, bd + 2 * sub, id[sub], sfa, sfb, sub ? 1u : acc0);
+        } else if (FMT == MOE_FMT_MXFP4) {
+            // two scale atoms per step; MMA sub reads atom sub / 2, byte pair 2 * (sub % 2)
+            if (CP) {
+#pragma unroll
+                for (int a = 0; a < 2; ++a) {
+                    tc_cp_sf(sfa + 4 * a, sfadesc0 + so + 32 * a);
+                    tc_cp_sf(sfb + 4 * a, sfbdesc0 + so + 32 * a);
+                }
+            }
+#pragma unroll
+            for (int sub = 0; sub < 4; ++sub)
+                mma_mxf4(d_tmem, ad + 2 * sub, bd + 2 * sub, id[sub], sfa + 4 * (sub / 2), sfb + 4 * (sub / 2),
+                         sub ? 1u : acc0);
         } else if (FMT == MOE_FMT_NVFP4) {
 #pragma unroll
             for (int sub = 0; sub < 4; ++sub)
@@ -639,9 +655,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                 if (p.sf_warps) {
                     if (C.fmt == MOE_FMT_MXFP8) n = MOE_SEG(MOE_FMT_MXFP8, false);
                     else if (C.fmt == MOE_FMT_NVFP4) n = MOE_SEG(MOE_FMT_NVFP4, false);
+                    else if (C.fmt == MOE_FMT_MXFP4) n = MOE_SEG(MOE_FMT_MXFP4, false);
                     else n = MOE_SEG(MOE_FMT_BF16, false);
                 } else {
                     if (C.fmt == MOE_FMT_MXFP8) n = MOE_SEG(MOE_FMT_MXFP8, true);
+                    else if (C.fmt == MOE_FMT_MXFP4) n = MOE_SEG(MOE_FMT_MXFP4, true);
                     else if (C.fmt == MOE_FMT_BF16) n = MOE_SEG(MOE_FMT_BF16, true);
                     else {
                         set_error(p.status, sm.abort_flag, MOE_ERR_UNSUPPORTED);
@@ -877,6 +895,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                         }
                         if (lane == 0)
                             hs_g[(size_t)sidx * kAtomBytes + (rg % 32) * 16 + (rg / 32) * 4 + (cb / 32)] = (uint8_t)(e + 127);
+                    } else if (C.out_fmt == MOE_FMT_MXFP4) {
+                        // one 32-feature block per warp: E8M0 exponent of the rule amax <= 6 * 2^e
+                        const float amax = warp_max_f(fabsf(h));
+                        const int e = mx4_exponent(amax);
+                        const uint32_t nib = e2m1x2(0.0f, __fmul_rn(h, exp2_int(-e))) & 0xFu;
+                        const uint32_t nb1 = __shfl_down_sync(0xffffffffu, nib, 1);
+                        const uint32_t byte = nib | (nb1 << 4);
+                        const uint32_t y1 = __shfl_down_sync(0xffffffffu, byte, 2);
+                        const uint32_t y2 = __shfl_down_sync(0xffffffffu, byte, 4);
+                        const uint32_t y3 = __shfl_down_sync(0xffffffffu, byte, 6);
+                        const int sidx = f / 256, cbyte = (f % 256) / 2;
+                        if ((lane & 7) == 0) {
+                            uint8_t* row = hq_g + (size_t)sidx * Rp * kStepBytes + (size_t)rg * kStepBytes;
+                            *reinterpret_cast<uint32_t*>(row + (((cbyte / 16) ^ (rg & 7)) * 16) + (cbyte % 16)) =
+                                (byte & 0xFFu) | ((y1 & 0xFFu) << 8) | ((y2 & 0xFFu) << 16) | ((y3 & 0xFFu) << 24);
+                        }
+                        if (lane == 0) {
+                            const int j = (f % 256) / 32;
+                            hs_g[(size_t)sidx * 2 * kAtomBytes + (j / 4) * kAtomBytes + (rg % 32) * 16 + (rg / 32) * 4 +
+                                 (j % 4)] = (uint8_t)(e + 127);
+                        }
                     } else if (C.out_fmt == MOE_FMT_NVFP4) {
                         float amax = fabsf(h);
 #pragma unroll

@@ -28,11 +28,11 @@ __host__ __device__ inline int64_t row_bytes(int fmt, int64_t K) {
     return fmt == MOE_FMT_BF16 ? 2 * K : (fmt == MOE_FMT_MXFP8 ? K : K / 2);
 }
 __host__ __device__ inline int64_t row_scales(int fmt, int64_t K) {
-    return fmt == MOE_FMT_MXFP8 ? K / 32 : (fmt == MOE_FMT_NVFP4 ? K / 16 : 0);
+    return (fmt == MOE_FMT_MXFP8 || fmt == MOE_FMT_MXFP4) ? K / 32 : (fmt == MOE_FMT_NVFP4 ? K / 16 : 0);
 }
-// Scale atoms per 128-byte K step (MXFP8 1, NVFP4 4, BF16 0).
+// Scale atoms per 128-byte K step (MXFP8 1, MXFP4 2, NVFP4 4, BF16 0).
 __host__ __device__ inline int atoms_per_step(int fmt) {
-    return fmt == MOE_FMT_MXFP8 ? 1 : (fmt == MOE_FMT_NVFP4 ? 4 : 0);
+    return fmt == MOE_FMT_MXFP8 ? 1 : (fmt == MOE_FMT_MXFP4 ? 2 : (fmt == MOE_FMT_NVFP4 ? 4 : 0));
 }
 __host__ __device__ inline int steps_of(int fmt, int K) { return (int)(row_bytes(fmt, K) / kStepBytes); }
 // Packed record: 128 rows x 128 B of codes plus the step's scale atoms.

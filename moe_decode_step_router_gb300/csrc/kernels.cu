@@ -37,7 +37,7 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 // ------------------------------------------------------------------------------------
-// FC1 input quantisation into the tiled layout. Unit = one scale block (MXFP8: 32
+// FC1 input quantisation into the tiled layout. Unit = one scale block (MXFP8, MXFP4: 32
 // elements, NVFP4: 16) or one 16-byte chunk (BF16) of one padded row; rows >= M are zero.
 __device__ void quant_unit(const uint16_t* __restrict__ x, int M, int H, int Mpad, int fmt, float gs, uint8_t* xq,
                            uint8_t* xs, int u) {
@@ -75,6 +75,38 @@ __device__ void quant_unit(const uint16_t* __restrict__ x, int M, int H, int Mpa
         *reinterpret_cast<uint4*>(row + ((c0 ^ (m & 7)) * 16)) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
         *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (m & 7)) * 16)) = make_uint4(wd[4], wd[5], wd[6], wd[7]);
         xs[(size_t)s * kAtomBytes + (m % 32) * 16 + (m / 32) * 4 + (bi % 4)] = (uint8_t)(e + 127);
+    } else if (fmt == MOE_FMT_MXFP4) {
+        const int nb = H / 32, m = u / nb, bi = u % nb;
+        float v[32];
+        if (m < M) {
+            const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)m * H + 32 * bi);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint4 w = __ldg(src + i);
+                v[8 * i + 0] = bf16_lo(w.x); v[8 * i + 1] = bf16_hi(w.x);
+                v[8 * i + 2] = bf16_lo(w.y); v[8 * i + 3] = bf16_hi(w.y);
+                v[8 * i + 4] = bf16_lo(w.z); v[8 * i + 5] = bf16_hi(w.z);
+                v[8 * i + 6] = bf16_lo(w.w); v[8 * i + 7] = bf16_hi(w.w);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        const int e = mx4_exponent(amax);
+        const float sc = exp2_int(-e);
+        uint32_t wd[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            wd[i / 4] |= (uint32_t)e2m1x2(__fmul_rn(v[2 * i + 1], sc), __fmul_rn(v[2 * i], sc)) << (8 * (i % 4));
+        // a 256-element step holds 8 blocks of 16 bytes each
+        const int s = bi / 8, c = bi % 8;
+        uint8_t* row = xq + (size_t)s * Mpad * kStepBytes + (size_t)m * kStepBytes;
+        *reinterpret_cast<uint4*>(row + ((c ^ (m & 7)) * 16)) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+        xs[(size_t)s * 2 * kAtomBytes + (c / 4) * kAtomBytes + (m % 32) * 16 + (m / 32) * 4 + (c % 4)] =
+            (uint8_t)(e + 127);
     } else if (fmt == MOE_FMT_NVFP4) {
         const int nb = H / 16, m = u / nb, bi = u % nb;
         float v[16];
@@ -121,7 +153,8 @@ __device__ void quant_unit(const uint16_t* __restrict__ x, int M, int H, int Mpa
 }
 
 __device__ __forceinline__ int quant_units(int fmt, int Mpad, int H) {
-    return fmt == MOE_FMT_MXFP8 ? Mpad * (H / 32) : (fmt == MOE_FMT_NVFP4 ? Mpad * (H / 16) : Mpad * (H / 8));
+    return (fmt == MOE_FMT_MXFP8 || fmt == MOE_FMT_MXFP4) ? Mpad * (H / 32)
+                                                          : (fmt == MOE_FMT_NVFP4 ? Mpad * (H / 16) : Mpad * (H / 8));
 }
 
 // ------------------------------------------------------------------------------------

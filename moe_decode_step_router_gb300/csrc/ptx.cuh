@@ -165,6 +165,15 @@ __device__ __forceinline__ void mma_nvf4(uint32_t d, uint64_t a, uint64_t b, uin
         "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb)
         : "memory");
 }
+__device__ __forceinline__ void mma_mxf4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                         uint32_t sfb, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::
+            "r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb)
+        : "memory");
+}
 __device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
@@ -208,6 +217,12 @@ __host__ __device__ __forceinline__ uint32_t idesc_mxf8(uint32_t N, uint32_t sf_
 }
 __host__ __device__ __forceinline__ uint32_t idesc_nvf4(uint32_t N) {
     return (0u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | (0u << 23) | ((128u >> 4) << 24);
+}
+// MXFP4: E2M1 A and B (type 1 of kind::mxf4nvf4), E8M0 scales (bit 23), two scale bytes
+// per row and MMA: sf_id 0 or 2 picks the pair within the scale word.
+__host__ __device__ __forceinline__ uint32_t idesc_mxf4(uint32_t N, uint32_t sf_id) {
+    return (sf_id << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | (1u << 23) | ((128u >> 4) << 24) |
+           (sf_id << 29);
 }
 __host__ __device__ __forceinline__ uint32_t idesc_bf16(uint32_t N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((128u >> 4) << 24);

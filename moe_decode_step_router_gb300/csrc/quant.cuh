@@ -1,5 +1,5 @@
 // Device encoders for the block formats of the MoE step (MXFP8: E4M3 + E8M0 per 32;
-// NVFP4: E2M1 + E4M3 per 16 with an fp32 global scale). All arithmetic that decides a
+// MXFP4: E2M1 + E8M0 per 32; NVFP4: E2M1 + E4M3 per 16 with an fp32 global scale). All arithmetic that decides a
 // code is IEEE fp32 with explicit rounding (no contraction), so the codes equal those
 // of any other exact fp32 implementation of the same rule.
 #pragma once
@@ -44,6 +44,17 @@ __device__ __forceinline__ int mx_exponent(float amax) {
     const uint32_t u = __float_as_uint(amax);
     int E = (int)((u >> 23) & 0xFF) - 127;
     int e = E - 8 + (((u & 0x7FFFFFu) > 0x600000u) ? 1 : 0);
+    if ((u >> 23) == 0) e = -127;  // subnormal amax
+    return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// MXFP4 block exponent: the smallest e in [-127, 127] with amax <= 6 * 2^e (6 = 1.5 * 2^2):
+// e = E - 2, plus one when amax's significand exceeds 1.5.
+__device__ __forceinline__ int mx4_exponent(float amax) {
+    if (!(amax > 0.0f)) return -127;
+    const uint32_t u = __float_as_uint(amax);
+    int E = (int)((u >> 23) & 0xFF) - 127;
+    int e = E - 2 + (((u & 0x7FFFFFu) > 0x400000u) ? 1 : 0);
     if ((u >> 23) == 0) e = -127;  // subnormal amax
     return e < -127 ? -127 : (e > 127 ? 127 : e);
 }

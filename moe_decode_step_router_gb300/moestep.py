@@ -14,7 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libmoestep.so")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT = range(5)
-MOE_FMT_BF16, MOE_FMT_MXFP8, MOE_FMT_NVFP4 = 0, 1, 2
+MOE_FMT_BF16, MOE_FMT_MXFP8, MOE_FMT_NVFP4, MOE_FMT_MXFP4 = 0, 1, 2, 3
 MOE_W13, MOE_W2, MOE_SH13, MOE_SH2 = 0, 1, 2, 3
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA",
                 4: "MOE_ERR_TIMEOUT"}

@@ -35,7 +35,7 @@ def row_bytes(fmt, K):
 
 
 def row_scales(fmt, K):
-    return K // 32 if fmt == 1 else (K // 16 if fmt == 2 else 0)
+    return K // 32 if fmt in (1, 3) else (K // 16 if fmt == 2 else 0)
 
 
 def untile(buf, fmt, rows, K, Rpad=None):
@@ -57,7 +57,7 @@ def untile_scales(buf, fmt, rows, K):
     buf = np.asarray(buf, np.uint8).ravel()
     rb = row_bytes(fmt, K)
     KS = rb // 128
-    A = 1 if fmt == 1 else 4
+    A = {1: 1, 2: 4, 3: 2}[fmt]
     at = buf[:KS * A * 512].reshape(KS, A, 512)
     out = np.zeros((rows, row_scales(fmt, K)), np.uint8)
     for r in range(rows):

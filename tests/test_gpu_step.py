@@ -17,6 +17,7 @@ SMALL = {
     "mx_bias": synth.config("tiny_mxfp8", H=2048, E=64, k=8, I=512, I_sh=512, has_bias=True, rsf=2.5),
     "nv_bf16": synth.config("nvfp4_h6144_e256_k8_16rows", H=1024, E=16, k=4, I=256, I_sh=256),
     "nv_mx": synth.config("nvfp4_h4096_e512_k10", H=1024, E=32, k=4, I=512, I_sh=256, emit_next=True),
+    "mx4_mx": synth.config("mxfp4_h7168_e256_k8", H=1024, E=16, k=4, I=256, I_sh=256),
 }
 
 
@@ -131,7 +132,8 @@ FULL = [("tiny_mxfp8", None, "auto"), ("mxfp8_h7168_e256_k8_8rows", None, "auto"
         ("nvfp4_h4096_e512_k10", 1, "auto"), ("nvfp4_h4096_e512_k10", 8, "auto"),
         ("nvfp4_h4096_e512_k10", 64, "auto"), ("mxfp8_h7168_e256_k8_8rows", None, "hybrid"),
         ("nvfp4_h6144_e256_k8_16rows", None, "dynamic"), ("nvfp4_h4096_e512_k10", 1, "dynamic"),
-        ("nvfp4_h4096_e512_k10", 32, "hybrid"), ("mxfp8_h7168_e256_k8_8rows", None, "dynamic")]
+        ("nvfp4_h4096_e512_k10", 32, "hybrid"), ("mxfp8_h7168_e256_k8_8rows", None, "dynamic"),
+        ("mxfp4_h7168_e256_k8", None, "auto"), ("mxfp4_h7168_e256_k8", 64, "auto")]
 
 
 @pytest.mark.parametrize("name,M,sched", FULL, ids=["%s-%s-%s" % f for f in FULL])
