@@ -153,6 +153,7 @@ WsLayout layout(const moe_layer_desc* d) {
     L.cnt_dn = take(4ull * L.U_dn);
     L.partials = take(4ull * kPartialSlots * kPartialFloats);
     L.sched = take(4ull * 4);  // gate_up and down: next work item, CTAs finished
+    L.gu_done = take(4ull * (kMaxE + 2));  // one launch for both GEMMs: per-group gate_up units done
     L.rpart = take(4ull * ((d->H + 511) / 512) * d->E * kMaxRows);
     L.rcnt = take(4ull * ((d->E + 7) / 8));
     L.total = o;
@@ -318,32 +319,20 @@ int gemm_pool_units(int grid) {
     return 0;
 }
 
-moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* wr, const moe_qweight* ws_,
-                       const GemmBuffers& b, int M, const WsLayout& L, uint8_t* ws, cudaStream_t st) {
-    DevInfo* di;
-    moe_status s = dev_info(&di);
-    if (s != MOE_OK) return s;
-    GemmParams p{};
-    p.mode = mode;
-    p.M = M;
-    p.k = d->k;
-    p.E = d->E;
-    p.H = d->H;
-    p.Mpad = round_up(M, 16);
-    p.has_shared = d->has_shared;
-    p.perm = b.perm;
-    p.groups = reinterpret_cast<const Group*>(ws + L.groups);
-    p.hdr = reinterpret_cast<const WsHeader*>(ws + L.header);
-    p.y = b.y;
-    p.counters = reinterpret_cast<int32_t*>(ws + (mode == 0 ? L.cnt_gu : L.cnt_dn));
-    p.partials = reinterpret_cast<float*>(ws + L.partials);
-    p.sched = reinterpret_cast<int32_t*>(ws + L.sched) + 2 * mode;
-    p.swiglu_limit = d->swiglu_limit > 0.0f ? d->swiglu_limit : 0.0f;
-    p.pool_units = gemm_pool_units(di->sms < kMaxGemmCtas ? di->sms : kMaxGemmCtas);
-    p.status = reinterpret_cast<int32_t*>(ws + L.header);
+// moe_step runs gate_up and down as one launch (a down item waits in the kernel for its
+// group's gate_up units) unless the environment variable MOE_FUSED_FFN=0, read at each
+// call, asks for the two separate launches.
+bool step_fuses_ffn() {
+    const char* e = getenv("MOE_FUSED_FFN");
+    return !(e && strcmp(e, "0") == 0);
+}
+
+// Weight classes of one GEMM (0 gate_up, 1 down): routed experts and the shared expert.
+void gemm_classes(int g, const moe_layer_desc* d, const moe_qweight* wr, const moe_qweight* ws_,
+                  const GemmBuffers& b, int M, GemmClass* cls) {
     const size_t hqr = hq_routed(d, M), hsr = hs_routed(d, M);
     for (int c = 0; c < 2; ++c) {
-        GemmClass& C = p.cls[c];
+        GemmClass& C = cls[c];
         const bool sh = c == 1;
         if (sh && !d->has_shared) {
             C.fmt = d->w_fmt;
@@ -359,7 +348,7 @@ moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* wr,
         C.I = I;
         C.out_fmt = C.fmt;
         const float gs1 = sh ? d->gs_a1_shared : d->gs_a1, gs2 = sh ? d->gs_a2_shared : d->gs_a2;
-        if (mode == 0) {
+        if (g == 0) {
             C.MB = 2 * I / kBlockRows;
             C.KS = steps_of(C.fmt, d->H);
             C.b = static_cast<const uint8_t*>(sh ? b.xq_sh : b.xq);
@@ -377,8 +366,45 @@ moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* wr,
             C.gs_out = 1.0f;
         }
     }
-    const int am = atoms_per_step(p.cls[0].fmt) > atoms_per_step(p.cls[1].fmt) ? atoms_per_step(p.cls[0].fmt)
-                                                                                : atoms_per_step(p.cls[1].fmt);
+}
+
+// One expert-GEMM launch: mode 0 gate_up, 1 down, 2 both (gate_up items first; a down item
+// waits in the kernel until its group's gate_up units are done).
+moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* w13, const moe_qweight* sh13,
+                       const moe_qweight* w2, const moe_qweight* sh2, const GemmBuffers& b, int M, const WsLayout& L,
+                       uint8_t* ws, cudaStream_t st) {
+    DevInfo* di;
+    moe_status s = dev_info(&di);
+    if (s != MOE_OK) return s;
+    GemmParams p{};
+    p.mode = mode;
+    p.M = M;
+    p.k = d->k;
+    p.E = d->E;
+    p.H = d->H;
+    p.Mpad = round_up(M, 16);
+    p.has_shared = d->has_shared;
+    p.perm = b.perm;
+    p.groups = reinterpret_cast<const Group*>(ws + L.groups);
+    p.hdr = reinterpret_cast<const WsHeader*>(ws + L.header);
+    p.y = b.y;
+    p.counters[0] = reinterpret_cast<int32_t*>(ws + L.cnt_gu);
+    p.counters[1] = reinterpret_cast<int32_t*>(ws + L.cnt_dn);
+    float* part = reinterpret_cast<float*>(ws + L.partials);
+    p.partials[0] = part;
+    // in one launch both GEMMs cut units at once: down uses the pool's slots (no pool then)
+    p.partials[1] = mode == 2 ? part + (size_t)kPoolSlot0 * kPartialFloats : part;
+    p.sched = reinterpret_cast<int32_t*>(ws + L.sched) + 2 * (mode == 1 ? 1 : 0);
+    p.gu_done = reinterpret_cast<int32_t*>(ws + L.gu_done);
+    p.swiglu_limit = d->swiglu_limit > 0.0f ? d->swiglu_limit : 0.0f;
+    p.pool_units = mode == 2 ? 0 : gemm_pool_units(di->sms < kMaxGemmCtas ? di->sms : kMaxGemmCtas);
+    p.status = reinterpret_cast<int32_t*>(ws + L.header);
+    if (mode != 1) gemm_classes(0, d, w13, sh13, b, M, p.cls[0]);
+    if (mode != 0) gemm_classes(1, d, w2, sh2, b, M, p.cls[1]);
+    const int g0 = mode == 1 ? 1 : 0;
+    int am = 0;
+    for (int g = g0; g <= (mode == 0 ? 0 : 1); ++g)
+        for (int c = 0; c < 2; ++c) am = atoms_per_step(p.cls[g][c].fmt) > am ? atoms_per_step(p.cls[g][c].fmt) : am;
     p.atoms_max = am;
     // NVFP4 stages carry 8 scale copies; issuing them from two extra warps keeps the MMA
     // issuers' streams short. MXFP8-only launches copy in the issuers (one hop less).
@@ -388,13 +414,13 @@ moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* wr,
     p.b_off = round_up(p.sfa_off + am * kAtomBytes, 1024);
     p.sfb_off = p.b_off + p.Mpad * kStepBytes;
     p.stage_bytes = round_up(p.sfb_off + am * kAtomBytes, 1024);
-    // alignment, epilogue staging, work-item queue, barriers and flags (1 KB covers those
+    // alignment, epilogue staging, work-item queue, deferred copies, barriers and flags (1 KB covers those
     // not counted per stage)
-    const int fixed = 1024 + p.Mpad * kBlockRows * 4 + kGemmQueue * 64 + 1024;
+    const int fixed = 1024 + p.Mpad * kBlockRows * 4 + kGemmQueue * 64 + kDeferBytes + 1024;
     int S = (di->smem_optin - fixed) / (p.stage_bytes + 24);  // + full/empty/ready barriers
     const int tmem_cap = am ? (512 - 2 * acc_bank_cols(am, p.Mpad)) / (8 * am) : 16;
     if (S > tmem_cap) S = tmem_cap;
-    if (S > 16) S = 16;
+    if (S > kMaxStages) S = kMaxStages;
     S &= ~1;  // even ring: items start on even slots
     if (S < 2) return fail(MOE_ERR_UNSUPPORTED, "not enough shared memory for the GEMM pipeline");
     p.stages = S;
@@ -408,7 +434,8 @@ moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* wr,
     int grid = di->sms;
     if (grid > kMaxGemmCtas) grid = kMaxGemmCtas;
     return launch_pdl(k_expert_gemm, dim3(grid), dim3(kGemmThreads), smem, st, p,
-                      mode == 0 ? "k_expert_gemm(gate_up) launch" : "k_expert_gemm(down) launch");
+                      mode == 0 ? "k_expert_gemm(gate_up) launch"
+                                : (mode == 1 ? "k_expert_gemm(down) launch" : "k_expert_gemm(gate_up+down) launch"));
 }
 
 moe_status launch_finalize(const moe_layer_desc* d, const float* y, const float* topk_w, const int32_t* inv_perm,
@@ -648,7 +675,7 @@ moe_status moe_expert_gate_up(const moe_layer_desc* d, const moe_qweight* w13, c
     b.hq = hq;
     b.hs = hq_scales;
     b.perm = perm;
-    s = launch_gemm(0, d, w13, sh13, b, M, L, static_cast<uint8_t*>(ws), (cudaStream_t)stream);
+    s = launch_gemm(0, d, w13, sh13, nullptr, nullptr, b, M, L, static_cast<uint8_t*>(ws), (cudaStream_t)stream);
     if (s != MOE_OK) return s;
     return ok();
 }
@@ -669,7 +696,7 @@ moe_status moe_expert_down(const moe_layer_desc* d, const moe_qweight* w2, const
     b.hq = const_cast<void*>(hq);
     b.hs = const_cast<void*>(hq_scales);
     b.y = y_pairs;
-    s = launch_gemm(1, d, w2, sh2, b, M, L, static_cast<uint8_t*>(ws), (cudaStream_t)stream);
+    s = launch_gemm(1, d, nullptr, nullptr, w2, sh2, b, M, L, static_cast<uint8_t*>(ws), (cudaStream_t)stream);
     if (s != MOE_OK) return s;
     return ok();
 }
@@ -748,10 +775,15 @@ moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void
     b.hs = w + L.hs;
     b.y = reinterpret_cast<float*>(w + L.y);
     b.perm = perm;
-    s = launch_gemm(0, d, &a->w13, &a->sh13, b, M, L, w, st);
-    if (s != MOE_OK) return s;
-    s = launch_gemm(1, d, &a->w2, &a->sh2, b, M, L, w, st);
-    if (s != MOE_OK) return s;
+    if (step_fuses_ffn()) {
+        s = launch_gemm(2, d, &a->w13, &a->sh13, &a->w2, &a->sh2, b, M, L, w, st);
+        if (s != MOE_OK) return s;
+    } else {
+        s = launch_gemm(0, d, &a->w13, &a->sh13, nullptr, nullptr, b, M, L, w, st);
+        if (s != MOE_OK) return s;
+        s = launch_gemm(1, d, nullptr, nullptr, &a->w2, &a->sh2, b, M, L, w, st);
+        if (s != MOE_OK) return s;
+    }
     s = launch_finalize(d, b.y, topk_w, inv_perm, M, a->residual, a->gamma, a->out,
                         d->emit_next_mxfp8 ? a->outq : nullptr, d->emit_next_mxfp8 ? a->outq_scales : nullptr, st);
     if (s != MOE_OK) return s;

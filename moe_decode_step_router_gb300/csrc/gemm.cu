@@ -31,6 +31,7 @@
 // Either way a slot's scale columns always have the same writer. Warps 2..5 add the two
 // banks and run the epilogue (gate_up: SwiGLU + requantisation into the tiled FC2 input;
 // down: fp32 rows in perm order).
+#include <climits>
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -46,7 +47,7 @@ constexpr int kMaxAcc = 8;  // up to 8 accumulator buffers per bank
 // One work item as published to the CTA's roles: the steps [ka, kb) of one unit with the
 // facts of its group, and where its partial sum goes when the unit is cut into pieces.
 struct WorkItem {
-    int cls;  // 0 routed, 1 shared, -1 end of the CTA's work
+    int cls;  // 2 * GEMM (0 gate_up, 1 down) + class (0 routed, 1 shared); -1 end of the CTA's work
     int b, ka, kb;
     int rot;  // the steps are taken in the order ka + (rot + j) % (kb - ka), j = 0, 1, ...
     int expert, rows, perm_off, row_off, gidx;
@@ -83,26 +84,27 @@ struct Ring {
 struct Walker {
     const Group* groups;
     long long T_r, T, t, t1;
-    int ngroups, MB0, KS0, MB1, KS1, M, ktop;
+    int gemm, ngroups, MB0, KS0, MB1, KS1, M, ktop;
     int cls, g, b, k;  // position of step t
     int4 cur, nxt;     // records of groups g and g + 1
-    // Steps of units [0, U0).
-    __device__ static long long steps_before(const GemmParams& p, int ngroups, int U0) {
-        const int NRU = ngroups * p.cls[0].MB;
-        return U0 <= NRU ? (long long)U0 * p.cls[0].KS
-                         : (long long)NRU * p.cls[0].KS + (long long)(U0 - NRU) * p.cls[1].KS;
+    // Steps of units [0, U0) of GEMM gm.
+    __device__ static long long steps_before(const GemmParams& p, int gm, int ngroups, int U0) {
+        const int NRU = ngroups * p.cls[gm][0].MB;
+        return U0 <= NRU ? (long long)U0 * p.cls[gm][0].KS
+                         : (long long)NRU * p.cls[gm][0].KS + (long long)(U0 - NRU) * p.cls[gm][1].KS;
     }
-    __device__ void init(const GemmParams& p, int ngroups_, int G, int c, int U0) {
+    __device__ void init(const GemmParams& p, int gm, int ngroups_, int G, int c, int U0) {
         groups = p.groups;
+        gemm = gm;
         ngroups = ngroups_;
-        MB0 = p.cls[0].MB;
-        KS0 = p.cls[0].KS;
-        MB1 = p.cls[1].MB;
-        KS1 = p.cls[1].KS;
+        MB0 = p.cls[gm][0].MB;
+        KS0 = p.cls[gm][0].KS;
+        MB1 = p.cls[gm][1].MB;
+        KS1 = p.cls[gm][1].KS;
         M = p.M;
         ktop = p.k;
         T_r = (long long)ngroups * MB0 * KS0;
-        T = steps_before(p, ngroups, U0);
+        T = steps_before(p, gm, ngroups, U0);
         t = t1 = 0;
         if (c >= G || T == 0) return;
         t = (long long)c * T / G;
@@ -129,7 +131,7 @@ struct Walker {
     __device__ __forceinline__ bool next(WorkItem& w, int G, int c) {
         if (t >= t1) return false;
         const int KS = cls ? KS1 : KS0;
-        w.cls = cls;
+        w.cls = 2 * gemm + cls;
         w.b = b;
         w.rot = 0;
         w.ka = k;
@@ -192,18 +194,19 @@ struct Walker {
 // neighbouring chunks.
 struct DynList {
     int NRU, U, U0, Uh, Urt, Ust, P0, P1, Cu, Nh, R, Wh, W, G;
-    int MB0, KS0, KS1, M, ktop;
-    // The pool: units [U0_, U).
-    __device__ void init(const GemmParams& p, int ngroups, int G_, int U0_) {
+    int gemm, MB0, KS0, KS1, M, ktop;
+    // The pool of GEMM gm: units [U0_, U).
+    __device__ void init(const GemmParams& p, int gm, int ngroups, int G_, int U0_) {
         G = G_;
         U0 = U0_;
-        MB0 = p.cls[0].MB;
-        KS0 = p.cls[0].KS;
-        KS1 = p.cls[1].KS;
+        gemm = gm;
+        MB0 = p.cls[gm][0].MB;
+        KS0 = p.cls[gm][0].KS;
+        KS1 = p.cls[gm][1].KS;
         M = p.M;
         ktop = p.k;
         NRU = ngroups * MB0;
-        const int Ush = p.has_shared ? p.cls[1].MB : 0;
+        const int Ush = p.has_shared ? p.cls[gm][1].MB : 0;
         U = NRU + Ush;
         const int Up = U - U0;
         const int Ut = Up < G ? Up : G;
@@ -254,7 +257,7 @@ struct DynList {
     __device__ __forceinline__ void item(int u, int pc, int P, int ti, int4 grp, WorkItem& it) const {
         const bool routed = u < NRU;
         const int KS = routed ? KS0 : KS1;
-        it.cls = routed ? 0 : 1;
+        it.cls = 2 * gemm + (routed ? 0 : 1);
         it.unit = u;
         if (routed) {
             const int g = u / MB0;
@@ -286,10 +289,22 @@ struct DynList {
     }
 };
 
+// One ring slot whose activation copies wait for the gate_up counter `dep` (both GEMMs in
+// one launch): sources, the slot's shared address and full barrier, bytes, its ring
+// position and its item's queue index.
+struct Deferred {
+    const uint8_t* b;
+    const uint8_t* s;
+    uint32_t stage, fb, bb, sb;
+    int pos, q, dep;
+};
+static_assert(sizeof(Deferred) * kMaxStages <= kDeferBytes, "deferred-copy list");
+
 struct GemmSmem {
     uint8_t* ring;
     float* stg;          // [Mpad][128] fp32 epilogue staging
     WorkItem* queue;     // [kGemmQueue]
+    Deferred* defer;     // [kMaxStages] producer only
     uint64_t* full;
     uint64_t* empty;
     uint64_t* acc_full;
@@ -315,6 +330,35 @@ __device__ __forceinline__ float warp_max_f(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
+}
+
+// Waits until *ctr >= target (acquire, bounded by kWaitLimitNs or the abort flag), then
+// orders this thread's later bulk copies (async proxy) after what the acquire made visible.
+__device__ __forceinline__ bool wait_at_least(const int32_t* ctr, int target, volatile int* abort) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+        if (v >= target) break;
+        if (i == 0) {
+            t0 = globaltimer();
+        } else if ((i & 15) == 0) {
+            if (*abort) return false;
+            if (globaltimer() - t0 > kWaitLimitNs) return false;
+        }
+        __nanosleep(128);
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
+}
+
+// One look at *ctr: true (with the same ordering as wait_at_least) when it is >= target.
+__device__ __forceinline__ bool poll_at_least(const int32_t* ctr, int target) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v < target) return false;
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
 }
 
 // Reads queue entry i, waiting until it is published; false on a timeout.
@@ -404,7 +448,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
     sm.ring = base;
     sm.stg = reinterpret_cast<float*>(base + (size_t)S * p.stage_bytes);
     sm.queue = reinterpret_cast<WorkItem*>(sm.stg + p.Mpad * kBlockRows);
-    sm.full = reinterpret_cast<uint64_t*>(sm.queue + kGemmQueue);
+    sm.defer = reinterpret_cast<Deferred*>(sm.queue + kGemmQueue);
+    sm.full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sm.defer) + kDeferBytes);
     sm.empty = sm.full + S;
     sm.acc_full = sm.empty + S;
     sm.acc_empty = sm.acc_full + kMaxAcc;
@@ -444,7 +489,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
     // share of them into L2. They are consumed at the end of the item list; the routed
     // weights streamed meanwhile carry an evict-first hint.
     if (threadIdx.x == 32 && p.has_shared) {
-        const GemmClass& C1 = p.cls[1];
+        const GemmClass& C1 = p.cls[p.mode == 1 ? 1 : 0][1];
         const size_t total = (size_t)C1.MB * C1.KS * record_bytes(C1.fmt);
         const size_t share = (total / gridDim.x + 15) & ~(size_t)15;
         const size_t b0 = (size_t)blockIdx.x * share;
@@ -470,14 +515,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
     pdl_trigger();
 
     const int ngroups = p.hdr->num_groups;
-    const int U_all = ngroups * p.cls[0].MB + (p.has_shared ? p.cls[1].MB : 0);
-    const int U_pool = p.pool_units < 0 || p.pool_units > U_all ? U_all : p.pool_units;
-    const int U0 = U_all - U_pool;  // units [0, U0) in static ranges, [U0, U_all) in the pool
-    const bool dyn = U_pool > 0;
-    const long long T_st = Walker::steps_before(p, ngroups, U0);
-    // static part: never more CTAs than steps, so every working CTA owns at least one step
-    // and the CTAs whose ranges meet a unit are exactly its pieces
-    const int G = (int)((long long)gridDim.x < T_st ? (long long)gridDim.x : T_st), c = blockIdx.x;
+    // the GEMMs of this launch: gate_up (0), down (1) or both, gate_up's items first
+    const int g_first = p.mode == 1 ? 1 : 0, g_last = p.mode == 0 ? 0 : 1;
+    auto units_of = [&](int gm) { return ngroups * p.cls[gm][0].MB + (p.has_shared ? p.cls[gm][1].MB : 0); };
+    // units at the end of the list handed out from the counter (single-GEMM launches only)
+    auto pool_of = [&](int gm) {
+        const int Ua = units_of(gm);
+        return p.mode == 2 ? 0 : (p.pool_units < 0 || p.pool_units > Ua ? Ua : p.pool_units);
+    };
+    const bool dyn = pool_of(g_first) > 0;
+    const int c = blockIdx.x;
     volatile int* abort_flag = sm.abort_flag;
 
     if (warp == 0) {
@@ -488,26 +535,62 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             uint32_t issued_mask = 0;  // stages with a copy in flight at least once
             bool ok = true;
             int qn = 0;  // items published
-            // Publishes one item and issues its copies (plus the bubble after an odd count).
-            auto issue = [&](const WorkItem& it) -> bool {
+            // Both GEMMs in one launch: a down item reads its group's hidden activations,
+            // written by the gate_up epilogues of any CTA. Its weight copies go out at once;
+            // its activation copies wait here, in ring order, until the group's gate_up
+            // counter is complete. So the ring fills with down weights while the last
+            // gate_up units finish. A deferred slot is issued before anything could wait on
+            // it: before its ring slot comes round again, and before its item's queue entry
+            // is needed again.
+            Deferred* dq = sm.defer;
+            int dh = 0, dt = 0;  // deferred slots issued / recorded
+            int pos = 0;         // ring slots filled so far (bubbles included)
+            int met = -1;        // group counter known to be complete (gu_done index)
+            auto dep_target = [&](int d) { return p.cls[0][d == kMaxE ? 1 : 0].MB; };
+            auto issue_b = [&](const Deferred& e) {
+                bulk_g2s(e.stage + p.b_off, e.b, e.bb, e.fb);
+                if (e.sb) bulk_g2s(e.stage + p.sfb_off, e.s, e.sb, e.fb);
+            };
+            // issues deferred slots from the front while their groups are complete; waits
+            // for the group of a slot at ring position <= pos_lim or of item <= q_lim
+            auto drain = [&](int pos_lim, int q_lim) -> bool {
+                while (dh < dt) {
+                    const Deferred& e = dq[dh % kMaxStages];
+                    if (e.dep != met) {
+                        if (e.pos <= pos_lim || e.q <= q_lim) {
+                            if (!wait_at_least(p.gu_done + e.dep, dep_target(e.dep), abort_flag)) return false;
+                        } else if (!poll_at_least(p.gu_done + e.dep, dep_target(e.dep))) {
+                            return true;
+                        }
+                        met = e.dep;
+                    }
+                    issue_b(e);
+                    ++dh;
+                }
+                return true;
+            };
+            // Publishes one item and issues its copies (plus the bubble after an odd count);
+            // dep >= 0: the gu_done counter the item's activations wait for.
+            auto issue = [&](const WorkItem& it, int dep) -> bool {
                 const int qi = qn % kGemmQueue;
+                if (dh < dt && !drain(INT_MIN, qn - kGemmQueue)) return false;
                 if (!mbar_wait_bounded(smem_u32(&sm.q_empty[qi]), ((uint32_t)(qn / kGemmQueue) & 1u) ^ 1u, abort_flag,
                                        kWaitLimitNs))
                     return false;
                 sm.queue[qi] = it;
                 mbar_arrive(smem_u32(&sm.q_full[qi]));
                 ++qn;
-                const GemmClass& C = p.cls[it.cls];
+                const GemmClass& C = p.cls[it.cls >> 1][it.cls & 1];
                 const int A = atoms_per_step(C.fmt);
                 const uint32_t REC = record_bytes(C.fmt);
                 int Rpad;
                 const uint8_t *bsrc, *bssrc;
-                if (p.mode == 0) {
+                if ((it.cls >> 1) == 0) {  // gate_up: all rows of x
                     Rpad = p.Mpad;
                     bsrc = C.b;
                     bssrc = C.bs;
-                } else {
-                    Rpad = (it.cls == 0) ? round_up(it.rows, 16) : p.Mpad;
+                } else {  // down: the group's rows of the hidden activations
+                    Rpad = ((it.cls & 1) == 0) ? round_up(it.rows, 16) : p.Mpad;
                     bsrc = C.b + (size_t)it.row_off * C.KS * kStepBytes;
                     bssrc = C.bs + (size_t)it.gidx * C.KS * A * kAtomBytes;
                 }
@@ -515,8 +598,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                 const uint32_t bbytes = (uint32_t)Rpad * kStepBytes;
                 const int nst = it.kb - it.ka;
                 int jr = it.rot;  // step of the item at position j
-                for (int j = 0; j < nst + (nst & 1); ++j, rg.adv1()) {
+                for (int j = 0; j < nst + (nst & 1); ++j, rg.adv1(), ++pos) {
                     const int st = rg.st;
+                    if (dh < dt && !drain(pos - S, INT_MIN)) return false;
                     if (!mbar_wait_bounded(smem_u32(&sm.empty[st]), rg.ph ^ 1u, abort_flag, kWaitLimitNs))
                         return false;
                     const uint32_t fb = smem_u32(&sm.full[st]);
@@ -527,23 +611,50 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                     }
                     const int kk = it.ka + jr;
                     if (++jr == nst) jr = 0;
-                    uint8_t* stage = sm.ring + (size_t)st * p.stage_bytes;
+                    const uint32_t stage = smem_u32(sm.ring + (size_t)st * p.stage_bytes);
                     mbar_arrive_expect_tx(fb, REC + bbytes + (uint32_t)A * kAtomBytes);
-                    bulk_g2s_hint(smem_u32(stage + p.a_off), wrec0 + (size_t)(kk - it.ka) * REC, REC, fb, pol);
-                    bulk_g2s(smem_u32(stage + p.b_off), bsrc + (size_t)kk * bbytes, bbytes, fb);
-                    if (A) bulk_g2s(smem_u32(stage + p.sfb_off), bssrc + (size_t)kk * A * kAtomBytes, A * kAtomBytes, fb);
+                    bulk_g2s_hint(stage + p.a_off, wrec0 + (size_t)(kk - it.ka) * REC, REC, fb, pol);
+                    const Deferred e{bsrc + (size_t)kk * bbytes, bssrc + (size_t)kk * A * kAtomBytes, stage, fb, bbytes,
+                                     (uint32_t)A * kAtomBytes, pos, qn - 1, dep};
+                    if (dep < 0 || dep == met) {
+                        issue_b(e);
+                    } else if (dh == dt && poll_at_least(p.gu_done + dep, dep_target(dep))) {
+                        met = dep;
+                        issue_b(e);
+                    } else {
+                        dq[dt % kMaxStages] = e;
+                        ++dt;
+                    }
                 }
                 return true;
             };
             WorkItem it;
+            for (int gm = g_first; ok && gm <= g_last; ++gm) {
+            if (gm == 1 && p.mode == 2 && p.has_shared) {
+                // as the down launch does before its wait: this CTA's share of the down
+                // GEMM's shared-expert weights into L2 while the gate_up units finish
+                const GemmClass& C1 = p.cls[1][1];
+                const size_t total = (size_t)C1.MB * C1.KS * record_bytes(C1.fmt);
+                const size_t share = (total / gridDim.x + 15) & ~(size_t)15;
+                const size_t b0 = (size_t)blockIdx.x * share;
+                const size_t b1 = b0 + share < total ? b0 + share : total;
+                for (size_t o = b0; o < b1; o += 65536)
+                    prefetch_l2(C1.w + o, (uint32_t)(b1 - o < 65536 ? b1 - o : 65536));
+            }
+            const int Up = pool_of(gm), U0 = units_of(gm) - Up;  // [0, U0) static, [U0, U) pool
+            const long long Tst = Walker::steps_before(p, gm, ngroups, U0);
+            // static part: never more CTAs than steps, so every working CTA owns at least one
+            // step and the CTAs whose ranges meet a unit are exactly its pieces
+            const int G = (int)((long long)gridDim.x < Tst ? (long long)gridDim.x : Tst);
             {
                 Walker wk;
-                wk.init(p, ngroups, G, c, U0);
-                while (ok && wk.next(it, G, c)) ok = issue(it);
+                wk.init(p, gm, ngroups, G, c, U0);
+                while (ok && wk.next(it, G, c))
+                    ok = issue(it, (gm == 1 && p.mode == 2) ? ((it.cls & 1) ? kMaxE : it.gidx) : -1);
             }
-            if (ok && dyn) {
+            if (ok && Up > 0) {
                 DynList dl;
-                dl.init(p, ngroups, gridDim.x, U0);
+                dl.init(p, gm, ngroups, gridDim.x, U0);
                 // grab w0 in hand with the records of its first unit's group ga0 and ga0 + 1;
                 // w1 taken; w2 requested while w0's copies go out
                 auto preload = [&](int w, int& ga, int4& ra, int4& rb) {
@@ -576,7 +687,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                         int4 rec = r0a;
                         if (g >= 0 && g != ga0) rec = (g == ga0 + 1) ? r0b : ld_group(p.groups + g);
                         dl.item(u, pc, P, ti, rec, it);
-                        if (!issue(it)) {
+                        if (!issue(it, -1)) {
                             ok = false;
                             break;
                         }
@@ -588,6 +699,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                     r0b = r1b;
                 }
             }
+            }
+            if (ok && dh < dt) ok = drain(INT_MAX, INT_MAX);
             if (!ok) set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
             // the end marker
             if (ok) {
@@ -637,9 +750,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                 }
                 mbar_arrive(smem_u32(&sm.q_empty[qn % kGemmQueue]));
                 if (it.cls < 0) break;
-                const GemmClass& C = p.cls[it.cls];
-                const uint32_t N =
-                    (p.mode == 0) ? (uint32_t)p.Mpad : (uint32_t)((it.cls == 0) ? round_up(it.rows, 16) : p.Mpad);
+                const GemmClass& C = p.cls[it.cls >> 1][it.cls & 1];
+                const uint32_t N = (it.cls == 2) ? (uint32_t)round_up(it.rows, 16) : (uint32_t)p.Mpad;
                 if (!mbar_wait_bounded(smem_u32(&sm.acc_empty[ab]), ((acc_ph >> ab) & 1u) ^ 1u, abort_flag,
                                        kWaitLimitNs)) {
                     set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
@@ -720,7 +832,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                 }
                 mbar_arrive(smem_u32(&sm.q_empty[qn % kGemmQueue]));
                 if (it.cls < 0) break;
-                const int A = atoms_per_step(p.cls[it.cls].fmt);
+                const int A = atoms_per_step(p.cls[it.cls >> 1][it.cls & 1].fmt);
                 const int a1 = A < a0 + 2 ? A : a0 + 2;
                 const int nst = it.kb - it.ka;
                 for (int s = 0; s < nst + (nst & 1); ++s, rg.adv1()) {
@@ -774,9 +886,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sm.q_empty[qi]));
             if (it.cls < 0) break;
-            const GemmClass& C = p.cls[it.cls];
+            const int gm = it.cls >> 1, cl = it.cls & 1;  // GEMM (0 gate_up, 1 down), class
+            const GemmClass& C = p.cls[gm][cl];
             const int expert = it.expert, rows = it.rows, perm_off = it.perm_off, row_off = it.row_off, gidx = it.gidx;
-            const int N = (p.mode == 0) ? p.Mpad : ((it.cls == 0) ? round_up(rows, 16) : p.Mpad);
+            const int N = (it.cls == 2) ? round_up(rows, 16) : p.Mpad;
             acc_ph ^= 1u << ab;
             tc_fence_after();
             // bank b holds the item's steps j with j % 2 == b; a single-step item wrote bank
@@ -805,7 +918,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             if (++ab == nacc) ab = 0;
             // compact the selected columns: column of group row rg -> stg[rg][r]; the
             // group's tokens are read once (in parallel) into shared memory
-            if (p.mode == 0 && it.cls == 0) {
+            if (it.cls == 0) {
                 if (et < rows) sm.tok[et] = p.perm[perm_off + et] / p.k;
                 named_bar(1, 128);
                 for (int rg = 0; rg < rows; ++rg) {
@@ -817,12 +930,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             // last piece adds them all, in piece order
             if (it.np > 1) {
                 const int npieces = it.np;
-                float* part = p.partials + (size_t)it.myslot * kPartialFloats;
+                float* part = p.partials[gm] + (size_t)it.myslot * kPartialFloats;
                 for (int rg = 0; rg < rows; ++rg) __stcg(part + rg * kBlockRows + r, stg[rg * kBlockRows + r]);
                 __threadfence();
                 named_bar(1, 128);
                 if (et == 0) {
-                    const int old = atomicAdd(p.counters + it.unit, 1);
+                    const int old = atomicAdd(p.counters[gm] + it.unit, 1);
                     *sm.bcast = (old == npieces - 1) ? 1 : 0;
                 }
                 named_bar(1, 128);
@@ -842,7 +955,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                         for (int qq = 0; qq < 4; ++qq) {
                             const int pc = min(pc0 + qq, npieces - 1);
                             const int slot = pc == 0 ? it.s0 : it.sb + pc * it.sstride;
-                            const float* src = p.partials + (size_t)slot * kPartialFloats + r;
+                            const float* src = p.partials[gm] + (size_t)slot * kPartialFloats + r;
 #pragma unroll
                             for (int i = 0; i < 8; ++i) v[qq][i] = __ldcg(src + min(rg0 + i, rows - 1) * kBlockRows);
                         }
@@ -856,20 +969,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                     for (int i = 0; i < 8; ++i)
                         if (rg0 + i < rows) stg[(rg0 + i) * kBlockRows + r] = sum[i];
                 }
-                if (et == 0) p.counters[it.unit] = 0;
+                if (et == 0) p.counters[gm][it.unit] = 0;
             }
             named_bar(1, 128);
             // ---- final epilogue
             const float alpha = C.gs_w ? C.gs_w[expert] * C.gs_a : 1.0f;
-            if (p.mode == 0) {
+            if (gm == 0) {
                 // SwiGLU on (gate, up) = rows (fi, fi + 64); warps take 32 features each
                 const int fi = 32 * (ew & 1) + lane;
                 const int f = 64 * it.b + fi;  // feature in [0, I)
-                const int Rp = (it.cls == 0) ? round_up(rows, 16) : p.Mpad;
-                uint8_t* hq_g = C.hq + (it.cls == 0 ? (size_t)row_off * row_bytes(C.out_fmt, C.I) : 0);
+                const int Rp = (cl == 0) ? round_up(rows, 16) : p.Mpad;
+                uint8_t* hq_g = C.hq + (cl == 0 ? (size_t)row_off * row_bytes(C.out_fmt, C.I) : 0);
                 const int Aout = atoms_per_step(C.out_fmt);
                 const int KSo = steps_of(C.out_fmt, C.I);
-                uint8_t* hs_g = C.hs + (it.cls == 0 ? (size_t)gidx * KSo * Aout * kAtomBytes : 0);
+                uint8_t* hs_g = C.hs + (cl == 0 ? (size_t)gidx * KSo * Aout * kAtomBytes : 0);
                 const float lim = p.swiglu_limit;
                 for (int rg = (ew >> 1); rg < rows; rg += 2) {
                     float g = stg[rg * kBlockRows + fi] * alpha;
@@ -959,12 +1072,38 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                     p.y[(size_t)pos * p.H + n] = stg[rg * kBlockRows + et] * alpha;
                 }
             }
+            if (p.mode == 2 && gm == 0) {
+                // the unit's hidden activations are complete: order the stores before the
+                // down items' bulk copies (async proxy) in other CTAs, then count the unit
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                named_bar(1, 128);
+                if (et == 0) {
+                    __threadfence();
+                    atomicAdd(p.gu_done + (cl ? kMaxE : gidx), 1);
+                }
+            }
         }
     }
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
+    }
+    // both GEMMs in one launch: the last CTA to finish resets the group counters
+    if (p.mode == 2) {
+        if (threadIdx.x == 0) {
+            __threadfence();
+            sm.bcast[0] = atomicAdd(p.gu_done + kMaxE + 1, 1) == (int)gridDim.x - 1 ? 1 : 0;
+        }
+        __syncthreads();
+        if (sm.bcast[0]) {
+            for (int i = threadIdx.x; i < ngroups; i += blockDim.x) p.gu_done[i] = 0;
+            if (threadIdx.x == 0) {
+                p.gu_done[kMaxE] = 0;
+                p.gu_done[kMaxE + 1] = 0;
+            }
+            __threadfence();
+        }
     }
     // pool: the last CTA to finish resets the item counter for the next launch
     if (dyn && threadIdx.x == 0) {

@@ -21,6 +21,8 @@ constexpr int kMaxPieces = 4;        // pieces of a unit cut in the dynamic pool
 constexpr int kPoolSlot0 = 2 * kMaxGemmCtas;  // static ranges: 2 slots per CTA; then the pool's
 constexpr int kPartialSlots = kPoolSlot0 + kMaxPieces * kMaxGemmCtas;
 constexpr int kGemmQueue = 16;       // work items in flight between a CTA's roles
+constexpr int kMaxStages = 16;       // ring slots of the GEMM pipeline
+constexpr int kDeferBytes = kMaxStages * 48;  // producer's deferred copies (shared memory)
 
 __host__ __device__ inline int round_up(int a, int b) { return (a + b - 1) / b * b; }
 
@@ -65,7 +67,7 @@ struct WsHeader {
 // Byte offsets of the workspace regions for a layer and a maximum row count.
 struct WsLayout {
     size_t header, groups, logits, scores, topk_idx, topk_w, counts, perm, inv_perm, tiles, num_tiles;
-    size_t xq, xs, xq_sh, xs_sh, hq, hs, y, cnt_gu, cnt_dn, partials, sched, rpart, rcnt, total;
+    size_t xq, xs, xq_sh, xs_sh, hq, hs, y, cnt_gu, cnt_dn, partials, sched, gu_done, rpart, rcnt, total;
     int max_rows, P_max, G_max, T_max, U_gu, U_dn;
     size_t hq_routed_bytes, hs_routed_bytes;  // shared group's data / scales start here
 };
@@ -115,17 +117,19 @@ struct GemmClass {            // one weight class: routed experts or the shared 
 };
 
 struct GemmParams {
-    int mode;                 // 0 gate_up, 1 down
+    int mode;                 // 0 gate_up, 1 down, 2 both in one launch (gate_up items first)
     int M, k, E, H, Mpad;
-    GemmClass cls[2];
+    GemmClass cls[2][2];      // [GEMM: 0 gate_up, 1 down][class: 0 routed, 1 shared]
     int has_shared;
     const int32_t* perm;
     const Group* groups;
     const WsHeader* hdr;
     float* y;                 // down output [P, H]
-    int32_t* counters;        // per unit: pieces finished (self-resetting)
-    float* partials;          // [kPartialSlots][kPartialFloats]
+    int32_t* counters[2];     // per GEMM, per unit: pieces finished (self-resetting)
+    float* partials[2];       // per GEMM: partial-sum slots (kPartialFloats each)
     int32_t* sched;           // [2]: next work item, CTAs finished (dynamic schedule, self-resetting)
+    int32_t* gu_done;         // mode 2: gate_up units finished per group ([kMaxE]: shared expert),
+                              // then CTAs finished at [kMaxE + 1] (self-resetting)
     int32_t* status;
     int stages, stage_bytes, a_off, sfa_off, b_off, sfb_off, atoms_max, sf_warps;
     int pool_units;           // units at the end of the list taken from the counter (-1: all)

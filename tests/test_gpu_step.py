@@ -195,3 +195,19 @@ def test_clamped_swiglu_full_size_sampled_rows():
     rows = [0, M - 1]
     ref = _oracle_rows(cfg, inp, rows)
     _check_rows(layer, inp, rows, out, res, oq, os_, ref)
+
+
+# moe_step runs gate_up and down as one launch (down items wait in the kernel for their
+# group's gate_up units); MOE_FUSED_FFN=0 gives the two separate launches. Both cut the
+# same units at the same steps, so the bytes must agree exactly.
+@pytest.mark.parametrize("name,M", [(n, m) for n in SMALL for m in (1, 23)] + [("full", 8)])
+def test_one_launch_ffn_equals_two_launches(name, M, monkeypatch):
+    cfg = synth.config("mxfp8_h7168_e256_k8_8rows") if name == "full" else SMALL[name]
+    inp, layer = make(cfg, seed=21 + M, M=M)
+    monkeypatch.setenv("MOE_FUSED_FFN", "0")
+    two = _run(layer, inp, M)
+    monkeypatch.delenv("MOE_FUSED_FFN")
+    one = _run(layer, inp, M)
+    assert torch.equal(one[0], two[0]) and torch.equal(one[1], two[1])
+    if one[2] is not None:
+        assert torch.equal(one[2], two[2]) and torch.equal(one[3], two[3])
