@@ -218,6 +218,19 @@ moe_status moe_expert_down(const moe_layer_desc* d, const moe_qweight* w2, const
                            const void* hq, const void* hq_scales, int M, float* y_pairs, void* ws,
                            moe_stream_t stream);
 
+/* a5 + a6 in one launch: the same bytes in hq, hq_scales and y_pairs as
+ * moe_expert_gate_up followed by moe_expert_down, with the arguments of both. A down unit
+ * starts as soon as every FC1 unit of its group is done (per-group counters in ws, which
+ * every launch leaves at zero), and its weight copies go out before that, so the FC2
+ * weights stream while the last FC1 units finish. The grid is one CTA per SM and relies on
+ * all of them being resident together; a wait that runs out (2 s) sets MOE_ERR_TIMEOUT in
+ * the status word and the launch returns. moe_step uses this call unless the environment
+ * sets MOE_FUSED_FFN=0. [README: moe and shared_ll rows] */
+moe_status moe_expert_ffn(const moe_layer_desc* d, const moe_qweight* w13, const moe_qweight* sh13,
+                          const moe_qweight* w2, const moe_qweight* sh2, const void* xq, const void* xq_scales,
+                          const void* xq_sh, const void* xq_sh_scales, const int32_t* perm, int M, void* hq,
+                          void* hq_scales, float* y_pairs, void* ws, moe_stream_t stream);
+
 /* a7. moe[m] = sum_j topk_w[m,j] * y_pairs[inv_perm[m*k+j]] (j ascending) + shared row;
  * residual (bf16 [M,H], in place) = bf16(residual + moe); out = bf16(residual *
  * rsqrt(mean(residual^2) + eps) * gamma); outq / outq_scales (optional) = MXFP8 of out,
@@ -226,8 +239,9 @@ moe_status moe_finalize_norm(const moe_layer_desc* d, const float* y_pairs, cons
                              const int32_t* inv_perm, int M, void* residual, const void* gamma, void* out,
                              void* outq, void* outq_scales, void* ws, moe_stream_t stream);
 
-/* a1..a7 in five launches chained with programmatic dependent launch; intermediates in
- * ws (see moe_ws_view). M in [1, 64]. Capture-safe. */
+/* a1..a7 in four launches chained with programmatic dependent launch (router, routing,
+ * moe_expert_ffn, finalize; five with MOE_FUSED_FFN=0, which runs FC1 and FC2 as two
+ * launches); intermediates in ws (see moe_ws_view). M in [1, 64]. Capture-safe. */
 moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void* ws, moe_stream_t stream);
 
 /* The router step (a1 + a2 + a3, as moe_router_topk) for callers that cannot give the

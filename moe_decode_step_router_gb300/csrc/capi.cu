@@ -195,17 +195,20 @@ moe_status dev_info(DevInfo** out) {
 // predecessor on the stream finishes; it waits in griddepcontrol.wait).
 template <typename Kern, typename Arg>
 moe_status launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st, const Arg& arg,
-                      const char* name) {
+                      const char* name, bool cooperative = false) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    // blocks that wait on one another: all of them resident at once, or no launch
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = cooperative ? 2 : 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, arg);
     if (e != cudaSuccess) return cuda_fail(e, name);
     return MOE_OK;
@@ -435,7 +438,8 @@ moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* w13
     if (grid > kMaxGemmCtas) grid = kMaxGemmCtas;
     return launch_pdl(k_expert_gemm, dim3(grid), dim3(kGemmThreads), smem, st, p,
                       mode == 0 ? "k_expert_gemm(gate_up) launch"
-                                : (mode == 1 ? "k_expert_gemm(down) launch" : "k_expert_gemm(gate_up+down) launch"));
+                                : (mode == 1 ? "k_expert_gemm(down) launch" : "k_expert_gemm(gate_up+down) launch"),
+                      mode == 2);
 }
 
 moe_status launch_finalize(const moe_layer_desc* d, const float* y, const float* topk_w, const int32_t* inv_perm,
@@ -486,6 +490,57 @@ moe_status check_qweight(const moe_qweight* w, int fmt, const char* name) {
 }  // namespace
 
 // ================================================================== C ABI
+namespace {
+
+// Arguments of the FC1 call (moe_expert_gate_up, and the first half of moe_expert_ffn).
+moe_status gate_up_buffers(const moe_layer_desc* d, const moe_qweight* w13, const moe_qweight* sh13, const void* xq,
+                           const void* xq_scales, const void* xq_sh, const void* xq_sh_scales, const int32_t* perm,
+                           int M, void* hq, void* hq_scales, void* ws, GemmBuffers& b) {
+    moe_status s = check_desc(d);
+    if (s != MOE_OK) return s;
+    REQUIRE(M >= 1 && M <= kMaxRows, "M=%d: need 1..%d", M, kMaxRows);
+    if ((s = check_qweight(w13, d->w_fmt, "w13")) != MOE_OK) return s;
+    if (d->has_shared && (s = check_qweight(sh13, d->shared_fmt, "sh13")) != MOE_OK) return s;
+    REQUIRE_PTR(xq, "xq");
+    REQUIRE_PTR(xq_scales, "xq_scales");
+    if (separate_shared_input(d)) {
+        REQUIRE_PTR(xq_sh, "xq_sh");
+        if (d->shared_fmt != MOE_FMT_BF16) REQUIRE_PTR(xq_sh_scales, "xq_sh_scales");
+    }
+    REQUIRE_PTR(perm, "perm");
+    REQUIRE_PTR(hq, "hq");
+    REQUIRE_PTR(hq_scales, "hq_scales");
+    REQUIRE_PTR(ws, "ws");
+    b.xq = xq;
+    b.xs = xq_scales;
+    b.xq_sh = separate_shared_input(d) ? xq_sh : xq;
+    b.xs_sh = separate_shared_input(d) ? xq_sh_scales : xq_scales;
+    b.hq = hq;
+    b.hs = hq_scales;
+    b.perm = perm;
+    return MOE_OK;
+}
+
+// Arguments of the FC2 call (moe_expert_down, and the second half of moe_expert_ffn).
+moe_status down_buffers(const moe_layer_desc* d, const moe_qweight* w2, const moe_qweight* sh2, const void* hq,
+                        const void* hq_scales, int M, float* y_pairs, void* ws, GemmBuffers& b) {
+    moe_status s = check_desc(d);
+    if (s != MOE_OK) return s;
+    REQUIRE(M >= 1 && M <= kMaxRows, "M=%d: need 1..%d", M, kMaxRows);
+    if ((s = check_qweight(w2, d->w_fmt, "w2")) != MOE_OK) return s;
+    if (d->has_shared && (s = check_qweight(sh2, d->shared_fmt, "sh2")) != MOE_OK) return s;
+    REQUIRE_PTR(hq, "hq");
+    REQUIRE_PTR(hq_scales, "hq_scales");
+    REQUIRE_PTR(y_pairs, "y_pairs");
+    REQUIRE_PTR(ws, "ws");
+    b.hq = const_cast<void*>(hq);
+    b.hs = const_cast<void*>(hq_scales);
+    b.y = y_pairs;
+    return MOE_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* moe_last_error_string(void) { return g_err.c_str(); }
@@ -651,52 +706,35 @@ moe_status moe_expert_gate_up(const moe_layer_desc* d, const moe_qweight* w13, c
                               const void* xq, const void* xq_scales, const void* xq_sh, const void* xq_sh_scales,
                               const int32_t* perm, int M, void* hq, void* hq_scales, void* ws,
                               moe_stream_t stream) {
-    moe_status s = check_desc(d);
-    if (s != MOE_OK) return s;
-    REQUIRE(M >= 1 && M <= kMaxRows, "M=%d: need 1..%d", M, kMaxRows);
-    if ((s = check_qweight(w13, d->w_fmt, "w13")) != MOE_OK) return s;
-    if (d->has_shared && (s = check_qweight(sh13, d->shared_fmt, "sh13")) != MOE_OK) return s;
-    REQUIRE_PTR(xq, "xq");
-    REQUIRE_PTR(xq_scales, "xq_scales");
-    if (separate_shared_input(d)) {
-        REQUIRE_PTR(xq_sh, "xq_sh");
-        if (d->shared_fmt != MOE_FMT_BF16) REQUIRE_PTR(xq_sh_scales, "xq_sh_scales");
-    }
-    REQUIRE_PTR(perm, "perm");
-    REQUIRE_PTR(hq, "hq");
-    REQUIRE_PTR(hq_scales, "hq_scales");
-    REQUIRE_PTR(ws, "ws");
-    const WsLayout L = layout(d);
     GemmBuffers b{};
-    b.xq = xq;
-    b.xs = xq_scales;
-    b.xq_sh = separate_shared_input(d) ? xq_sh : xq;
-    b.xs_sh = separate_shared_input(d) ? xq_sh_scales : xq_scales;
-    b.hq = hq;
-    b.hs = hq_scales;
-    b.perm = perm;
-    s = launch_gemm(0, d, w13, sh13, nullptr, nullptr, b, M, L, static_cast<uint8_t*>(ws), (cudaStream_t)stream);
+    moe_status s = gate_up_buffers(d, w13, sh13, xq, xq_scales, xq_sh, xq_sh_scales, perm, M, hq, hq_scales, ws, b);
+    if (s != MOE_OK) return s;
+    s = launch_gemm(0, d, w13, sh13, nullptr, nullptr, b, M, layout(d), static_cast<uint8_t*>(ws),
+                    (cudaStream_t)stream);
     if (s != MOE_OK) return s;
     return ok();
 }
 
 moe_status moe_expert_down(const moe_layer_desc* d, const moe_qweight* w2, const moe_qweight* sh2, const void* hq,
                            const void* hq_scales, int M, float* y_pairs, void* ws, moe_stream_t stream) {
-    moe_status s = check_desc(d);
-    if (s != MOE_OK) return s;
-    REQUIRE(M >= 1 && M <= kMaxRows, "M=%d: need 1..%d", M, kMaxRows);
-    if ((s = check_qweight(w2, d->w_fmt, "w2")) != MOE_OK) return s;
-    if (d->has_shared && (s = check_qweight(sh2, d->shared_fmt, "sh2")) != MOE_OK) return s;
-    REQUIRE_PTR(hq, "hq");
-    REQUIRE_PTR(hq_scales, "hq_scales");
-    REQUIRE_PTR(y_pairs, "y_pairs");
-    REQUIRE_PTR(ws, "ws");
-    const WsLayout L = layout(d);
     GemmBuffers b{};
-    b.hq = const_cast<void*>(hq);
-    b.hs = const_cast<void*>(hq_scales);
-    b.y = y_pairs;
-    s = launch_gemm(1, d, nullptr, nullptr, w2, sh2, b, M, L, static_cast<uint8_t*>(ws), (cudaStream_t)stream);
+    moe_status s = down_buffers(d, w2, sh2, hq, hq_scales, M, y_pairs, ws, b);
+    if (s != MOE_OK) return s;
+    s = launch_gemm(1, d, nullptr, nullptr, w2, sh2, b, M, layout(d), static_cast<uint8_t*>(ws),
+                    (cudaStream_t)stream);
+    if (s != MOE_OK) return s;
+    return ok();
+}
+
+moe_status moe_expert_ffn(const moe_layer_desc* d, const moe_qweight* w13, const moe_qweight* sh13,
+                          const moe_qweight* w2, const moe_qweight* sh2, const void* xq, const void* xq_scales,
+                          const void* xq_sh, const void* xq_sh_scales, const int32_t* perm, int M, void* hq,
+                          void* hq_scales, float* y_pairs, void* ws, moe_stream_t stream) {
+    GemmBuffers b{};
+    moe_status s = gate_up_buffers(d, w13, sh13, xq, xq_scales, xq_sh, xq_sh_scales, perm, M, hq, hq_scales, ws, b);
+    if (s != MOE_OK) return s;
+    if ((s = down_buffers(d, w2, sh2, hq, hq_scales, M, y_pairs, ws, b)) != MOE_OK) return s;
+    s = launch_gemm(2, d, w13, sh13, w2, sh2, b, M, layout(d), static_cast<uint8_t*>(ws), (cudaStream_t)stream);
     if (s != MOE_OK) return s;
     return ok();
 }

@@ -22,7 +22,8 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 # Every symbol the header declares.
 EXPORTS = ("moe_last_error_string", "moe_packed_bytes", "moe_act_bytes", "moe_act_scale_bytes", "moe_hq_bytes",
            "moe_hq_scale_bytes", "moe_workspace_bytes", "moe_workspace_init", "moe_ws_view", "moe_pack_weights",
-           "moe_router_topk", "moe_route_tiles", "moe_expert_gate_up", "moe_expert_down", "moe_finalize_norm",
+           "moe_router_topk", "moe_route_tiles", "moe_expert_gate_up", "moe_expert_down", "moe_expert_ffn",
+           "moe_finalize_norm",
            "moe_step", "moe_get_status", "moe_router_topk_noalloc")
 
 
@@ -88,6 +89,8 @@ def lib():
             "moe_expert_gate_up": (I32, [D, ctypes.POINTER(QWeight), ctypes.POINTER(QWeight), P, P, P, P, P, I32,
                                          P, P, P, P]),
             "moe_expert_down": (I32, [D, ctypes.POINTER(QWeight), ctypes.POINTER(QWeight), P, P, I32, P, P, P]),
+            "moe_expert_ffn": (I32, [D, ctypes.POINTER(QWeight), ctypes.POINTER(QWeight), ctypes.POINTER(QWeight),
+                                     ctypes.POINTER(QWeight), P, P, P, P, P, I32, P, P, P, P, P]),
             "moe_finalize_norm": (I32, [D, P, P, P, I32, P, P, P, P, P, P, P]),
             "moe_step": (I32, [D, ctypes.POINTER(StepArgs), I32, P, P]),
             "moe_get_status": (I32, [P, P, ctypes.POINTER(ctypes.c_int)]),
@@ -202,6 +205,13 @@ def moe_expert_gate_up(d, w13, sh13, xq, xq_scales, xq_sh, xq_sh_scales, perm, M
 def moe_expert_down(d, w2, sh2, hq, hq_scales, M, y_pairs, ws, stream=None):
     _check(lib().moe_expert_down(ctypes.byref(d), ctypes.byref(w2), ctypes.byref(sh2), _ptr(hq), _ptr(hq_scales),
                                  M, _ptr(y_pairs), _ptr(ws), _stream(stream)))
+
+
+def moe_expert_ffn(d, w13, sh13, w2, sh2, xq, xq_scales, xq_sh, xq_sh_scales, perm, M, hq, hq_scales, y_pairs, ws,
+                   stream=None):
+    _check(lib().moe_expert_ffn(ctypes.byref(d), ctypes.byref(w13), ctypes.byref(sh13), ctypes.byref(w2),
+                                ctypes.byref(sh2), _ptr(xq), _ptr(xq_scales), _ptr(xq_sh), _ptr(xq_sh_scales),
+                                _ptr(perm), M, _ptr(hq), _ptr(hq_scales), _ptr(y_pairs), _ptr(ws), _stream(stream)))
 
 
 def moe_finalize_norm(d, y_pairs, topk_w, inv_perm, M, residual, gamma, out, outq, outq_scales, ws, stream=None):

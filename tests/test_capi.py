@@ -82,5 +82,11 @@ def test_bad_rows_and_pointers_rejected_before_launch(lib):
     st = lib.moe_expert_gate_up(ctypes.byref(nv), ctypes.byref(q), ctypes.byref(q), fake, fake, fake, None, fake, 4,
                                 fake, fake, fake, None)
     assert st == ms.MOE_ERR_INVALID_ARG and "global_scale" in lib.moe_last_error_string().decode()
+    st = lib.moe_expert_ffn(ctypes.byref(nv), ctypes.byref(q), ctypes.byref(q), ctypes.byref(q), ctypes.byref(q),
+                            fake, fake, fake, None, fake, 4, fake, fake, fake, fake, None)
+    assert st == ms.MOE_ERR_INVALID_ARG and "global_scale" in lib.moe_last_error_string().decode()
+    st = lib.moe_expert_ffn(ctypes.byref(d), ctypes.byref(q), ctypes.byref(q), ctypes.byref(q), ctypes.byref(q),
+                            fake, fake, fake, None, fake, 4, fake, fake, None, fake, None)
+    assert st == ms.MOE_ERR_INVALID_ARG and "y_pairs" in lib.moe_last_error_string().decode()
     with pytest.raises(ms.MoeError):
         ms._check(ms.MOE_ERR_INVALID_ARG)

@@ -188,6 +188,13 @@ def test_stages_against_oracle(name, M):
     y = npy(t["y"])
     for p, yr in ref_y.items():
         assert rel_l2(y[inv[p]], yr) < (3e-2 if fr in (2, 3) else 1e-2), (p, rel_l2(y[inv[p]], yr))
+    # ---- a5 + a6 in one launch: the same bytes as the two calls
+    hq1, hs1, y1 = torch.zeros_like(t["hq"]), torch.zeros_like(t["hs"]), torch.zeros_like(t["y"])
+    ms.moe_expert_ffn(d, layer.qw["w13"], layer.qw["sh13"], layer.qw["w2"], layer.qw["sh2"], t["xq"], t["xs"], xq_sh,
+                      xs_sh, t["perm"], M, hq1, hs1, y1, layer.ws)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    assert torch.equal(hq1, t["hq"]) and torch.equal(hs1, t["hs"]) and torch.equal(y1, t["y"])
     # ---- a7 finalize, and the whole step against the oracle's own step
     res = inp["residual"].clone()
     ms.moe_finalize_norm(d, t["y"], t["w"], t["inv"], M, res, inp["gamma"], t["out"], None, None, layer.ws)
