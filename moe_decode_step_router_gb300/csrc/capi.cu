@@ -156,6 +156,7 @@ WsLayout layout(const moe_layer_desc* d) {
     L.gu_done = take(4ull * (kMaxE + 2));  // one launch for both GEMMs: per-group gate_up units done
     L.rpart = take(4ull * ((d->H + 511) / 512) * d->E * kMaxRows);
     L.rcnt = take(4ull * ((d->E + 7) / 8));
+    L.tcnt = take(16);
     L.total = o;
     return L;
 }
@@ -217,8 +218,10 @@ moe_status launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_
 // ------------------------------------------------------------------ launch helpers
 moe_status launch_router(const moe_layer_desc* d, const WsLayout& L, uint8_t* ws, const void* x,
                          const void* w_gate, const float* logits_in, int M, float* logits_out, float* scores,
-                         cudaStream_t st) {
+                         cudaStream_t st, const void* l2_pf = nullptr, size_t l2_pf_bytes = 0) {
     RouterParams p{};
+    p.l2_pf = static_cast<const uint8_t*>(l2_pf);
+    p.l2_pf_bytes = l2_pf_bytes;
     p.x = static_cast<const uint16_t*>(x);
     p.wg = static_cast<const uint16_t*>(w_gate);
     p.logits_in = logits_in;
@@ -280,6 +283,9 @@ moe_status launch_topk_route(const moe_layer_desc* d, const WsLayout& L, uint8_t
     p.num_tiles = num_tiles;
     p.groups = reinterpret_cast<Group*>(ws + L.groups);
     p.hdr = reinterpret_cast<WsHeader*>(ws + L.header);
+    // one row per warp: ceil(M / 16) CTAs of 16 warps take the top-k
+    p.topk_ctas = do_topk ? (M + kRouteThreads / 32 - 1) / (kRouteThreads / 32) : 1;
+    p.topk_arrivals = (p.topk_ctas > 1 && do_route) ? reinterpret_cast<int32_t*>(ws + L.tcnt) : nullptr;
     int qctas = 0;
     if (qa.x) {
         p.x = static_cast<const uint16_t*>(qa.x);
@@ -297,7 +303,8 @@ moe_status launch_topk_route(const moe_layer_desc* d, const WsLayout& L, uint8_t
         if (p.quant_shared && quant_units_host(p.fmt_s, M, d->H) > units) units = quant_units_host(p.fmt_s, M, d->H);
         qctas = (units + 511) / 512;
     }
-    return launch_pdl(k_topk_route, dim3(1 + qctas), dim3(512), 0, st, p, "k_topk_route launch");
+    return launch_pdl(k_topk_route, dim3(p.topk_ctas + qctas), dim3(kRouteThreads), 0, st, p,
+                      "k_topk_route launch");
 }
 
 struct GemmBuffers {
@@ -375,7 +382,7 @@ void gemm_classes(int g, const moe_layer_desc* d, const moe_qweight* wr, const m
 // waits in the kernel until its group's gate_up units are done).
 moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* w13, const moe_qweight* sh13,
                        const moe_qweight* w2, const moe_qweight* sh2, const GemmBuffers& b, int M, const WsLayout& L,
-                       uint8_t* ws, cudaStream_t st) {
+                       uint8_t* ws, cudaStream_t st, bool prefetch_shared = true) {
     DevInfo* di;
     moe_status s = dev_info(&di);
     if (s != MOE_OK) return s;
@@ -400,6 +407,7 @@ moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* w13
     p.sched = reinterpret_cast<int32_t*>(ws + L.sched) + 2 * (mode == 1 ? 1 : 0);
     p.gu_done = reinterpret_cast<int32_t*>(ws + L.gu_done);
     p.swiglu_limit = d->swiglu_limit > 0.0f ? d->swiglu_limit : 0.0f;
+    p.prefetch_shared = prefetch_shared ? 1 : 0;
     p.pool_units = mode == 2 ? 0 : gemm_pool_units(di->sms < kMaxGemmCtas ? di->sms : kMaxGemmCtas);
     p.status = reinterpret_cast<int32_t*>(ws + L.header);
     if (mode != 1) gemm_classes(0, d, w13, sh13, b, M, p.cls[0]);
@@ -792,7 +800,13 @@ moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void
     float* topk_w = reinterpret_cast<float*>(w + L.topk_w);
     int32_t* perm = reinterpret_cast<int32_t*>(w + L.perm);
     int32_t* inv_perm = reinterpret_cast<int32_t*>(w + L.inv_perm);
-    s = launch_router(d, L, w, a->x, a->w_gate, nullptr, M, logits, scores, st);
+    // the shared expert's gate_up records do not depend on the routing: the router launch
+    // prefetches them into L2 while the front end runs (the GEMM launch then does not)
+    const size_t sh13_bytes = d->has_shared ? (size_t)(2 * d->I_shared / kBlockRows) *
+                                                  steps_of(d->shared_fmt, d->H) * record_bytes(d->shared_fmt)
+                                            : 0;
+    s = launch_router(d, L, w, a->x, a->w_gate, nullptr, M, logits, scores, st,
+                      d->has_shared ? a->sh13.packed : nullptr, sh13_bytes);
     if (s != MOE_OK) return s;
     QuantArgs qa;
     qa.x = a->x;
@@ -814,10 +828,10 @@ moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void
     b.y = reinterpret_cast<float*>(w + L.y);
     b.perm = perm;
     if (step_fuses_ffn()) {
-        s = launch_gemm(2, d, &a->w13, &a->sh13, &a->w2, &a->sh2, b, M, L, w, st);
+        s = launch_gemm(2, d, &a->w13, &a->sh13, &a->w2, &a->sh2, b, M, L, w, st, false);
         if (s != MOE_OK) return s;
     } else {
-        s = launch_gemm(0, d, &a->w13, &a->sh13, nullptr, nullptr, b, M, L, w, st);
+        s = launch_gemm(0, d, &a->w13, &a->sh13, nullptr, nullptr, b, M, L, w, st, false);
         if (s != MOE_OK) return s;
         s = launch_gemm(1, d, nullptr, nullptr, &a->w2, &a->sh2, b, M, L, w, st);
         if (s != MOE_OK) return s;

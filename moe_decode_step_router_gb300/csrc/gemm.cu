@@ -488,7 +488,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
     // of the step still run (HBM is otherwise idle then), every CTA prefetches its 1/G
     // share of them into L2. They are consumed at the end of the item list; the routed
     // weights streamed meanwhile carry an evict-first hint.
-    if (threadIdx.x == 32 && p.has_shared) {
+    if (threadIdx.x == 32 && p.has_shared && p.prefetch_shared) {
         const GemmClass& C1 = p.cls[p.mode == 1 ? 1 : 0][1];
         const size_t total = (size_t)C1.MB * C1.KS * record_bytes(C1.fmt);
         const size_t share = (total / gridDim.x + 15) & ~(size_t)15;

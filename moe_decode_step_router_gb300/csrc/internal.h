@@ -67,7 +67,7 @@ struct WsHeader {
 // Byte offsets of the workspace regions for a layer and a maximum row count.
 struct WsLayout {
     size_t header, groups, logits, scores, topk_idx, topk_w, counts, perm, inv_perm, tiles, num_tiles;
-    size_t xq, xs, xq_sh, xs_sh, hq, hs, y, cnt_gu, cnt_dn, partials, sched, gu_done, rpart, rcnt, total;
+    size_t xq, xs, xq_sh, xs_sh, hq, hs, y, cnt_gu, cnt_dn, partials, sched, gu_done, rpart, rcnt, tcnt, total;
     int max_rows, P_max, G_max, T_max, U_gu, U_dn;
     size_t hq_routed_bytes, hs_routed_bytes;  // shared group's data / scales start here
 };
@@ -82,7 +82,11 @@ struct RouterParams {
     int M, H, E;
     float* part;              // [H/512][E][64] partial logits (workspace)
     int32_t* counters;        // [ceil(E/8)] arrivals per expert block (self-resetting)
+    const uint8_t* l2_pf;     // bytes a later launch streams that do not depend on this one
+    size_t l2_pf_bytes;       // (the shared expert's gate_up records): prefetched into L2
 };
+
+constexpr int kRouteThreads = 512;  // k_topk_route: 16 warps, one row each
 
 struct TopkRouteParams {
     const float* scores;      // [M, E] (topk stage)
@@ -90,11 +94,13 @@ struct TopkRouteParams {
     int32_t* topk_idx;        // [M, k]
     float* topk_w;            // [M, k]
     int M, E, k, renormalize, has_shared, do_topk, do_route;
+    int topk_ctas;            // CTAs 0..topk_ctas-1 take the rows (one per warp); the last to finish routes
+    int32_t* topk_arrivals;   // their arrival counter (self-resetting; used when topk_ctas > 1 and routing)
     float rsf;
     int32_t *counts, *perm, *inv_perm, *tiles, *num_tiles;
     Group* groups;
     WsHeader* hdr;
-    // FC1 input quantisation into the tiled layout (CTAs 1.. of the launch)
+    // FC1 input quantisation into the tiled layout (CTAs topk_ctas.. of the launch)
     const uint16_t* x;        // bf16 [M, H]
     int H, fmt_r, fmt_s, quant_shared;
     uint8_t *xq, *xs, *xq_sh, *xs_sh;
@@ -134,6 +140,7 @@ struct GemmParams {
     int stages, stage_bytes, a_off, sfa_off, b_off, sfb_off, atoms_max, sf_warps;
     int pool_units;           // units at the end of the list taken from the counter (-1: all)
     float swiglu_limit;       // > 0: clamped SwiGLU in the gate_up epilogue
+    int prefetch_shared;      // 1: prefetch the shared expert's records into L2 before the wait
 };
 
 struct FinalizeParams {

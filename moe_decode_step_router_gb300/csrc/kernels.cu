@@ -190,6 +190,15 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(RouterParams p) {
         }
         cp_async_commit();
     }
+    // records a later launch streams whatever the routing (the shared expert's): every CTA
+    // prefetches its share into L2 while HBM is otherwise idle in the front end
+    if (p.l2_pf && threadIdx.x == 32) {
+        const size_t nct = (size_t)gridDim.x * gridDim.y, cta = (size_t)blockIdx.y * gridDim.x + blockIdx.x;
+        const size_t share = (p.l2_pf_bytes / nct + 15) & ~(size_t)15;
+        const size_t b0 = cta * share, b1 = b0 + share < p.l2_pf_bytes ? b0 + share : p.l2_pf_bytes;
+        for (size_t o = b0; o < b1; o += 65536)
+            prefetch_l2(p.l2_pf + o, (uint32_t)(b1 - o < 65536 ? b1 - o : 65536));
+    }
     pdl_wait();
     if (!p.logits_in) {
         for (int v = threadIdx.x; v < M * VPR; v += blockDim.x) {
@@ -260,10 +269,10 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(RouterParams p) {
 }
 
 // ------------------------------------------------------------------------------------
-// a2 + a4 in one CTA: top-k of the selection key (score + bias) with ties to the lower
-// expert index, renormalised weights (fp32, within a few ulps of the exact value), then the stable counting
+// a2 + a4: top-k of the selection key (score + bias) with ties to the lower expert index
+// and renormalised weights (fp32, within a few ulps of the exact value), one row per warp
+// over the first ceil(M / 16) CTAs; the last of them to finish then runs the stable counting
 // sort of the (row, slot) pairs into 8-row tiles and the per-expert group table.
-constexpr int kRouteThreads = 512;
 
 // Order-preserving map of an fp32 key to u32: a larger key gives a larger integer; every
 // finite key maps above 0, which marks taken or absent experts.
@@ -305,13 +314,14 @@ __global__ void __launch_bounds__(kRouteThreads) k_topk_route(TopkRouteParams p)
     __shared__ unsigned long long sel[kMaxE + 1];
     __shared__ float bias_s[kMaxE];
     __shared__ int4 sh_warp[32];
-    __shared__ int s_bad;
+    __shared__ int s_bad, s_last;
     pdl_wait();
     pdl_trigger();  // the GEMM's CTAs may take the other SMs and wait there
-    if (blockIdx.x > 0) {
-        // a3: the FC1 input quantisation, on CTAs 1.. beside the top-k of CTA 0
+    const int tk = p.topk_ctas;
+    if ((int)blockIdx.x >= tk) {
+        // a3: the FC1 input quantisation, on the CTAs after the top-k ones
         const int Mpad = round_up(p.M, 16);
-        const int nthreads = (gridDim.x - 1) * blockDim.x, tid = (blockIdx.x - 1) * blockDim.x + threadIdx.x;
+        const int nthreads = (gridDim.x - tk) * blockDim.x, tid = (blockIdx.x - tk) * blockDim.x + threadIdx.x;
         const int nr = quant_units(p.fmt_r, Mpad, p.H);
         for (int u = tid; u < nr; u += nthreads) quant_unit(p.x, p.M, p.H, Mpad, p.fmt_r, p.gs_r, p.xq, p.xs, u);
         if (p.quant_shared) {
@@ -327,7 +337,7 @@ __global__ void __launch_bounds__(kRouteThreads) k_topk_route(TopkRouteParams p)
         if (p.bias)
             for (int e = threadIdx.x; e < E; e += blockDim.x) bias_s[e] = p.bias[e];
         __syncthreads();
-        for (int m = warp; m < M; m += kRouteThreads / 32) {
+        for (int m = (int)blockIdx.x * (kRouteThreads / 32) + warp; m < M; m += tk * (kRouteThreads / 32)) {
             // keys as order-preserving u32 (0 = taken / absent); lane owns e = lane + 32 i
             uint32_t ku[kMaxE / 32];
             float sc[kMaxE / 32];
@@ -388,13 +398,26 @@ __global__ void __launch_bounds__(kRouteThreads) k_topk_route(TopkRouteParams p)
         __syncthreads();
     }
     if (!p.do_route) return;
+    if (tk > 1) {
+        // the last top-k CTA to finish routes every row (the others' rows through L2)
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const int old = atomicAdd(p.topk_arrivals, 1);
+            s_last = (old == tk - 1) ? 1 : 0;
+            if (s_last) *p.topk_arrivals = 0;  // every CTA has arrived: ready for the next launch
+        }
+        __syncthreads();
+        if (!s_last) return;
+        __threadfence();
+    }
     // ---- route
     const int P = M * k;
     if (threadIdx.x == 0) s_bad = 0;
     for (int e = threadIdx.x; e <= E; e += blockDim.x) sel[e] = 0ull;
     __syncthreads();
     for (int q = threadIdx.x; q < P; q += blockDim.x) {
-        const int e = p.topk_idx[q];
+        const int e = __ldcg(p.topk_idx + q);
         if (e < 0 || e >= E) {
             s_bad = 1;
         } else {
@@ -450,7 +473,7 @@ __global__ void __launch_bounds__(kRouteThreads) k_topk_route(TopkRouteParams p)
     }
     __syncthreads();
     for (int q = threadIdx.x; q < P; q += blockDim.x) {
-        const int ee = p.topk_idx[q], m = q / k;
+        const int ee = __ldcg(p.topk_idx + q), m = q / k;
         const unsigned long long below = (m == 0) ? 0ull : (sel[ee] & ((1ull << m) - 1ull));
         const int pos = s_off[ee] + __popcll(below);
         p.perm[pos] = q;
