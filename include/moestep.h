@@ -249,12 +249,10 @@ moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void
  * plugins no allocator, or a serving loop that must not allocate once running (an
  * allocation can synchronise the device or fail under memory pressure). The pages have no
  * counterpart: their engines allocate their buffers at load.
- *  - Takes no workspace and allocates nothing: its scratch (partial logits, scores,
- *    arrival counters; about 1.2 MiB) is one fixed array inside the library, held by every
- *    GPU that loads the library until the process exits. Inputs and outputs are the
- *    caller's, exactly as for moe_router_topk, and the results are the same.
- *  - Limit: when the GEMV runs (logits_in == NULL), ceil(H/512) * E must be <= 4096;
- *    larger layers are rejected with MOE_ERR_UNSUPPORTED before anything is launched.
+ *  - Takes no workspace and allocates nothing: its scratch (the scores; 128 KiB) is one
+ *    fixed array inside the library, held by every GPU that loads the library until the
+ *    process exits. Inputs and outputs are the caller's, exactly as for moe_router_topk,
+ *    and the results are the same, for every layer moe_router_topk accepts.
  *  - The first call on a device looks up the array's device address (with that device
  *    current); make that first call before any stream capture.
  *  - Every call uses the same array and it keeps the last call's contents (each call

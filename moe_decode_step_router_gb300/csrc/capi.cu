@@ -13,6 +13,7 @@
 
 namespace moe {
 __global__ void k_router(RouterParams p);
+__global__ void k_router_rows(RouterParams p);
 __global__ void k_topk_route(TopkRouteParams p);
 __global__ void k_finalize(FinalizeParams p);
 __global__ void k_pack(PackParams p);
@@ -154,8 +155,6 @@ WsLayout layout(const moe_layer_desc* d) {
     L.partials = take(4ull * kPartialSlots * kPartialFloats);
     L.sched = take(4ull * 4);  // gate_up and down: next work item, CTAs finished
     L.gu_done = take(4ull * (kMaxE + 2));  // one launch for both GEMMs: per-group gate_up units done
-    L.rpart = take(4ull * ((d->H + 511) / 512) * d->E * kMaxRows);
-    L.rcnt = take(4ull * ((d->E + 7) / 8));
     L.tcnt = take(16);
     L.total = o;
     return L;
@@ -164,7 +163,7 @@ WsLayout layout(const moe_layer_desc* d) {
 struct DevInfo {
     int dev = -1, sms = 0, smem_optin = 0;
     bool gemm_attr_set = false;
-    bool router_attr_set = false;
+    bool router_rows_attr_set = false;
 };
 thread_local DevInfo g_dev;
 
@@ -216,9 +215,9 @@ moe_status launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_
 }
 
 // ------------------------------------------------------------------ launch helpers
-moe_status launch_router(const moe_layer_desc* d, const WsLayout& L, uint8_t* ws, const void* x,
-                         const void* w_gate, const float* logits_in, int M, float* logits_out, float* scores,
-                         cudaStream_t st, const void* l2_pf = nullptr, size_t l2_pf_bytes = 0) {
+moe_status launch_router(const moe_layer_desc* d, const void* x, const void* w_gate, const float* logits_in, int M,
+                         float* logits_out, float* scores, cudaStream_t st, const void* l2_pf = nullptr,
+                         size_t l2_pf_bytes = 0) {
     RouterParams p{};
     p.l2_pf = static_cast<const uint8_t*>(l2_pf);
     p.l2_pf_bytes = l2_pf_bytes;
@@ -230,21 +229,24 @@ moe_status launch_router(const moe_layer_desc* d, const WsLayout& L, uint8_t* ws
     p.M = M;
     p.H = d->H;
     p.E = d->E;
-    p.part = reinterpret_cast<float*>(ws + L.rpart);
-    p.counters = reinterpret_cast<int32_t*>(ws + L.rcnt);
-    const int nslices = logits_in ? 1 : (d->H + 511) / 512;
-    const int nblocks = (d->E + 7) / 8;
-    const size_t smem = logits_in ? 0 : (size_t)(M + 8) * (512 + 8) * 2;
     DevInfo* di;
     moe_status s = dev_info(&di);
     if (s != MOE_OK) return s;
-    if (!di->router_attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_router, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (kMaxRows + 8) * (512 + 8) * 2);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(k_router)");
-        di->router_attr_set = true;
+    // the GEMV: CTAs of 4 experts x 8 rows over the whole of H, x rows and gate rows in
+    // shared memory ((4 + 8) * H * 2 <= 192 KB, plus 1 KB of static shared memory)
+    if (!logits_in) {
+        const size_t rsmem = (size_t)(4 + (M < 8 ? M : 8)) * d->H * 2;
+        if (!di->router_rows_attr_set) {
+            cudaError_t e = cudaFuncSetAttribute(k_router_rows, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 di->smem_optin - 1024);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(k_router_rows)");
+            di->router_rows_attr_set = true;
+        }
+        return launch_pdl(k_router_rows, dim3((d->E + 3) / 4, (M + 7) / 8), dim3(256), rsmem, st, p,
+                          "k_router_rows launch");
     }
-    return launch_pdl(k_router, dim3(nslices, nblocks), dim3(256), smem, st, p, "k_router launch");
+    // the logits are given: scores only
+    return launch_pdl(k_router, dim3((M * d->E + 255) / 256), dim3(256), 0, st, p, "k_router launch");
 }
 
 // FC1 input quantisation arguments, carried by the top-k launch (CTAs 1..).
@@ -676,7 +678,7 @@ moe_status moe_router_topk(const moe_layer_desc* d, const void* x, const void* w
     uint8_t* w = static_cast<uint8_t*>(ws);
     float* scores = reinterpret_cast<float*>(w + L.scores);
     cudaStream_t st = (cudaStream_t)stream;
-    s = launch_router(d, L, w, x, w_gate, logits_in, M, logits_out, scores, st);
+    s = launch_router(d, x, w_gate, logits_in, M, logits_out, scores, st);
     if (s != MOE_OK) return s;
     QuantArgs qa;
     qa.x = x;
@@ -805,8 +807,8 @@ moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void
     const size_t sh13_bytes = d->has_shared ? (size_t)(2 * d->I_shared / kBlockRows) *
                                                   steps_of(d->shared_fmt, d->H) * record_bytes(d->shared_fmt)
                                             : 0;
-    s = launch_router(d, L, w, a->x, a->w_gate, nullptr, M, logits, scores, st,
-                      d->has_shared ? a->sh13.packed : nullptr, sh13_bytes);
+    s = launch_router(d, a->x, a->w_gate, nullptr, M, logits, scores, st, d->has_shared ? a->sh13.packed : nullptr,
+                      sh13_bytes);
     if (s != MOE_OK) return s;
     QuantArgs qa;
     qa.x = a->x;
@@ -848,17 +850,13 @@ moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void
 // Some callers cannot give the library device memory: a host framework that owns every
 // allocation and hands plugins no allocator, or a serving loop that must not allocate once
 // it is running (an allocation can synchronise the device or fail under memory pressure).
-// For them the router step keeps its scratch (partial logits, scores, arrival counters) in
-// one fixed array in the library's own device memory, allocated when the library is
-// loaded and held by every GPU that loads it until the process exits.
+// For them the router step keeps its scratch (the scores) in one fixed array in the
+// library's own device memory, allocated when the library is loaded and held by every GPU
+// that loads it until the process exits.
 //
-// Layout: [256 B header][256 B per-block counters][scores 64 x 512 fp32][partial logits].
-// The partial-logit region holds 1 MiB, so ceil(H / 512) * E may be at most 4096 when the
-// GEMV runs (logits_in == NULL).
-constexpr size_t kNaHeader = 0, kNaCounters = 256, kNaScores = 512;
-constexpr size_t kNaPartials = kNaScores + 4ull * kMaxRows * kMaxE;
-constexpr size_t kNaPartialFloats = (1u << 20) / 4;
-constexpr size_t kNoAllocScratchBytes = kNaPartials + 4ull * kNaPartialFloats;
+// Layout: [256 B header][scores 64 x 512 fp32].
+constexpr size_t kNaHeader = 0, kNaScores = 256;
+constexpr size_t kNoAllocScratchBytes = kNaScores + 4ull * kMaxRows * kMaxE;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -911,25 +909,16 @@ extern "C" moe_status moe_router_topk_noalloc(const moe_layer_desc* d, const voi
         REQUIRE_PTR(xq_sh, "xq_sh");
         if (d->shared_fmt != MOE_FMT_BF16) REQUIRE_PTR(xq_sh_scales, "xq_sh_scales");
     }
-    const size_t need = logits_in ? 0 : (size_t)((d->H + 511) / 512) * d->E * kMaxRows;
-    if (need > kNaPartialFloats)
-        return fail(MOE_ERR_UNSUPPORTED,
-                    "ceil(H/512) * E = %d exceeds the fixed scratch of the no-allocation router (limit 4096)",
-                    (d->H + 511) / 512 * d->E);
     uint8_t* scratch = noalloc_scratch(&s);
     if (!scratch) return s;
-    // scratch regions as a workspace layout for the shared launch helpers
+    // scratch regions as a workspace layout for the shared launch helpers (the top-k-only
+    // launch reads no group table and no arrival counter)
     WsLayout L{};
     L.header = kNaHeader;
-    L.groups = kNaHeader;  // unused by the top-k-only launch
-    L.rcnt = kNaCounters;
-    L.rpart = kNaPartials;
+    L.groups = kNaHeader;
     cudaStream_t st = (cudaStream_t)stream;
-    // the arrival counters must start at zero; the array keeps the last call's contents
-    cudaError_t e = cudaMemsetAsync(scratch + kNaCounters, 0, 256, st);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(noalloc counters)");
     float* scores = reinterpret_cast<float*>(scratch + kNaScores);
-    s = launch_router(d, L, scratch, x, w_gate, logits_in, M, logits_out, scores, st);
+    s = launch_router(d, x, w_gate, logits_in, M, logits_out, scores, st);
     if (s != MOE_OK) return s;
     QuantArgs qa;
     qa.x = x;

@@ -67,7 +67,7 @@ struct WsHeader {
 // Byte offsets of the workspace regions for a layer and a maximum row count.
 struct WsLayout {
     size_t header, groups, logits, scores, topk_idx, topk_w, counts, perm, inv_perm, tiles, num_tiles;
-    size_t xq, xs, xq_sh, xs_sh, hq, hs, y, cnt_gu, cnt_dn, partials, sched, gu_done, rpart, rcnt, tcnt, total;
+    size_t xq, xs, xq_sh, xs_sh, hq, hs, y, cnt_gu, cnt_dn, partials, sched, gu_done, tcnt, total;
     int max_rows, P_max, G_max, T_max, U_gu, U_dn;
     size_t hq_routed_bytes, hs_routed_bytes;  // shared group's data / scales start here
 };
@@ -80,8 +80,6 @@ struct RouterParams {
     float* logits_out;        // [M, E] or null
     float* scores;            // [M, E]
     int M, H, E;
-    float* part;              // [H/512][E][64] partial logits (workspace)
-    int32_t* counters;        // [ceil(E/8)] arrivals per expert block (self-resetting)
     const uint8_t* l2_pf;     // bytes a later launch streams that do not depend on this one
     size_t l2_pf_bytes;       // (the shared expert's gate_up records): prefetched into L2
 };

@@ -158,40 +158,48 @@ __device__ __forceinline__ int quant_units(int fmt, int Mpad, int H) {
 }
 
 // ------------------------------------------------------------------------------------
-// a1: router GEMV with fp32 accumulation and the fp32 sigmoid score evaluated in double
-// and rounded once (the FC1 input quantisation runs beside the top-k, in k_topk_route).
-// Grid (H slices) x (blocks of 8 experts). A CTA stages its x slice [M][512] and the
-// block's Wg slice [8][512] in shared memory; warp w owns expert e0 + w, its lanes split
-// (row, h range). Partial logits go to the workspace; the last CTA of an expert block
-// sums them in slice order (deterministic) and applies the sigmoid.
+// a2 with the logits given (moe_router_topk with logits_in): the fp32 sigmoid score,
+// evaluated in double and rounded once, as after the GEMV below.
 constexpr int kRouterThreads = 256;
-constexpr int kRouterEB = 8;      // experts per block (one per warp)
-constexpr int kRouterHS = 512;    // H slice
-constexpr int kRouterPitch = kRouterHS + 8;
-constexpr int kRouterMaxSlices = 8192 / kRouterHS;
 
 __global__ void __launch_bounds__(kRouterThreads) k_router(RouterParams p) {
-    extern __shared__ __align__(16) uint16_t rsm[];
-    __shared__ int s_last;
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int H = p.H, M = p.M, E = p.E;
-    const int e0 = blockIdx.y * kRouterEB, slice = blockIdx.x, nslices = gridDim.x;
-    const int h0 = slice * kRouterHS;
-    const int len = min(kRouterHS, H - h0);         // 512, or 256 for the last slice
-    const int VPR = len / 8;                        // 16-byte vectors per row slice
-    uint16_t* xs = rsm;                             // [M][pitch]
-    uint16_t* ws = rsm + (size_t)M * kRouterPitch;  // [8][pitch]
-    if (!p.logits_in) {
-        // the gate weights do not depend on earlier launches: their copies start before
-        // the wait (asynchronous 16-byte copies, all in flight at once)
-        for (int v = threadIdx.x; v < kRouterEB * VPR; v += blockDim.x) {
-            const int r = v / VPR, c = v % VPR, e = min(e0 + r, E - 1);
-            cp_async16(ws + (size_t)r * kRouterPitch + 8 * c, p.wg + (size_t)e * H + h0 + 8 * c);
-        }
-        cp_async_commit();
+    pdl_wait();
+    const int n = p.M * p.E;
+    for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < n; q += gridDim.x * blockDim.x) {
+        const float lg = p.logits_in[q];
+        p.scores[q] = (float)(1.0 / (1.0 + exp(-(double)lg)));
+        if (p.logits_out) p.logits_out[q] = lg;
     }
-    // records a later launch streams whatever the routing (the shared expert's): every CTA
-    // prefetches its share into L2 while HBM is otherwise idle in the front end
+    pdl_trigger();
+}
+
+// ------------------------------------------------------------------------------------
+// a1 with no partial sums leaving the CTA: CTA (i, j) takes experts EPC i .. EPC i + EPC - 1
+// and rows R j .. R j + R - 1 over the whole of H. Their gate rows are copied into shared
+// memory before the dependency wait (they do not depend on earlier launches), the x rows
+// after it. Thread t takes the 16-byte
+// chunks t, t + 256, ... of H for all EPC x R (expert, row) dot products; a warp then folds
+// its 32 partial sums by recursive halving, so that lane l ends with the warp's sum for
+// output l = expert * R + row, and thread l adds the 8 warps' sums in warp order. The order
+// of every addition is fixed: the logits are deterministic. The score is the same fp32
+// sigmoid as in k_router (evaluated in double, rounded once).
+template <int EPC, int R>
+__device__ __forceinline__ void router_rows(const RouterParams& p) {
+    static_assert(EPC * R == 32, "one output per lane");
+    extern __shared__ __align__(16) uint16_t rrs[];
+    __shared__ float red[kRouterThreads / 32][32];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int H = p.H, E = p.E;
+    const int e0 = blockIdx.x * EPC, m0 = blockIdx.y * R;
+    const int M = min(R, p.M - m0);          // rows of this CTA
+    const int V = H / 8;                     // 16-byte chunks per row
+    uint16_t* wsm = rrs;                     // [EPC][H]
+    uint16_t* xsm = rrs + (size_t)EPC * H;   // [M][H]: rows m0 ..
+    for (int v = threadIdx.x; v < EPC * V; v += blockDim.x) {
+        const int r = v / V, c = v % V, e = min(e0 + r, E - 1);
+        cp_async16(wsm + (size_t)r * H + 8 * c, p.wg + (size_t)e * H + 8 * c);
+    }
+    cp_async_commit();
     if (p.l2_pf && threadIdx.x == 32) {
         const size_t nct = (size_t)gridDim.x * gridDim.y, cta = (size_t)blockIdx.y * gridDim.x + blockIdx.x;
         const size_t share = (p.l2_pf_bytes / nct + 15) & ~(size_t)15;
@@ -200,73 +208,62 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(RouterParams p) {
             prefetch_l2(p.l2_pf + o, (uint32_t)(b1 - o < 65536 ? b1 - o : 65536));
     }
     pdl_wait();
-    if (!p.logits_in) {
-        for (int v = threadIdx.x; v < M * VPR; v += blockDim.x) {
-            const int r = v / VPR, c = v % VPR;
-            cp_async16(xs + (size_t)r * kRouterPitch + 8 * c, p.x + (size_t)r * H + h0 + 8 * c);
-        }
-        cp_async_commit();
-        cp_async_wait_all();
-        __syncthreads();
-        // lanes: R row lanes x (32 / R) h splits; rows above 32 handled as a second pass
-        int R = 1;
-        while (R < M && R < 32) R <<= 1;
-        const int nsplit = 32 / R, r = lane % R, sp = lane / R;
-        const int hl = len / nsplit, hb = sp * hl;
-        const int e = e0 + warp;
-        const uint16_t* wrow = ws + (size_t)warp * kRouterPitch;
-        for (int rr = r; rr < ((M + 31) / 32) * 32 && rr < 64; rr += 32) {
-            float acc = 0.0f;
-            if (rr < M) {
-                const uint16_t* xrow = xs + (size_t)rr * kRouterPitch;
-                for (int h = hb; h < hb + hl; h += 8) {
-                    const uint4 xv = *reinterpret_cast<const uint4*>(xrow + h);
-                    const uint4 wv = *reinterpret_cast<const uint4*>(wrow + h);
-                    acc = fmaf(bf16_lo(xv.x), bf16_lo(wv.x), acc); acc = fmaf(bf16_hi(xv.x), bf16_hi(wv.x), acc);
-                    acc = fmaf(bf16_lo(xv.y), bf16_lo(wv.y), acc); acc = fmaf(bf16_hi(xv.y), bf16_hi(wv.y), acc);
-                    acc = fmaf(bf16_lo(xv.z), bf16_lo(wv.z), acc); acc = fmaf(bf16_hi(xv.z), bf16_hi(wv.z), acc);
-                    acc = fmaf(bf16_lo(xv.w), bf16_lo(wv.w), acc); acc = fmaf(bf16_hi(xv.w), bf16_hi(wv.w), acc);
+    const uint16_t* xg = p.x + (size_t)m0 * H;
+    for (int v = threadIdx.x; v < M * V; v += blockDim.x) cp_async16(xsm + 8 * (size_t)v, xg + 8 * (size_t)v);
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
+    float acc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+    for (int c = threadIdx.x; c < V; c += blockDim.x) {
+        uint4 wv[EPC];
+#pragma unroll
+        for (int e = 0; e < EPC; ++e) wv[e] = *reinterpret_cast<const uint4*>(wsm + (size_t)e * H + 8 * c);
+#pragma unroll
+        for (int m = 0; m < R; ++m) {
+            if (m < M) {
+                const uint4 xv = *reinterpret_cast<const uint4*>(xsm + (size_t)m * H + 8 * c);
+#pragma unroll
+                for (int e = 0; e < EPC; ++e) {
+                    float a = acc[e * R + m];
+                    a = fmaf(bf16_lo(xv.x), bf16_lo(wv[e].x), a); a = fmaf(bf16_hi(xv.x), bf16_hi(wv[e].x), a);
+                    a = fmaf(bf16_lo(xv.y), bf16_lo(wv[e].y), a); a = fmaf(bf16_hi(xv.y), bf16_hi(wv[e].y), a);
+                    a = fmaf(bf16_lo(xv.z), bf16_lo(wv[e].z), a); a = fmaf(bf16_hi(xv.z), bf16_hi(wv[e].z), a);
+                    a = fmaf(bf16_lo(xv.w), bf16_lo(wv[e].w), a); a = fmaf(bf16_hi(xv.w), bf16_hi(wv[e].w), a);
+                    acc[e * R + m] = a;
                 }
             }
-            for (int o = R; o < 32; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            if (sp == 0 && rr < M && e < E) __stcg(p.part + ((size_t)slice * E + e) * kMaxRows + rr, acc);
         }
-        pdl_trigger();  // let the top-k launch get scheduled while the slices are summed
-        __threadfence();
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            const int old = atomicAdd(p.counters + blockIdx.y, 1);
-            s_last = (old == nslices - 1) ? 1 : 0;
-        }
-        __syncthreads();
-        if (!s_last) return;
-        __threadfence();
     }
-    // the last CTA of the block: sum the slices in order, sigmoid in double, write scores
-    for (int q = threadIdx.x; q < kRouterEB * M; q += blockDim.x) {
-        const int e = e0 + q / M, m = q % M;
-        if (e >= E) continue;
-        float lg;
-        if (p.logits_in) {
-            lg = p.logits_in[(size_t)m * E + e];
-        } else {
-            // issue every slice's load before the first add (a loop-carried load would
-            // expose one L2 round trip per slice), then sum in slice order
-            float v[kRouterMaxSlices];
+    pdl_trigger();  // let the top-k launch get scheduled while the sums are folded
+    // recursive halving: at the step of width s a lane keeps the half of its live values
+    // selected by its bit s and adds its partner's copy of that half
 #pragma unroll
-            for (int sl = 0; sl < kRouterMaxSlices; ++sl)
-                v[sl] = __ldcg(p.part + ((size_t)min(sl, nslices - 1) * E + e) * kMaxRows + m);
-            lg = v[0];
+    for (int sw = 16; sw >= 1; sw >>= 1) {
+        const bool upper = (lane & sw) != 0;
 #pragma unroll
-            for (int sl = 1; sl < kRouterMaxSlices; ++sl)
-                if (sl < nslices) lg += v[sl];
+        for (int i = 0; i < sw; ++i) {
+            const float send = upper ? acc[i] : acc[i + sw];
+            const float keep = upper ? acc[i + sw] : acc[i];
+            acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, sw);
         }
-        p.scores[(size_t)m * E + e] = (float)(1.0 / (1.0 + exp(-(double)lg)));
-        if (p.logits_out) p.logits_out[(size_t)m * E + e] = lg;
     }
-    if (threadIdx.x == 0 && !p.logits_in) p.counters[blockIdx.y] = 0;
-    pdl_trigger();
+    red[warp][lane] = acc[0];
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int e = e0 + threadIdx.x / R, m = threadIdx.x % R;
+        float lg = red[0][threadIdx.x];
+#pragma unroll
+        for (int w = 1; w < kRouterThreads / 32; ++w) lg += red[w][threadIdx.x];
+        if (m < M && e < E) {
+            p.scores[(size_t)(m0 + m) * E + e] = (float)(1.0 / (1.0 + exp(-(double)lg)));
+            if (p.logits_out) p.logits_out[(size_t)(m0 + m) * E + e] = lg;
+        }
+    }
 }
+
+__global__ void __launch_bounds__(kRouterThreads) k_router_rows(RouterParams p) { router_rows<4, 8>(p); }
 
 // ------------------------------------------------------------------------------------
 // a2 + a4: top-k of the selection key (score + bias) with ties to the lower expert index
@@ -312,7 +309,7 @@ __device__ __forceinline__ void block_scan4(int4 v, int4* out_excl, int4* total,
 
 __global__ void __launch_bounds__(kRouteThreads) k_topk_route(TopkRouteParams p) {
     __shared__ unsigned long long sel[kMaxE + 1];
-    __shared__ float bias_s[kMaxE];
+    __shared__ int s_topk[kMaxRows * kMaxK];  // this CTA's selections, when it also routes
     __shared__ int4 sh_warp[32];
     __shared__ int s_bad, s_last;
     pdl_wait();
@@ -334,20 +331,22 @@ __global__ void __launch_bounds__(kRouteThreads) k_topk_route(TopkRouteParams p)
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int M = p.M, E = p.E, k = p.k;
     if (p.do_topk) {
-        if (p.bias)
-            for (int e = threadIdx.x; e < E; e += blockDim.x) bias_s[e] = p.bias[e];
-        __syncthreads();
         for (int m = (int)blockIdx.x * (kRouteThreads / 32) + warp; m < M; m += tk * (kRouteThreads / 32)) {
             // keys as order-preserving u32 (0 = taken / absent); lane owns e = lane + 32 i
             uint32_t ku[kMaxE / 32];
-            float sc[kMaxE / 32];
-            // unconditional (clamped) loads, all in flight before the first use
+            float sc[kMaxE / 32], bi[kMaxE / 32];
+            // unconditional (clamped) loads of the row's scores and of the bias, all in
+            // flight before the first use
 #pragma unroll
             for (int i = 0; i < kMaxE / 32; ++i) sc[i] = __ldcg(p.scores + (size_t)m * E + min(lane + 32 * i, E - 1));
+            if (p.bias) {
+#pragma unroll
+                for (int i = 0; i < kMaxE / 32; ++i) bi[i] = __ldg(p.bias + min(lane + 32 * i, E - 1));
+            }
 #pragma unroll
             for (int i = 0; i < kMaxE / 32; ++i) {
                 const bool valid = lane + 32 * i < E;
-                ku[i] = valid ? key_u32(p.bias ? __fadd_rn(sc[i], bias_s[lane + 32 * i]) : sc[i]) : 0u;
+                ku[i] = valid ? key_u32(p.bias ? __fadd_rn(sc[i], bi[i]) : sc[i]) : 0u;
                 if (!valid) sc[i] = 0.0f;
             }
             // this lane's best: largest key, lowest index among equals (ascending scan)
@@ -391,6 +390,7 @@ __global__ void __launch_bounds__(kRouteThreads) k_topk_route(TopkRouteParams p)
             }
             if (lane < k) {
                 p.topk_idx[(size_t)m * k + lane] = my_idx;
+                s_topk[m * k + lane] = my_idx;
                 p.topk_w[(size_t)m * k + lane] =
                     p.renormalize ? __fmul_rn(__fdiv_rn(my_sc, ssum), p.rsf) : __fmul_rn(my_sc, p.rsf);
             }
@@ -416,8 +416,10 @@ __global__ void __launch_bounds__(kRouteThreads) k_topk_route(TopkRouteParams p)
     if (threadIdx.x == 0) s_bad = 0;
     for (int e = threadIdx.x; e <= E; e += blockDim.x) sel[e] = 0ull;
     __syncthreads();
+    // the selections: this CTA's own (shared memory) when it took every row, else through L2
+    const bool own = p.do_topk && tk == 1;
     for (int q = threadIdx.x; q < P; q += blockDim.x) {
-        const int e = __ldcg(p.topk_idx + q);
+        const int e = own ? s_topk[q] : __ldcg(p.topk_idx + q);
         if (e < 0 || e >= E) {
             s_bad = 1;
         } else {
@@ -473,7 +475,7 @@ __global__ void __launch_bounds__(kRouteThreads) k_topk_route(TopkRouteParams p)
     }
     __syncthreads();
     for (int q = threadIdx.x; q < P; q += blockDim.x) {
-        const int ee = __ldcg(p.topk_idx + q), m = q / k;
+        const int ee = own ? s_topk[q] : __ldcg(p.topk_idx + q), m = q / k;
         const unsigned long long below = (m == 0) ? 0ull : (sel[ee] & ((1ull << m) - 1ull));
         const int pos = s_off[ee] + __popcll(below);
         p.perm[pos] = q;

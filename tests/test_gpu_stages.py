@@ -205,10 +205,17 @@ def test_stages_against_oracle(name, M):
     check_output(u16(res), ref["res_out"], "residual")
 
 
-def test_router_gemv_logits_and_routing():
-    cfg = synth.config("tiny_mxfp8", E=64, k=6, H=4096, has_bias=True, rsf=2.5)
-    M = 33
-    inp, layer = make(cfg, seed=3, M=M)
+# The GEMV runs in CTAs of 4 experts x 8 rows over the whole of H. (H, E, M): one row block
+# (1, 5, 8 rows), several with a ragged last one (16, 33, 48 rows), E not a multiple of 4
+# (60, 62), the 256-expert layers' shapes, and 64 rows of the 512-expert layer up to H 8192.
+ROUTER_CASES = [(4096, 64, 33), (4096, 64, 1), (4096, 60, 5), (4096, 64, 8), (4096, 62, 16), (7168, 256, 8),
+                (6144, 256, 16), (7168, 256, 48), (4096, 512, 64), (8192, 512, 64)]
+
+
+@pytest.mark.parametrize("H,E,M", ROUTER_CASES)
+def test_router_gemv_logits_and_routing(H, E, M):
+    cfg = synth.config("tiny_mxfp8", E=E, k=6, H=H, has_bias=True, rsf=2.5)
+    inp, layer = make(cfg, seed=3 + M, M=M)
     t = _alloc(layer, M)
     ms.moe_router_topk(layer.d, inp["x"], inp["wg"], inp["bias"], None, M, t["logits"], t["idx"], t["w"], t["xq"],
                        t["xs"], t["xq_sh"], t["xs_sh"], layer.ws)
@@ -223,6 +230,13 @@ def test_router_gemv_logits_and_routing():
     ok_rows = margin >= 1e-5
     assert ok_rows.mean() > 0.5
     assert (npy(t["idx"])[ok_rows] == oidx[ok_rows]).all()
+    assert np.allclose(npy(t["w"])[ok_rows], ow[ok_rows], rtol=2 ** -20, atol=0)
+    # the summation order is fixed: a second call gives the same logits, bit for bit
+    first = npy(t["logits"]).copy()
+    ms.moe_router_topk(layer.d, inp["x"], inp["wg"], inp["bias"], None, M, t["logits"], t["idx"], t["w"], t["xq"],
+                       t["xs"], t["xq_sh"], t["xs_sh"], layer.ws)
+    torch.cuda.synchronize()
+    assert (npy(t["logits"]) == first).all()
 
 
 @pytest.mark.parametrize("M,skew", [(1, False), (8, False), (48, True), (64, True)])
