@@ -499,8 +499,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             prefetch_l2(C1.w + o, (uint32_t)n);
         }
     }
-    // Everything below reads the previous launches' outputs.
-    pdl_wait();
+    // Tensor memory does not depend on earlier launches either (no kernel before this one in
+    // the step holds any, and two GEMM CTAs never share an SM): allocate it before the wait.
     if (warp == 1) {
         tmem_alloc(smem_u32(sm.tmem_base), kTmemCols);
         tmem_relinquish();
@@ -512,9 +512,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
     // nacc - 1 items ahead of the epilogue
     const int bank = acc_bank_cols(p.atoms_max, p.Mpad);
     const int nacc = min(kMaxAcc, bank / p.Mpad);
+    // Everything below reads the previous launches' outputs.
+    pdl_wait();
+    const int ngroups = p.hdr->num_groups;
     pdl_trigger();
 
-    const int ngroups = p.hdr->num_groups;
     // the GEMMs of this launch: gate_up (0), down (1) or both, gate_up's items first
     const int g_first = p.mode == 1 ? 1 : 0, g_last = p.mode == 0 ? 0 : 1;
     auto units_of = [&](int gm) { return ngroups * p.cls[gm][0].MB + (p.has_shared ? p.cls[gm][1].MB : 0); };
