@@ -216,9 +216,10 @@ moe_status launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_
 
 // ------------------------------------------------------------------ launch helpers
 moe_status launch_router(const moe_layer_desc* d, const void* x, const void* w_gate, const float* logits_in, int M,
-                         float* logits_out, float* scores, cudaStream_t st, const void* l2_pf = nullptr,
-                         size_t l2_pf_bytes = 0) {
+                         float* logits_out, float* scores, int32_t* status, cudaStream_t st,
+                         const void* l2_pf = nullptr, size_t l2_pf_bytes = 0) {
     RouterParams p{};
+    p.status = status;
     p.l2_pf = static_cast<const uint8_t*>(l2_pf);
     p.l2_pf_bytes = l2_pf_bytes;
     p.x = static_cast<const uint16_t*>(x);
@@ -233,12 +234,12 @@ moe_status launch_router(const moe_layer_desc* d, const void* x, const void* w_g
     moe_status s = dev_info(&di);
     if (s != MOE_OK) return s;
     // the GEMV: CTAs of 4 experts x 8 rows over the whole of H, x rows and gate rows in
-    // shared memory ((4 + 8) * H * 2 <= 192 KB, plus 1 KB of static shared memory)
+    // shared memory ((4 + 8) * H * 2 <= 192 KB, plus ~1 KB of static shared memory)
     if (!logits_in) {
         const size_t rsmem = (size_t)(4 + (M < 8 ? M : 8)) * d->H * 2;
         if (!di->router_rows_attr_set) {
             cudaError_t e = cudaFuncSetAttribute(k_router_rows, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 di->smem_optin - 1024);
+                                                 di->smem_optin - 2048);
             if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(k_router_rows)");
             di->router_rows_attr_set = true;
         }
@@ -678,7 +679,7 @@ moe_status moe_router_topk(const moe_layer_desc* d, const void* x, const void* w
     uint8_t* w = static_cast<uint8_t*>(ws);
     float* scores = reinterpret_cast<float*>(w + L.scores);
     cudaStream_t st = (cudaStream_t)stream;
-    s = launch_router(d, x, w_gate, logits_in, M, logits_out, scores, st);
+    s = launch_router(d, x, w_gate, logits_in, M, logits_out, scores, reinterpret_cast<int32_t*>(w + L.header), st);
     if (s != MOE_OK) return s;
     QuantArgs qa;
     qa.x = x;
@@ -807,8 +808,8 @@ moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void
     const size_t sh13_bytes = d->has_shared ? (size_t)(2 * d->I_shared / kBlockRows) *
                                                   steps_of(d->shared_fmt, d->H) * record_bytes(d->shared_fmt)
                                             : 0;
-    s = launch_router(d, a->x, a->w_gate, nullptr, M, logits, scores, st, d->has_shared ? a->sh13.packed : nullptr,
-                      sh13_bytes);
+    s = launch_router(d, a->x, a->w_gate, nullptr, M, logits, scores, reinterpret_cast<int32_t*>(w + L.header), st,
+                      d->has_shared ? a->sh13.packed : nullptr, sh13_bytes);
     if (s != MOE_OK) return s;
     QuantArgs qa;
     qa.x = a->x;
@@ -918,7 +919,8 @@ extern "C" moe_status moe_router_topk_noalloc(const moe_layer_desc* d, const voi
     L.groups = kNaHeader;
     cudaStream_t st = (cudaStream_t)stream;
     float* scores = reinterpret_cast<float*>(scratch + kNaScores);
-    s = launch_router(d, x, w_gate, logits_in, M, logits_out, scores, st);
+    s = launch_router(d, x, w_gate, logits_in, M, logits_out, scores, reinterpret_cast<int32_t*>(scratch + kNaHeader),
+                      st);
     if (s != MOE_OK) return s;
     QuantArgs qa;
     qa.x = x;

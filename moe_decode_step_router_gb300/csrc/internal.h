@@ -80,6 +80,7 @@ struct RouterParams {
     float* logits_out;        // [M, E] or null
     float* scores;            // [M, E]
     int M, H, E;
+    int32_t* status;          // status word (MOE_ERR_TIMEOUT when a copy wait runs out)
     const uint8_t* l2_pf;     // bytes a later launch streams that do not depend on this one
     size_t l2_pf_bytes;       // (the shared expert's gate_up records): prefetched into L2
 };

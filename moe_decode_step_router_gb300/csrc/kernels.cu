@@ -176,8 +176,9 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(RouterParams p) {
 // ------------------------------------------------------------------------------------
 // a1 with no partial sums leaving the CTA: CTA (i, j) takes experts EPC i .. EPC i + EPC - 1
 // and rows R j .. R j + R - 1 over the whole of H. Their gate rows are copied into shared
-// memory before the dependency wait (they do not depend on earlier launches), the x rows
-// after it. Thread t takes the 16-byte
+// memory (one bulk copy per row) before the dependency wait (they do not depend on earlier
+// launches), the x rows (one bulk copy) after it.
+constexpr uint64_t kRouterWaitNs = 2000000000ull;  // 2 s Thread t takes the 16-byte
 // chunks t, t + 256, ... of H for all EPC x R (expert, row) dot products; a warp then folds
 // its 32 partial sums by recursive halving, so that lane l ends with the warp's sum for
 // output l = expert * R + row, and thread l adds the 8 warps' sums in warp order. The order
@@ -188,6 +189,8 @@ __device__ __forceinline__ void router_rows(const RouterParams& p) {
     static_assert(EPC * R == 32, "one output per lane");
     extern __shared__ __align__(16) uint16_t rrs[];
     __shared__ float red[kRouterThreads / 32][32];
+    __shared__ __align__(8) uint64_t rbar[2];  // gate rows, x rows
+    __shared__ int s_never;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int H = p.H, E = p.E;
     const int e0 = blockIdx.x * EPC, m0 = blockIdx.y * R;
@@ -195,11 +198,17 @@ __device__ __forceinline__ void router_rows(const RouterParams& p) {
     const int V = H / 8;                     // 16-byte chunks per row
     uint16_t* wsm = rrs;                     // [EPC][H]
     uint16_t* xsm = rrs + (size_t)EPC * H;   // [M][H]: rows m0 ..
-    for (int v = threadIdx.x; v < EPC * V; v += blockDim.x) {
-        const int r = v / V, c = v % V, e = min(e0 + r, E - 1);
-        cp_async16(wsm + (size_t)r * H + 8 * c, p.wg + (size_t)e * H + 8 * c);
+    const uint32_t bar_w = smem_u32(&rbar[0]), bar_x = smem_u32(&rbar[1]);
+    if (threadIdx.x == 0) {
+        s_never = 0;
+        mbar_init(bar_w, 1);
+        mbar_init(bar_x, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(bar_w, (uint32_t)(EPC * H * 2));
+        for (int r = 0; r < EPC; ++r)
+            bulk_g2s(smem_u32(wsm + (size_t)r * H), p.wg + (size_t)min(e0 + r, E - 1) * H, (uint32_t)(H * 2), bar_w);
     }
-    cp_async_commit();
+    __syncthreads();  // the barriers are initialised before anyone waits on them
     if (p.l2_pf && threadIdx.x == 32) {
         const size_t nct = (size_t)gridDim.x * gridDim.y, cta = (size_t)blockIdx.y * gridDim.x + blockIdx.x;
         const size_t share = (p.l2_pf_bytes / nct + 15) & ~(size_t)15;
@@ -208,11 +217,20 @@ __device__ __forceinline__ void router_rows(const RouterParams& p) {
             prefetch_l2(p.l2_pf + o, (uint32_t)(b1 - o < 65536 ? b1 - o : 65536));
     }
     pdl_wait();
-    const uint16_t* xg = p.x + (size_t)m0 * H;
-    for (int v = threadIdx.x; v < M * V; v += blockDim.x) cp_async16(xsm + 8 * (size_t)v, xg + 8 * (size_t)v);
-    cp_async_commit();
-    cp_async_wait_all();
-    __syncthreads();
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(bar_x, (uint32_t)(M * H * 2));
+        bulk_g2s(smem_u32(xsm), p.x + (size_t)m0 * H, (uint32_t)(M * H * 2), bar_x);
+    }
+    bool ok = mbar_wait_bounded(bar_w, 0, &s_never, kRouterWaitNs);
+    ok = mbar_wait_bounded(bar_x, 0, &s_never, kRouterWaitNs) && ok;
+    if (!__syncthreads_and(ok)) {
+        // a copy did not land in time: record it, give the copies one more bounded wait so
+        // that none still writes shared memory when the CTA leaves, and produce nothing
+        if (threadIdx.x == 0 && p.status) atomicCAS(p.status, 0, (int)MOE_ERR_TIMEOUT);
+        mbar_wait_bounded(bar_w, 0, &s_never, kRouterWaitNs / 2);
+        mbar_wait_bounded(bar_x, 0, &s_never, kRouterWaitNs / 2);
+        return;
+    }
     float acc[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
