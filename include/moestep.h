@@ -185,6 +185,8 @@ moe_status moe_pack_weights(const moe_layer_desc* d, int which, const void* code
  * shared expert's format differs, for the shared FC1 (xq_sh, xq_sh_scales; BF16 has no
  * scales). x bf16 [M,H], w_gate bf16 [E,H], bias fp32 [E] | NULL, logits_in fp32 [M,E]
  * | NULL; outputs logits_out fp32 [M,E] | NULL, topk_idx int32 [M,k], topk_w fp32 [M,k].
+ * The GEMV's copy waits are bounded: one that runs out (2 s) sets MOE_ERR_TIMEOUT in the
+ * workspace status word and leaves the outputs unwritten.
  * [README: gate row; Qwen3.5 route row; PR24 Target spec] */
 moe_status moe_router_topk(const moe_layer_desc* d, const void* x, const void* w_gate, const float* bias,
                            const float* logits_in, int M, float* logits_out, int32_t* topk_idx,

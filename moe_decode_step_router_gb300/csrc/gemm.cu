@@ -20,6 +20,13 @@
 // Item boundaries depend only on the routing and every item starts on an even ring slot,
 // so the arithmetic of each output is fixed whichever CTA computes it.
 //
+// A launch runs gate_up (mode 0), down (mode 1) or both (mode 2, moe_expert_ffn). In mode 2
+// every CTA takes its static range of gate_up's units, then its range of down's, cut as the
+// two launches cut them (so the bytes are the same). The gate_up epilogue that completes a
+// unit counts it in its group's counter; a down item's weight copies go out at once and its
+// activation copies wait, in ring order, until its group's counter is complete. The grid
+// waits on itself, so mode 2 is a cooperative launch; every wait is bounded.
+//
 // Roles: warp 0 lane 0 takes the work items, publishes them to the other roles through a
 // shared-memory queue and issues the bulk copies (weight record + activation tile + its
 // scales) into a ring of shared-memory stages. Two MMA issuers (lane 0 of warps 1 and 6)
