@@ -90,3 +90,39 @@ def test_bad_rows_and_pointers_rejected_before_launch(lib):
     assert st == ms.MOE_ERR_INVALID_ARG and "y_pairs" in lib.moe_last_error_string().decode()
     with pytest.raises(ms.MoeError):
         ms._check(ms.MOE_ERR_INVALID_ARG)
+
+
+# Every region moe_ws_view hands out, at the largest step (64 rows), with its size from
+# the shapes the header documents: inside the workspace, 16-byte aligned, and disjoint
+# from every other region (the shared FC1 input may alias the routed one when the
+# formats agree). Host arithmetic only: the base address is never dereferenced.
+@pytest.mark.parametrize("name", list(synth.CONFIGS) + ["nv_bf16_shared"])
+def test_workspace_regions_are_disjoint_and_aligned(lib, name):
+    cfg = (synth.config("nvfp4_h6144_e256_k8_16rows", H=1024, E=16, k=4, I=256, I_sh=256) if name == "nv_bf16_shared"
+           else synth.config(name))
+    d = ms.layer_desc(cfg, synth.act_global_scales(cfg))
+    total = ms.moe_workspace_bytes(d)
+    base = 1 << 40
+    v = ms.WsPtrs()
+    assert lib.moe_ws_view(ctypes.byref(d), ctypes.c_void_p(base), ctypes.byref(v)) == 0
+    M, E, k, H = 64, cfg["E"], cfg["k"], cfg["H"]
+    P = M * k + M
+    fr, fs = cfg["w_fmt"], cfg["sh_fmt"]
+    size = {
+        "status": 32, "logits": 4 * M * E, "scores": 4 * M * E, "topk_idx": 4 * M * k, "topk_w": 4 * M * k,
+        "expert_counts": 4 * (E + 1), "perm": 4 * P, "inv_perm": 4 * P, "tiles": 12 * (P + E + 1), "num_tiles": 4,
+        "xq": ms.moe_act_bytes(fr, M, H), "xq_scales": ms.moe_act_scale_bytes(fr, M, H),
+        "xq_shared": ms.moe_act_bytes(fs, M, H), "xq_shared_scales": ms.moe_act_scale_bytes(fs, M, H),
+        "hq": ms.moe_hq_bytes(d, M), "hq_scales": ms.moe_hq_scale_bytes(d, M), "y_pairs": 4 * P * H}
+    regions = []
+    for field, n in size.items():
+        ptr = getattr(v, field)
+        assert ptr is not None and ptr % 16 == 0, field
+        assert base <= ptr and ptr + n <= base + total, field
+        if n:
+            regions.append((ptr, ptr + n, field))
+    regions.sort()
+    for (a0, a1, fa), (b0, b1, fb) in zip(regions, regions[1:]):
+        if a0 == b0 and {fa, fb} in ({"xq", "xq_shared"}, {"xq_scales", "xq_shared_scales"}) and fr == fs:
+            continue  # the routed and shared FC1 inputs are one buffer when the formats agree
+        assert a1 <= b0, "%s overlaps %s" % (fa, fb)
