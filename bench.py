@@ -152,6 +152,18 @@ def _dist():
     return ws, rank, local
 
 
+def _max_over_ranks(v, world, device):
+    """The job's figure from every rank's own: the largest (the slowest rank's step time)."""
+    if world == 1:
+        return float(v)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _cpu_baseline(cfg, inp, budget_s=20.0):
     """Time the oracle, as it stands, on whole rows of the same workload (bounded)."""
     import numpy as np
@@ -313,11 +325,7 @@ def main():
         dist.barrier()
     clk = clocks.stop()
     step_ms = [s.elapsed_time(e) for s, e in ev]
-    ms_step = float(np.mean(step_ms))
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = _max_over_ranks(np.mean(step_ms), world, dev)
     st = layer.status(stream)
     if st != 0:
         raise RuntimeError("device status %d after the timed steps" % st)
