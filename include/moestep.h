@@ -86,6 +86,14 @@ typedef enum { MOE_FMT_BF16 = 0, MOE_FMT_MXFP8 = 1, MOE_FMT_NVFP4 = 2, MOE_FMT_M
 
 typedef enum { MOE_W13 = 0, MOE_W2 = 1, MOE_SH13 = 2, MOE_SH2 = 3 } moe_proj;
 
+/* How the expert GEMM launches hand their work to the CTAs (moe_layer_desc.gemm_schedule).
+ * STATIC: the units' K steps are cut into equal contiguous ranges, one per CTA (the
+ * default; the fastest on GB300). HYBRID: the last 2 units per CTA are taken from an
+ * atomic counter by whichever CTA finishes its range first. DYNAMIC: every unit is taken
+ * from the counter. All three are deterministic and agree with each other up to the fp32
+ * summation order of a unit cut into pieces. The one-launch FFN always runs STATIC. */
+typedef enum { MOE_SCHED_STATIC = 0, MOE_SCHED_HYBRID = 1, MOE_SCHED_DYNAMIC = 2 } moe_schedule;
+
 /* One MoE layer. Limits: 1 <= k <= 16, k <= E <= 512; H % 256 == 0 and 1024 <= H <= 8192;
  * I, I_shared % 256 == 0 and 256 <= I <= 4096. w_fmt is MXFP8, NVFP4 or MXFP4; shared_fmt is
  * BF16, MXFP8, NVFP4 or MXFP4. gs_a1 / gs_a2 are the static NVFP4 global scales of the routed
@@ -93,7 +101,12 @@ typedef enum { MOE_W13 = 0, MOE_W2 = 1, MOE_SH13 = 2, MOE_SH2 = 3 } moe_proj;
  * they are ignored for other formats. swiglu_limit > 0 selects the clamped SwiGLU of the
  * routed and the shared experts ("SGLang-NVIDIA-Mega" README, shared_ll row): the gate
  * is cut to min(g, L) and the up projection to clamp(u, -L, L) before silu(g) * u, with
- * L = swiglu_limit; 0 (or any value <= 0) is the plain SwiGLU; NaN is rejected. */
+ * L = swiglu_limit; 0 (or any value <= 0) is the plain SwiGLU; NaN is rejected.
+ * Execution choices, fixed when the layer is set up (the pages' engines choose their
+ * kernels and tactics at load, "SGLang-NVIDIA-Mega" README, Design): gemm_schedule is a
+ * moe_schedule (0 = STATIC); ffn_launches is 0 or 1 for gate_up and down in one launch in
+ * moe_step (the default), 2 for two launches. A workspace serves only descriptors whose
+ * moe_workspace_bytes it was sized with (the schedule changes the size). */
 typedef struct {
     int32_t H, E, k, I, I_shared;
     int32_t w_fmt, shared_fmt;
@@ -101,6 +114,7 @@ typedef struct {
     float routed_scaling_factor, rms_eps;
     float gs_a1, gs_a2, gs_a1_shared, gs_a2_shared;
     float swiglu_limit;
+    int32_t gemm_schedule, ffn_launches;
 } moe_layer_desc;
 
 /* A packed projection: the moe_pack_weights output and, for NVFP4, the fp32 global
@@ -226,8 +240,8 @@ moe_status moe_expert_down(const moe_layer_desc* d, const moe_qweight* w2, const
  * every launch leaves at zero), and its weight copies go out before that, so the FC2
  * weights stream while the last FC1 units finish. The grid is one CTA per SM and relies on
  * all of them being resident together; a wait that runs out (2 s) sets MOE_ERR_TIMEOUT in
- * the status word and the launch returns. moe_step uses this call unless the environment
- * sets MOE_FUSED_FFN=0. [README: moe and shared_ll rows] */
+ * the status word and the launch returns. moe_step uses this launch unless the layer's
+ * ffn_launches is 2. [README: moe and shared_ll rows] */
 moe_status moe_expert_ffn(const moe_layer_desc* d, const moe_qweight* w13, const moe_qweight* sh13,
                           const moe_qweight* w2, const moe_qweight* sh2, const void* xq, const void* xq_scales,
                           const void* xq_sh, const void* xq_sh_scales, const int32_t* perm, int M, void* hq,
@@ -242,8 +256,9 @@ moe_status moe_finalize_norm(const moe_layer_desc* d, const float* y_pairs, cons
                              void* outq, void* outq_scales, void* ws, moe_stream_t stream);
 
 /* a1..a7 in four launches chained with programmatic dependent launch (router, routing,
- * moe_expert_ffn, finalize; five with MOE_FUSED_FFN=0, which runs FC1 and FC2 as two
- * launches); intermediates in ws (see moe_ws_view). M in [1, 64]. Capture-safe. */
+ * moe_expert_ffn, finalize; five when the layer's ffn_launches is 2, which runs FC1 and
+ * FC2 as two launches); intermediates in ws (see moe_ws_view). M in [1, 64].
+ * Capture-safe. */
 moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void* ws, moe_stream_t stream);
 
 /* The router step (a1 + a2 + a3, as moe_router_topk) for callers that cannot give the
@@ -251,7 +266,8 @@ moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void
  * plugins no allocator, or a serving loop that must not allocate once running (an
  * allocation can synchronise the device or fail under memory pressure). The pages have no
  * counterpart: their engines allocate their buffers at load.
- *  - Takes no workspace and allocates nothing: its scratch (the scores; 128 KiB) is one
+ *  - Takes no workspace and allocates nothing: its scratch (a 256-byte header and the
+ *    scores of up to 64 rows x 512 experts in fp32: 131,328 bytes, 128 KiB + 256 B) is one
  *    fixed array inside the library, held by every GPU that loads the library until the
  *    process exits. Inputs and outputs are the caller's, exactly as for moe_router_topk,
  *    and the results are the same, for every layer moe_router_topk accepts.
@@ -260,7 +276,9 @@ moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void
  *  - Every call uses the same array and it keeps the last call's contents (each call
  *    clears the counters it needs at zero). Calls that overlap on the GPU race: issue them
  *    on one stream, or order them.
- *  - Device-side status has no workspace to go to; host-side errors are returned as usual. */
+ *  - Device-side status has no workspace to go to. If a router copy wait runs out (2 s),
+ *    the call writes -1 expert ids and zero weights for every row instead of results, and
+ *    leaves the scratch ready for the next call. Host-side errors are returned as usual. */
 moe_status moe_router_topk_noalloc(const moe_layer_desc* d, const void* x, const void* w_gate, const float* bias,
                                    const float* logits_in, int M, float* logits_out, int32_t* topk_idx,
                                    float* topk_w, void* xq, void* xq_scales, void* xq_sh, void* xq_sh_scales,

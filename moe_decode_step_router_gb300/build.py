@@ -50,7 +50,7 @@ def build(verbose: bool = False, extra_flags=()) -> str:
         o = os.path.join(BUILD, src.replace(".cu", ".o"))
         objs.append(o)
         if _stale(o, [s] + headers):
-            jobs.append([nvcc()] + _flags(extra_flags) + ["-dc" if False else "-c", s, "-o", o])
+            jobs.append([nvcc()] + _flags(extra_flags) + ["-c", s, "-o", o])
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)

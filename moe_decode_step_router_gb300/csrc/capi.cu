@@ -79,6 +79,9 @@ moe_status check_desc(const moe_layer_desc* d) {
     REQUIRE(d->routed_scaling_factor == d->routed_scaling_factor, "routed_scaling_factor is NaN");
     REQUIRE(d->rms_eps >= 0.0f, "rms_eps must be >= 0");
     REQUIRE(d->swiglu_limit == d->swiglu_limit, "swiglu_limit must not be NaN");
+    REQUIRE(d->gemm_schedule >= MOE_SCHED_STATIC && d->gemm_schedule <= MOE_SCHED_DYNAMIC,
+            "gemm_schedule=%d: need 0 (static), 1 (hybrid) or 2 (dynamic)", d->gemm_schedule);
+    REQUIRE(d->ffn_launches >= 0 && d->ffn_launches <= 2, "ffn_launches=%d: need 0, 1 or 2", d->ffn_launches);
     if (d->w_fmt == MOE_FMT_NVFP4) REQUIRE(d->gs_a1 > 0.0f && d->gs_a2 > 0.0f, "NVFP4 needs gs_a1, gs_a2 > 0");
     if (d->has_shared && d->shared_fmt == MOE_FMT_NVFP4)
         REQUIRE(d->gs_a1_shared > 0.0f && d->gs_a2_shared > 0.0f, "NVFP4 shared needs gs_a1_shared, gs_a2_shared > 0");
@@ -152,7 +155,7 @@ WsLayout layout(const moe_layer_desc* d) {
     L.y = take(4ull * L.P_max * d->H);
     L.cnt_gu = take(4ull * L.U_gu);
     L.cnt_dn = take(4ull * L.U_dn);
-    L.partials = take(4ull * kPartialSlots * kPartialFloats);
+    L.partials = take(4ull * partial_slots(d->gemm_schedule) * kPartialFloats);
     L.sched = take(4ull * 4);  // gate_up and down: next work item, CTAs finished
     L.gu_done = take(4ull * (kMaxE + 2));  // one launch for both GEMMs: per-group gate_up units done
     L.tcnt = take(16);
@@ -254,6 +257,9 @@ moe_status launch_router(const moe_layer_desc* d, const void* x, const void* w_g
 struct QuantArgs {
     const void* x = nullptr;
     void *xq = nullptr, *xs = nullptr, *xq_sh = nullptr, *xs_sh = nullptr;
+    // router step without a workspace: where the router records a timeout, and the top-k
+    // CTAs' arrival counter that decides which of them clears it
+    int32_t *router_status = nullptr, *arrivals = nullptr;
 };
 
 int quant_units_host(int fmt, int M, int H) {
@@ -289,6 +295,10 @@ moe_status launch_topk_route(const moe_layer_desc* d, const WsLayout& L, uint8_t
     // one row per warp: ceil(M / 16) CTAs of 16 warps take the top-k
     p.topk_ctas = do_topk ? (M + kRouteThreads / 32 - 1) / (kRouteThreads / 32) : 1;
     p.topk_arrivals = (p.topk_ctas > 1 && do_route) ? reinterpret_cast<int32_t*>(ws + L.tcnt) : nullptr;
+    if (qa.router_status) {
+        p.router_status = qa.router_status;
+        p.topk_arrivals = qa.arrivals;
+    }
     int qctas = 0;
     if (qa.x) {
         p.x = static_cast<const uint16_t*>(qa.x);
@@ -318,26 +328,15 @@ struct GemmBuffers {
 };
 
 // Units at the end of a GEMM launch's list that CTAs take from a shared counter once they
-// have finished their equal static range. The default is none: on GB300 the counter-fed
-// items stream measurably slower than the static ranges, which wins everywhere except the
-// largest units. The environment variable MOE_GEMM_SCHEDULE (read at each launch; a
-// captured graph keeps the schedule it was captured with) selects =static (the default),
-// =hybrid (2 units per CTA in the pool) or =dynamic (all units from the counter). Every
-// schedule agrees with the definition of the step within the tolerance of the fp32
-// accumulation, and each is deterministic.
-int gemm_pool_units(int grid) {
-    const char* e = getenv("MOE_GEMM_SCHEDULE");
-    if (e && strcmp(e, "dynamic") == 0) return -1;
-    if (e && strcmp(e, "hybrid") == 0) return 2 * grid;
+// have finished their equal static range (the layer's gemm_schedule). STATIC (the default)
+// takes none: on GB300 the counter-fed items stream measurably slower than the static
+// ranges. HYBRID puts 2 units per CTA in the pool, DYNAMIC all of them. Every schedule
+// agrees with the definition of the step within the tolerance of the fp32 accumulation,
+// and each is deterministic.
+int gemm_pool_units(int schedule, int grid) {
+    if (schedule == MOE_SCHED_DYNAMIC) return -1;
+    if (schedule == MOE_SCHED_HYBRID) return 2 * grid;
     return 0;
-}
-
-// moe_step runs gate_up and down as one launch (a down item waits in the kernel for its
-// group's gate_up units) unless the environment variable MOE_FUSED_FFN=0, read at each
-// call, asks for the two separate launches.
-bool step_fuses_ffn() {
-    const char* e = getenv("MOE_FUSED_FFN");
-    return !(e && strcmp(e, "0") == 0);
 }
 
 // Weight classes of one GEMM (0 gate_up, 1 down): routed experts and the shared expert.
@@ -383,9 +382,12 @@ void gemm_classes(int g, const moe_layer_desc* d, const moe_qweight* wr, const m
 
 // One expert-GEMM launch: mode 0 gate_up, 1 down, 2 both (gate_up items first; a down item
 // waits in the kernel until its group's gate_up units are done).
+constexpr uint64_t kGemmWaitNs = 2000000000ull;  // 2 s: limit of every wait in the GEMM kernel
+
 moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* w13, const moe_qweight* sh13,
                        const moe_qweight* w2, const moe_qweight* sh2, const GemmBuffers& b, int M, const WsLayout& L,
-                       uint8_t* ws, cudaStream_t st, bool prefetch_shared = true) {
+                       uint8_t* ws, cudaStream_t st, bool prefetch_shared = true, uint64_t wait_ns = kGemmWaitNs,
+                       int dep_extra = 0) {
     DevInfo* di;
     moe_status s = dev_info(&di);
     if (s != MOE_OK) return s;
@@ -411,7 +413,9 @@ moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* w13
     p.gu_done = reinterpret_cast<int32_t*>(ws + L.gu_done);
     p.swiglu_limit = d->swiglu_limit > 0.0f ? d->swiglu_limit : 0.0f;
     p.prefetch_shared = prefetch_shared ? 1 : 0;
-    p.pool_units = mode == 2 ? 0 : gemm_pool_units(di->sms < kMaxGemmCtas ? di->sms : kMaxGemmCtas);
+    p.wait_ns = wait_ns;
+    p.dep_extra = dep_extra;
+    p.pool_units = mode == 2 ? 0 : gemm_pool_units(d->gemm_schedule, di->sms < kMaxGemmCtas ? di->sms : kMaxGemmCtas);
     p.status = reinterpret_cast<int32_t*>(ws + L.header);
     if (mode != 1) gemm_classes(0, d, w13, sh13, b, M, p.cls[0]);
     if (mode != 0) gemm_classes(1, d, w2, sh2, b, M, p.cls[1]);
@@ -830,7 +834,7 @@ moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void
     b.hs = w + L.hs;
     b.y = reinterpret_cast<float*>(w + L.y);
     b.perm = perm;
-    if (step_fuses_ffn()) {
+    if (d->ffn_launches != 2) {
         s = launch_gemm(2, d, &a->w13, &a->sh13, &a->w2, &a->sh2, b, M, L, w, st, false);
         if (s != MOE_OK) return s;
     } else {
@@ -855,8 +859,8 @@ moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void
 // library's own device memory, allocated when the library is loaded and held by every GPU
 // that loads it until the process exits.
 //
-// Layout: [256 B header][scores 64 x 512 fp32].
-constexpr size_t kNaHeader = 0, kNaScores = 256;
+// Layout: [256 B header: router status word, top-k arrival counter][scores 64 x 512 fp32].
+constexpr size_t kNaHeader = 0, kNaArrivals = 16, kNaScores = 256;
 constexpr size_t kNoAllocScratchBytes = kNaScores + 4ull * kMaxRows * kMaxE;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -928,8 +932,32 @@ extern "C" moe_status moe_router_topk_noalloc(const moe_layer_desc* d, const voi
     qa.xs = xq_scales;
     qa.xq_sh = xq_sh;
     qa.xs_sh = xq_sh_scales;
+    qa.router_status = reinterpret_cast<int32_t*>(scratch + kNaHeader);
+    qa.arrivals = reinterpret_cast<int32_t*>(scratch + kNaArrivals);
     s = launch_topk_route(d, L, scratch, M, scores, bias, topk_idx, topk_w, 1, 0, nullptr, nullptr, nullptr, nullptr,
                           nullptr, st, qa);
+    if (s != MOE_OK) return s;
+    return ok();
+}
+
+// Test of the GEMM's timeout path, not part of the public ABI (the header does not declare
+// it): moe_expert_ffn with every down item's counter target one above what the FC1 units
+// can reach and all waits limited to wait_ns, so the producers give up after wait_ns, record
+// MOE_ERR_TIMEOUT in the workspace status word, and every CTA drains its copies and MMAs,
+// frees its tensor memory and returns. The workspace then needs moe_workspace_init.
+moe_status moe_internal_ffn_unreachable_wait(const moe_layer_desc* d, const moe_qweight* w13, const moe_qweight* sh13,
+                                             const moe_qweight* w2, const moe_qweight* sh2, const void* xq,
+                                             const void* xq_scales, const void* xq_sh, const void* xq_sh_scales,
+                                             const int32_t* perm, int M, void* hq, void* hq_scales, float* y_pairs,
+                                             void* ws, uint64_t wait_ns, moe_stream_t stream) {
+    GemmBuffers b{};
+    moe_status s = gate_up_buffers(d, w13, sh13, xq, xq_scales, xq_sh, xq_sh_scales, perm, M, hq, hq_scales, ws, b);
+    if (s != MOE_OK) return s;
+    if ((s = down_buffers(d, w2, sh2, hq, hq_scales, M, y_pairs, ws, b)) != MOE_OK) return s;
+    REQUIRE(wait_ns >= 1000000ull && wait_ns <= kGemmWaitNs, "wait_ns=%llu: need 1 ms .. 2 s",
+            (unsigned long long)wait_ns);
+    s = launch_gemm(2, d, w13, sh13, w2, sh2, b, M, layout(d), static_cast<uint8_t*>(ws), (cudaStream_t)stream, true,
+                    wait_ns, 1);
     if (s != MOE_OK) return s;
     return ok();
 }

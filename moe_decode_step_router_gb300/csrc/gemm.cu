@@ -47,7 +47,6 @@
 
 namespace moe {
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxAcc = 8;  // up to 8 accumulator buffers per bank
 
@@ -339,9 +338,9 @@ __device__ __forceinline__ float warp_max_f(float v) {
     return v;
 }
 
-// Waits until *ctr >= target (acquire, bounded by kWaitLimitNs or the abort flag), then
-// orders this thread's later bulk copies (async proxy) after what the acquire made visible.
-__device__ __forceinline__ bool wait_at_least(const int32_t* ctr, int target, volatile int* abort) {
+// Waits until *ctr >= target (acquire, bounded by lim ns or the abort flag), then orders
+// this thread's later bulk copies (async proxy) after what the acquire made visible.
+__device__ __forceinline__ bool wait_at_least(const int32_t* ctr, int target, volatile int* abort, uint64_t lim) {
     uint64_t t0 = 0;
     for (uint32_t i = 0;; ++i) {
         int v;
@@ -351,7 +350,7 @@ __device__ __forceinline__ bool wait_at_least(const int32_t* ctr, int target, vo
             t0 = globaltimer();
         } else if ((i & 15) == 0) {
             if (*abort) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) return false;
+            if (globaltimer() - t0 > lim) return false;
         }
         __nanosleep(128);
     }
@@ -369,9 +368,9 @@ __device__ __forceinline__ bool poll_at_least(const int32_t* ctr, int target) {
 }
 
 // Reads queue entry i, waiting until it is published; false on a timeout.
-__device__ __forceinline__ bool q_read(const GemmSmem& sm, int i, WorkItem& w, volatile int* abort) {
+__device__ __forceinline__ bool q_read(const GemmSmem& sm, int i, WorkItem& w, volatile int* abort, uint64_t lim) {
     const int qi = i % kGemmQueue;
-    if (!mbar_wait_bounded(smem_u32(&sm.q_full[qi]), (uint32_t)(i / kGemmQueue) & 1u, abort, kWaitLimitNs))
+    if (!mbar_wait_bounded(smem_u32(&sm.q_full[qi]), (uint32_t)(i / kGemmQueue) & 1u, abort, lim))
         return false;
     w = sm.queue[qi];
     return true;
@@ -388,7 +387,7 @@ template <int FMT, bool CP>
 __device__ __forceinline__ int mma_segment(uint32_t ready0, uint32_t empty0, Ring& rg, int ka, int kb, int par,
                                            uint64_t adesc0, uint64_t bdesc0, uint64_t sfadesc0, uint64_t sfbdesc0,
                                            uint32_t stage16, uint32_t d_tmem, uint32_t sf_t0, uint32_t sf_stride,
-                                           uint32_t sfb_cols, uint32_t N, volatile int* abort) {
+                                           uint32_t sfb_cols, uint32_t N, volatile int* abort, uint64_t lim) {
     static_assert(!(CP && FMT == MOE_FMT_NVFP4), "NVFP4 scales are copied by the copy warps");
     uint32_t id[4];
 #pragma unroll
@@ -401,7 +400,7 @@ __device__ __forceinline__ int mma_segment(uint32_t ready0, uint32_t empty0, Rin
     for (int kk = ka; kk < kb; ++kk, rg.adv1()) {
         const int st = rg.st;
         if ((st & 1) != par) continue;
-        if (!mbar_wait_bounded(ready0 + 8u * st, rg.ph, abort, kWaitLimitNs)) return -1;
+        if (!mbar_wait_bounded(ready0 + 8u * st, rg.ph, abort, lim)) return -1;
         tc_fence_after();
         const uint64_t so = (uint64_t)st * stage16;
         const uint64_t ad = adesc0 + so, bd = bdesc0 + so;
@@ -535,6 +534,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
     const bool dyn = pool_of(g_first) > 0;
     const int c = blockIdx.x;
     volatile int* abort_flag = sm.abort_flag;
+    const uint64_t wlim = p.wait_ns;  // limit of every wait
 
     if (warp == 0) {
         // ================================================================ producer
@@ -555,7 +555,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             int dh = 0, dt = 0;  // deferred slots issued / recorded
             int pos = 0;         // ring slots filled so far (bubbles included)
             int met = -1;        // group counter known to be complete (gu_done index)
-            auto dep_target = [&](int d) { return p.cls[0][d == kMaxE ? 1 : 0].MB; };
+            auto dep_target = [&](int d) { return p.cls[0][d == kMaxE ? 1 : 0].MB + p.dep_extra; };
             auto issue_b = [&](const Deferred& e) {
                 bulk_g2s(e.stage + p.b_off, e.b, e.bb, e.fb);
                 if (e.sb) bulk_g2s(e.stage + p.sfb_off, e.s, e.sb, e.fb);
@@ -567,7 +567,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                     const Deferred& e = dq[dh % kMaxStages];
                     if (e.dep != met) {
                         if (e.pos <= pos_lim || e.q <= q_lim) {
-                            if (!wait_at_least(p.gu_done + e.dep, dep_target(e.dep), abort_flag)) return false;
+                            if (!wait_at_least(p.gu_done + e.dep, dep_target(e.dep), abort_flag, wlim)) return false;
                         } else if (!poll_at_least(p.gu_done + e.dep, dep_target(e.dep))) {
                             return true;
                         }
@@ -584,7 +584,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                 const int qi = qn % kGemmQueue;
                 if (dh < dt && !drain(INT_MIN, qn - kGemmQueue)) return false;
                 if (!mbar_wait_bounded(smem_u32(&sm.q_empty[qi]), ((uint32_t)(qn / kGemmQueue) & 1u) ^ 1u, abort_flag,
-                                       kWaitLimitNs))
+                                       wlim))
                     return false;
                 sm.queue[qi] = it;
                 mbar_arrive(smem_u32(&sm.q_full[qi]));
@@ -610,7 +610,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                 for (int j = 0; j < nst + (nst & 1); ++j, rg.adv1(), ++pos) {
                     const int st = rg.st;
                     if (dh < dt && !drain(pos - S, INT_MIN)) return false;
-                    if (!mbar_wait_bounded(smem_u32(&sm.empty[st]), rg.ph ^ 1u, abort_flag, kWaitLimitNs))
+                    if (!mbar_wait_bounded(smem_u32(&sm.empty[st]), rg.ph ^ 1u, abort_flag, wlim))
                         return false;
                     const uint32_t fb = smem_u32(&sm.full[st]);
                     issued_mask |= 1u << st;
@@ -711,11 +711,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             }
             if (ok && dh < dt) ok = drain(INT_MAX, INT_MAX);
             if (!ok) set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
+            // after a timeout, slots still deferred get their activation copies anyway (stale
+            // data that no MMA reads: the other roles have seen the abort flag), so that every
+            // stage's barrier completes and the drain below finds no copy missing
+            while (dh < dt) {
+                issue_b(dq[dh % kMaxStages]);
+                ++dh;
+            }
             // the end marker
             if (ok) {
                 const int qi = qn % kGemmQueue;
                 if (mbar_wait_bounded(smem_u32(&sm.q_empty[qi]), ((uint32_t)(qn / kGemmQueue) & 1u) ^ 1u, abort_flag,
-                                      kWaitLimitNs)) {
+                                      wlim)) {
                     sm.queue[qi].cls = -1;
                     mbar_arrive(smem_u32(&sm.q_full[qi]));
                 } else {
@@ -728,7 +735,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             for (int i = 0; i < S; ++i) {
                 if (!(issued_mask >> i & 1u)) continue;
                 const uint32_t par = (i < rg.st) ? rg.ph : (rg.ph ^ 1u);
-                mbar_wait_bounded(smem_u32(&sm.full[i]), par, sm.never, kWaitLimitNs / 2);
+                mbar_wait_bounded(smem_u32(&sm.full[i]), par, sm.never, wlim / 2);
             }
         }
     } else if (warp == 1 || warp == 6) {
@@ -753,7 +760,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             const uint32_t bank_t = tmem + (uint32_t)(par * bank);
             for (int qn = 0;; ++qn) {
                 WorkItem it;
-                if (!q_read(sm, qn, it, abort_flag)) {
+                if (!q_read(sm, qn, it, abort_flag, wlim)) {
                     set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
                     break;
                 }
@@ -762,7 +769,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                 const GemmClass& C = p.cls[it.cls >> 1][it.cls & 1];
                 const uint32_t N = (it.cls == 2) ? (uint32_t)round_up(it.rows, 16) : (uint32_t)p.Mpad;
                 if (!mbar_wait_bounded(smem_u32(&sm.acc_empty[ab]), ((acc_ph >> ab) & 1u) ^ 1u, abort_flag,
-                                       kWaitLimitNs)) {
+                                       wlim)) {
                     set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
                     break;
                 }
@@ -770,7 +777,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                 const uint32_t d_tmem = bank_t + (uint32_t)(ab * p.Mpad);
 #define MOE_SEG(F, CPV)                                                                                        \
     mma_segment<F, CPV>(wait0, empty0, rg, it.ka, it.kb, par, adesc0, bdesc0, sfadesc0, sfbdesc0, stage16, d_tmem, \
-                        sf_t0, 8 * am, 4 * am, N, abort_flag)
+                        sf_t0, 8 * am, 4 * am, N, abort_flag, wlim)
                 // launches with NVFP4 weights always have the copy warps (host invariant)
                 int n;
                 if (p.sf_warps) {
@@ -796,7 +803,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                 // back to the producer
                 if ((it.kb - it.ka) & 1) {
                     if ((rg.st & 1) == par) {
-                        if (!mbar_wait_bounded(wait0 + 8u * rg.st, rg.ph, abort_flag, kWaitLimitNs)) {
+                        if (!mbar_wait_bounded(wait0 + 8u * rg.st, rg.ph, abort_flag, wlim)) {
                             set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
                             break;
                         }
@@ -813,7 +820,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             }
             // wait until every issued MMA has completed before the TMEM is released
             tc_commit(smem_u32(&sm.drain[par]));
-            mbar_wait_bounded(smem_u32(&sm.drain[par]), 0u, sm.never, kWaitLimitNs / 2);
+            mbar_wait_bounded(smem_u32(&sm.drain[par]), 0u, sm.never, wlim / 2);
         }
     } else if (warp >= 7) {
         // ================================================================ scale-factor copies
@@ -835,7 +842,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             bool ok = true;
             for (int qn = 0; ok; ++qn) {
                 WorkItem it;
-                if (!q_read(sm, qn, it, abort_flag)) {
+                if (!q_read(sm, qn, it, abort_flag, wlim)) {
                     set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
                     break;
                 }
@@ -846,7 +853,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                 const int nst = it.kb - it.ka;
                 for (int s = 0; s < nst + (nst & 1); ++s, rg.adv1()) {
                     const int st = rg.st;
-                    if (!mbar_wait_bounded(full0 + 8u * st, rg.ph, abort_flag, kWaitLimitNs)) {
+                    if (!mbar_wait_bounded(full0 + 8u * st, rg.ph, abort_flag, wlim)) {
                         set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);
                         ok = false;
                         break;
@@ -863,7 +870,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                 }
             }
             tc_commit(smem_u32(&sm.sf_drain[j]));
-            mbar_wait_bounded(smem_u32(&sm.sf_drain[j]), 0u, sm.never, kWaitLimitNs / 2);
+            mbar_wait_bounded(smem_u32(&sm.sf_drain[j]), 0u, sm.never, wlim / 2);
         }
     } else {
         // ================================================================ epilogue
@@ -883,9 +890,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             bool ok = true;
             if (et == 0) {
                 ok = mbar_wait_bounded(smem_u32(&sm.q_full[qi]), (uint32_t)(qn / kGemmQueue) & 1u, abort_flag,
-                                       kWaitLimitNs);
+                                       wlim);
                 if (ok && sm.queue[qi].cls >= 0)
-                    ok = mbar_wait_bounded(smem_u32(&sm.acc_full[ab]), (acc_ph >> ab) & 1u, abort_flag, kWaitLimitNs);
+                    ok = mbar_wait_bounded(smem_u32(&sm.acc_full[ab]), (acc_ph >> ab) & 1u, abort_flag, wlim);
             }
             if (!named_bar_and(1, 128, ok)) {
                 if (et == 0) set_error(p.status, sm.abort_flag, MOE_ERR_TIMEOUT);

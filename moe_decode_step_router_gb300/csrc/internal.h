@@ -15,11 +15,16 @@ constexpr int kTileRows = 8;         // route tile height
 constexpr int kStepBytes = 128;      // K bytes per pipeline step (one 128-byte swizzle row)
 constexpr int kBlockRows = 128;      // weight rows per MMA block (the MMA's M)
 constexpr int kAtomBytes = 512;      // scale atom: 128 rows x 4 bytes
-constexpr int kMaxGemmCtas = 256;    // partial-sum slots are sized for this many CTAs
+constexpr int kMaxGemmCtas = 160;    // GEMM grid cap (one CTA per SM); partial-sum slots are sized for it
 constexpr int kPartialFloats = kMaxRows * kBlockRows;  // one partial sum of a unit piece
 constexpr int kMaxPieces = 4;        // pieces of a unit cut in the dynamic pool
 constexpr int kPoolSlot0 = 2 * kMaxGemmCtas;  // static ranges: 2 slots per CTA; then the pool's
-constexpr int kPartialSlots = kPoolSlot0 + kMaxPieces * kMaxGemmCtas;
+// Partial-sum slots of a workspace: a single-GEMM launch uses [0, kPoolSlot0) for its
+// static ranges and, with a counter-fed schedule, the pool's kMaxPieces per CTA after them;
+// the one-launch FFN uses [0, kPoolSlot0) for gate_up and the next kPoolSlot0 for down.
+__host__ __device__ inline int partial_slots(int schedule) {
+    return kPoolSlot0 + (schedule == MOE_SCHED_STATIC ? kPoolSlot0 : kMaxPieces * kMaxGemmCtas);
+}
 constexpr int kGemmQueue = 16;       // work items in flight between a CTA's roles
 constexpr int kMaxStages = 16;       // ring slots of the GEMM pipeline
 constexpr int kDeferBytes = kMaxStages * 48;  // producer's deferred copies (shared memory)
@@ -94,7 +99,10 @@ struct TopkRouteParams {
     float* topk_w;            // [M, k]
     int M, E, k, renormalize, has_shared, do_topk, do_route;
     int topk_ctas;            // CTAs 0..topk_ctas-1 take the rows (one per warp); the last to finish routes
-    int32_t* topk_arrivals;   // their arrival counter (self-resetting; used when topk_ctas > 1 and routing)
+    int32_t* topk_arrivals;   // their arrival counter (self-resetting; used when topk_ctas > 1 and routing,
+                              // or to clear router_status)
+    int32_t* router_status;   // or null: a router timeout recorded here (no workspace) makes every row
+                              // -1 ids / 0 weights; the last top-k CTA clears it
     float rsf;
     int32_t *counts, *perm, *inv_perm, *tiles, *num_tiles;
     Group* groups;
@@ -140,6 +148,9 @@ struct GemmParams {
     int pool_units;           // units at the end of the list taken from the counter (-1: all)
     float swiglu_limit;       // > 0: clamped SwiGLU in the gate_up epilogue
     int prefetch_shared;      // 1: prefetch the shared expert's records into L2 before the wait
+    uint64_t wait_ns;         // limit of every wait (2 s)
+    int dep_extra;            // 0; 1 makes the down items' counter targets unreachable (a test
+                              // of the timeout path, never set by the public calls)
 };
 
 struct FinalizeParams {

@@ -166,13 +166,14 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(RouterParams p) {
 // a1 with no partial sums leaving the CTA: CTA (i, j) takes experts EPC i .. EPC i + EPC - 1
 // and rows R j .. R j + R - 1 over the whole of H. Their gate rows are copied into shared
 // memory (one bulk copy per row) before the dependency wait (they do not depend on earlier
-// launches), the x rows (one bulk copy) after it.
-constexpr uint64_t kRouterWaitNs = 2000000000ull;  // 2 s Thread t takes the 16-byte
-// chunks t, t + 256, ... of H for all EPC x R (expert, row) dot products; a warp then folds
+// launches), the x rows (one bulk copy) after it. Thread t takes the 16-byte chunks
+// t, t + 256, ... of H for all EPC x R (expert, row) dot products; a warp then folds
 // its 32 partial sums by recursive halving, so that lane l ends with the warp's sum for
 // output l = expert * R + row, and thread l adds the 8 warps' sums in warp order. The order
 // of every addition is fixed: the logits are deterministic. The score is the same fp32
 // sigmoid as in k_router (evaluated in double, rounded once).
+constexpr uint64_t kRouterWaitNs = 2000000000ull;  // 2 s: limit of the router's copy waits
+
 template <int EPC, int R>
 __device__ __forceinline__ void router_rows(const RouterParams& p) {
     static_assert(EPC * R == 32, "one output per lane");
@@ -337,6 +338,29 @@ __global__ void __launch_bounds__(kRouteThreads) k_topk_route(TopkRouteParams p)
     }
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int M = p.M, E = p.E, k = p.k;
+    // without a workspace a router timeout has no status word to go to: its scores were
+    // never written, so every row gets -1 ids and zero weights instead of stale results
+    const bool router_failed = p.router_status && __ldcg(p.router_status) != 0;
+    if (p.do_topk && router_failed) {
+        for (int q = (int)blockIdx.x * blockDim.x + threadIdx.x; q < M * k; q += tk * blockDim.x) {
+            p.topk_idx[q] = -1;
+            p.topk_w[q] = 0.0f;
+        }
+    }
+    if (p.router_status) {
+        // the last top-k CTA to read the record clears it for the next call
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            bool last = true;
+            if (tk > 1) {
+                __threadfence();
+                last = atomicAdd(p.topk_arrivals, 1) == tk - 1;
+                if (last) *p.topk_arrivals = 0;
+            }
+            if (last && router_failed) *p.router_status = 0;
+        }
+        if (router_failed) return;
+    }
     if (p.do_topk) {
         for (int m = (int)blockIdx.x * (kRouteThreads / 32) + warp; m < M; m += tk * (kRouteThreads / 32)) {
             // keys as order-preserving u32 (0 = taken / absent); lane owns e = lane + 32 i

@@ -16,6 +16,8 @@ LIB_PATH = os.path.join(HERE, "libmoestep.so")
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT = range(5)
 MOE_FMT_BF16, MOE_FMT_MXFP8, MOE_FMT_NVFP4, MOE_FMT_MXFP4 = 0, 1, 2, 3
 MOE_W13, MOE_W2, MOE_SH13, MOE_SH2 = 0, 1, 2, 3
+MOE_SCHED_STATIC, MOE_SCHED_HYBRID, MOE_SCHED_DYNAMIC = 0, 1, 2
+SCHEDULES = {"static": MOE_SCHED_STATIC, "hybrid": MOE_SCHED_HYBRID, "dynamic": MOE_SCHED_DYNAMIC}
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA",
                 4: "MOE_ERR_TIMEOUT"}
 
@@ -40,7 +42,7 @@ class LayerDesc(ctypes.Structure):
                 ("emit_next_mxfp8", ctypes.c_int32), ("routed_scaling_factor", ctypes.c_float),
                 ("rms_eps", ctypes.c_float), ("gs_a1", ctypes.c_float), ("gs_a2", ctypes.c_float),
                 ("gs_a1_shared", ctypes.c_float), ("gs_a2_shared", ctypes.c_float),
-                ("swiglu_limit", ctypes.c_float)]
+                ("swiglu_limit", ctypes.c_float), ("gemm_schedule", ctypes.c_int32), ("ffn_launches", ctypes.c_int32)]
 
 
 class QWeight(ctypes.Structure):
@@ -127,10 +129,13 @@ def _check(st):
 
 
 def layer_desc(cfg, gs_a=(1.0, 1.0, 1.0, 1.0)) -> LayerDesc:
+    """The layer descriptor of a workload dict; `schedule` ("static", "hybrid", "dynamic")
+    and `ffn_launches` (1 or 2) are the optional execution choices."""
     return LayerDesc(cfg["H"], cfg["E"], cfg["k"], cfg["I"], cfg["I_sh"], cfg["w_fmt"], cfg["sh_fmt"],
                      int(cfg.get("has_shared", True)), int(cfg["has_bias"]), int(cfg.get("renormalize", True)),
                      int(cfg.get("emit_next", False)), float(cfg["rsf"]), float(cfg["eps"]), float(gs_a[0]),
-                     float(gs_a[1]), float(gs_a[2]), float(gs_a[3]), float(cfg.get("swiglu_limit", 0.0)))
+                     float(gs_a[1]), float(gs_a[2]), float(gs_a[3]), float(cfg.get("swiglu_limit", 0.0)),
+                     SCHEDULES[cfg.get("schedule", "static")], int(cfg.get("ffn_launches", 1)))
 
 
 def qweight(packed, gs=None) -> QWeight:

@@ -3,6 +3,9 @@ canonical ones (numpy), drive the oracle on the same seeded inputs, and apply th
 output tolerance of the step."""
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import torch
 
@@ -122,3 +125,28 @@ def make(cfg, seed=0, M=None, device="cuda"):
 
 def oracle_layer(cfg, inp):
     return oracle.make_layer(cfg, inp["gs_a"])
+
+
+def oracle_step_rows_parallel(L, rows, *args, **kw):
+    """oracle.step_rows over `rows`, one row per task on a pool of host threads.
+
+    Rows are independent in the step's definition, and the oracle's C code keeps no
+    global state and releases the interpreter lock while it runs, so the rows run in
+    parallel; the result is the same dict as one call over all the rows."""
+    rows = [int(r) for r in rows]
+    with ThreadPoolExecutor(max_workers=max(1, min(len(rows), os.cpu_count() or 1))) as ex:
+        parts = list(ex.map(lambda r: oracle.step_rows(L, [r], *args, **kw), rows))
+    out = {}
+    for key in parts[0]:
+        vals = [p[key] for p in parts]
+        out[key] = None if vals[0] is None else np.concatenate(vals, axis=0)
+    return out
+
+
+def check_next_mxfp8(out16, oq, os_):
+    """The next layer's MXFP8 input is the block quantisation of the step's own bf16 output:
+    bit for bit the oracle's quantiser applied to the same values."""
+    v = bf16_to_f64(out16).astype(np.float32)
+    rq, rs = oracle.quant(oracle.FMT_MXFP8, v)
+    assert (np.asarray(oq) == rq).all(), "next-layer MXFP8 codes differ from the quantiser of the output"
+    assert (np.asarray(os_) == rs).all(), "next-layer MXFP8 scales differ from the quantiser of the output"

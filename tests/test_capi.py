@@ -53,7 +53,9 @@ def test_sizes(lib):
 @pytest.mark.parametrize("field,value,status", [
     ("H", 1000, ms.MOE_ERR_INVALID_ARG), ("E", 0, ms.MOE_ERR_INVALID_ARG), ("k", 17, ms.MOE_ERR_INVALID_ARG),
     ("I", 300, ms.MOE_ERR_INVALID_ARG), ("w_fmt", ms.MOE_FMT_BF16, ms.MOE_ERR_UNSUPPORTED),
-    ("shared_fmt", 7, ms.MOE_ERR_UNSUPPORTED), ("swiglu_limit", float("nan"), ms.MOE_ERR_INVALID_ARG)])
+    ("shared_fmt", 7, ms.MOE_ERR_UNSUPPORTED), ("swiglu_limit", float("nan"), ms.MOE_ERR_INVALID_ARG),
+    ("gemm_schedule", 3, ms.MOE_ERR_INVALID_ARG), ("gemm_schedule", -1, ms.MOE_ERR_INVALID_ARG),
+    ("ffn_launches", 3, ms.MOE_ERR_INVALID_ARG)])
 def test_bad_descriptor_rejected(lib, field, value, status):
     d = _desc()
     setattr(d, field, value)
@@ -126,3 +128,18 @@ def test_workspace_regions_are_disjoint_and_aligned(lib, name):
         if a0 == b0 and {fa, fb} in ({"xq", "xq_shared"}, {"xq_scales", "xq_shared_scales"}) and fr == fs:
             continue  # the routed and shared FC1 inputs are one buffer when the formats agree
         assert a1 <= b0, "%s overlaps %s" % (fa, fb)
+
+
+def test_workspace_size_follows_the_schedule(lib):
+    """The counter-fed schedules need the pool's partial-sum slots (4 per CTA of 64 x 128
+    fp32); the default static schedule does not carry them."""
+    cfg = synth.config("mxfp8_h7168_e256_k8_8rows")
+    sizes = {}
+    for name in ("static", "hybrid", "dynamic"):
+        d = ms.layer_desc(dict(cfg, schedule=name), synth.act_global_scales(cfg))
+        sizes[name] = ms.moe_workspace_bytes(d)
+    slot = 64 * 128 * 4
+    assert sizes["hybrid"] == sizes["dynamic"]
+    assert sizes["hybrid"] - sizes["static"] == (4 * 160 - 2 * 160) * slot
+    d = ms.layer_desc(dict(cfg, ffn_launches=2), synth.act_global_scales(cfg))
+    assert ms.moe_workspace_bytes(d) == sizes["static"]

@@ -13,8 +13,8 @@ import oracle
 from moe_decode_step_router_gb300 import moestep as ms
 from moe_decode_step_router_gb300 import synth
 
-from gpu_util import (bf16_to_f64, check_output, expert_weights_for, host_weights, make, npy, oracle_layer, rel_l2,
-                      row_bytes, row_scales, u16, untile, untile_scales)
+from gpu_util import (bf16_to_f64, check_next_mxfp8, check_output, expert_weights_for, host_weights, make, npy,
+                      oracle_layer, rel_l2, row_bytes, row_scales, u16, untile, untile_scales)
 
 pytestmark = pytest.mark.gpu
 
@@ -195,14 +195,25 @@ def test_stages_against_oracle(name, M):
     torch.cuda.synchronize()
     assert layer.status() == 0
     assert torch.equal(hq1, t["hq"]) and torch.equal(hs1, t["hs"]) and torch.equal(y1, t["y"])
-    # ---- a7 finalize, and the whole step against the oracle's own step
+    # ---- a7 finalize (with the next layer's MXFP8 input), and the whole step against the
+    # oracle's own step
     res = inp["residual"].clone()
-    ms.moe_finalize_norm(d, t["y"], t["w"], t["inv"], M, res, inp["gamma"], t["out"], None, None, layer.ws)
+    M8 = -(-M // 8) * 8
+    oq = torch.full((M8, H), 0xAB, dtype=torch.uint8, device="cuda")
+    osc = torch.full((M8, H // 32), 0xAB, dtype=torch.uint8, device="cuda")
+    ms.moe_finalize_norm(d, t["y"], t["w"], t["inv"], M, res, inp["gamma"], t["out"], oq, osc, layer.ws)
     torch.cuda.synchronize()
     ref = oracle.step_rows(L, np.arange(M), x16, u16(inp["residual"]), u16(inp["gamma"]), wg16, bias, w13, w2, sh13,
                            sh2, logits_in=li)
     check_output(u16(t["out"]), ref["out"], "out")
     check_output(u16(res), ref["res_out"], "residual")
+    check_next_mxfp8(u16(t["out"]), npy(oq)[:M], npy(osc)[:M])
+    assert (npy(oq)[M:] == 0).all() and (npy(osc)[M:] == 0).all(), "padding rows of the 8-row tiles"
+    # without the optional output the other outputs are the same bytes
+    res2, out2 = inp["residual"].clone(), torch.zeros_like(t["out"])
+    ms.moe_finalize_norm(d, t["y"], t["w"], t["inv"], M, res2, inp["gamma"], out2, None, None, layer.ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out2, t["out"]) and torch.equal(res2, res)
 
 
 # The GEMV runs in CTAs of 4 experts x 8 rows over the whole of H. (H, E, M): one row block
@@ -270,3 +281,70 @@ def test_route_rejects_out_of_range_expert_ids():
     assert int(npy(t["nt"])[0]) == 0
     ms.moe_workspace_init(layer.d, layer.ws)
     assert layer.status() == 0
+
+
+# Ties of the selection key ("ties going to the lower index"). The GPU top-k keeps each
+# lane's candidates in registers (expert e in lane e % 32) and breaks a tie between lanes
+# by a second reduction, a tie inside a lane by its ascending scan; every case below is
+# decided by the index rule alone, and the oracle decides it by a full sort.
+def _tie_logits(M, E, k, rng):
+    lg = (rng.standard_normal((M, E)) - 3.0).astype(np.float32)
+    v = np.float32(5.0)
+    # 0: ten equal keys over several lanes, and three in one lane (2, 34, 66), straddling the k-th slot
+    lg[0, [2, 34, 66, 98, 7, 39, 11, 200, 13, 250]] = v
+    # 1: every key equal: the k lowest indices
+    lg[1, :] = np.float32(0.0)
+    # 2: different logits whose fp32 sigmoid is the same (1.0): ties by index, then the rest
+    lg[2, [40, 8, 100]] = [30.0, 25.0, 20.0]
+    # 3: six distinct leaders, then three equal keys in one lane (6, 38, 70) for the last two slots
+    lg[3, :6] = [9.0, 8.5, 8.0, 7.5, 7.0, 6.5]
+    lg[3, [70, 38, 6]] = np.float32(2.0)
+    # 4: scores of exactly zero (sigmoid underflow) fill the slots after three positive ones
+    lg[4, :] = np.float32(-200.0)
+    lg[4, [150, 3, 77]] = np.float32(1.0)
+    # 5..: random rows with every value repeated at another expert
+    for m in range(5, M):
+        src = rng.permutation(E)[: E // 2]
+        dst = rng.permutation(E)[: E // 2]
+        lg[m, dst] = lg[m, src]
+        lg[m, rng.permutation(E)[:k]] = np.float32(4.0)
+    return lg
+
+
+@pytest.mark.parametrize("E,k,bias", [(256, 8, False), (256, 8, True), (512, 10, True), (512, 10, False)])
+def test_topk_ties_go_to_the_lower_index(E, k, bias):
+    M = 12
+    cfg = synth.config("tiny_mxfp8", E=E, k=k, has_bias=bias, rsf=2.5)
+    inp, layer = make(cfg, seed=2, M=M)
+    rng = np.random.default_rng(E + k)
+    li = _tie_logits(M, E, k, rng)
+    b = None
+    if bias:
+        # equal biases keep the ties above; on row 4 two experts get equal keys from
+        # different scores: s = 0.5 (logit 0) + 0.25 and s' + (0.75 - s'), exact in fp32
+        b = np.full(E, np.float32(0.125), np.float32)
+        L0 = oracle_layer(dict(cfg, has_bias=False), inp)
+        li[4, 9] = np.float32(0.0)
+        li[4, 21] = np.float32(1.7)
+        _, sc, _, _, _ = oracle.router(L0, u16(inp["x"]), u16(inp["wg"]), logits_in=li)
+        b[9] = np.float32(0.25)
+        b[21] = np.float32(np.float32(0.75) - sc[4, 21])
+        assert np.float32(sc[4, 9] + b[9]) == np.float32(sc[4, 21] + b[21]) == np.float32(0.75)
+        assert sc[4, 9] != sc[4, 21]
+        inp["bias"] = torch.from_numpy(b).cuda()
+    t = _alloc(layer, M)
+    ms.moe_router_topk(layer.d, inp["x"], inp["wg"], inp["bias"] if bias else None, torch.from_numpy(li).cuda(), M,
+                       t["logits"], t["idx"], t["w"], t["xq"], t["xs"], t["xq_sh"], t["xs_sh"], layer.ws)
+    torch.cuda.synchronize()
+    L = oracle_layer(cfg, inp)
+    _, _, oidx, ow, _ = oracle.router(L, u16(inp["x"]), u16(inp["wg"]), bias=b, logits_in=li)
+    gidx = npy(t["idx"])
+    assert (gidx == oidx).all(), "rows %s differ" % np.nonzero((gidx != oidx).any(1))[0]
+    assert np.allclose(npy(t["w"]), ow, rtol=2 ** -20, atol=0)
+    # the cases are what they claim to be
+    if not bias:  # (with the bias, experts 9 and 21 lead row 1)
+        assert list(oidx[1]) == list(range(k))
+    assert oidx[0][:min(k, 10)].tolist() == sorted([2, 34, 66, 98, 7, 39, 11, 200, 13, 250])[:min(k, 10)]
+    assert oidx[2][:3].tolist() == [8, 40, 100]
+    if bias:
+        assert 9 in oidx[4] and 21 in oidx[4] and list(oidx[4]).index(9) < list(oidx[4]).index(21)

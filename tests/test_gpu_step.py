@@ -1,6 +1,7 @@
-"""End-to-end moe_step (five PDL-chained launches) against the oracle, in eager mode and
-under CUDA-graph replay; bitwise determinism over repeated replays; row-map invariance;
-and the full-size workloads, checked on rows the oracle computes one by one."""
+"""End-to-end moe_step (four PDL-chained launches; five with two FFN launches) against the
+oracle, in eager mode and under CUDA-graph replay; bitwise determinism over repeated
+replays; row-map invariance; and the full-size workloads, every row of each checked
+against the oracle (rows run on parallel host threads)."""
 import numpy as np
 import pytest
 import torch
@@ -8,7 +9,8 @@ import torch
 import oracle
 from moe_decode_step_router_gb300 import synth
 
-from gpu_util import check_output, expert_weights_for, host_weights, make, npy, oracle_layer, u16
+from gpu_util import (check_next_mxfp8, check_output, expert_weights_for, host_weights, make, npy, oracle_layer,
+                      oracle_step_rows_parallel, u16)
 
 pytestmark = pytest.mark.gpu
 
@@ -43,12 +45,11 @@ def _oracle_rows(cfg, inp, rows):
     L = oracle_layer(cfg, inp)
     x16, wg16 = u16(inp["x"]), u16(inp["wg"])
     bias = npy(inp["bias"])
-    sel = []
     _, _, idx, _, _ = oracle.router(L, x16[rows], wg16, bias=bias)
     w13, w2 = expert_weights_for(inp, idx.ravel())
     _, _, sh13, sh2 = host_weights(dict(inp, w13=inp["w13"], w2=inp["w2"]), 0)
-    return oracle.step_rows(L, np.asarray(rows), x16, u16(inp["residual"]), u16(inp["gamma"]), wg16, bias, w13, w2,
-                            sh13, sh2, want_q=bool(cfg.get("emit_next")))
+    return oracle_step_rows_parallel(L, rows, x16, u16(inp["residual"]), u16(inp["gamma"]), wg16, bias, w13, w2,
+                                     sh13, sh2, want_q=bool(cfg.get("emit_next")))
 
 
 def _check_rows(layer, inp, rows, out, res, oq, os_, ref):
@@ -61,22 +62,19 @@ def _check_rows(layer, inp, rows, out, res, oq, os_, ref):
     if keep.any():
         check_output(u16(out)[rows][keep], ref["out"][keep], "out")
         check_output(u16(res)[rows][keep], ref["res_out"][keep], "residual")
-        if oq is not None:
-            q, s = npy(oq)[rows][keep], npy(os_)[rows][keep]
-            eq = (q == ref["outq"][keep]).mean()
-            assert eq > 0.95, "next-layer MXFP8 codes agree on only %.3f" % eq
-            assert (np.abs(s.astype(int) - ref["outs"][keep].astype(int)) <= 1).all()
+    if oq is not None:
+        # every row, excused or not: the quantiser of the GPU's own output, bit for bit
+        check_next_mxfp8(u16(out)[rows], npy(oq)[rows], npy(os_)[rows])
 
 
 @pytest.mark.parametrize("sched", ["static", "dynamic"])
 @pytest.mark.parametrize("name", list(SMALL))
 @pytest.mark.parametrize("M", [1, 8, 23, 64])
-def test_step_matches_oracle(name, M, sched, monkeypatch):
+def test_step_matches_oracle(name, M, sched):
     # the GEMMs' work schedule (equal static ranges, items taken from a counter, or both)
     # changes only how units are cut between CTAs, never the result beyond fp32 summation
     # order
-    monkeypatch.setenv("MOE_GEMM_SCHEDULE", sched)
-    cfg = SMALL[name]
+    cfg = dict(SMALL[name], schedule=sched)
     inp, layer = make(cfg, seed=10 + M, M=M)
     out, res, oq, os_ = _run(layer, inp, M)
     rows = list(range(M))
@@ -87,11 +85,10 @@ def test_step_matches_oracle(name, M, sched, monkeypatch):
 
 
 @pytest.mark.parametrize("sched", ["static", "dynamic", "hybrid"])
-def test_graph_replay_equals_eager_and_is_deterministic(sched, monkeypatch):
+def test_graph_replay_equals_eager_and_is_deterministic(sched):
     # when items come from a counter the CTA that computes one changes from run to run;
     # the bytes must not
-    monkeypatch.setenv("MOE_GEMM_SCHEDULE", sched)
-    cfg = SMALL["nv_mx"]
+    cfg = dict(SMALL["nv_mx"], schedule=sched)
     M = 19
     inp, layer = make(cfg, seed=5, M=M)
     out_e, res_e, oq_e, os_e = _run(layer, inp, M)
@@ -126,29 +123,30 @@ def test_row_map_invariance():
     assert torch.equal(out1[p], out2) and torch.equal(res1[p], res2)
 
 
-# (workload, rows, GEMM schedule); "auto" is the default (static ranges)
-FULL = [("tiny_mxfp8", None, "auto"), ("mxfp8_h7168_e256_k8_8rows", None, "auto"),
-        ("nvfp4_h6144_e256_k8_16rows", None, "auto"), ("mxfp8_skew_48rows", None, "auto"),
-        ("nvfp4_h4096_e512_k10", 1, "auto"), ("nvfp4_h4096_e512_k10", 8, "auto"),
-        ("nvfp4_h4096_e512_k10", 64, "auto"), ("mxfp8_h7168_e256_k8_8rows", None, "hybrid"),
+# (workload, rows, GEMM schedule); "static" is the default. Every row of each is compared
+# with the oracle: at these sizes the kernels take their multi-tile, stream-K and
+# hot-expert paths.
+FULL = [("tiny_mxfp8", None, "static"), ("mxfp8_h7168_e256_k8_8rows", None, "static"),
+        ("nvfp4_h6144_e256_k8_16rows", None, "static"), ("mxfp8_skew_48rows", None, "static"),
+        ("nvfp4_h4096_e512_k10", 1, "static"), ("nvfp4_h4096_e512_k10", 8, "static"),
+        ("nvfp4_h4096_e512_k10", 16, "static"), ("nvfp4_h4096_e512_k10", 64, "static"),
+        ("mxfp8_h7168_e256_k8_8rows", None, "hybrid"),
         ("nvfp4_h6144_e256_k8_16rows", None, "dynamic"), ("nvfp4_h4096_e512_k10", 1, "dynamic"),
         ("nvfp4_h4096_e512_k10", 32, "hybrid"), ("mxfp8_h7168_e256_k8_8rows", None, "dynamic"),
-        ("mxfp4_h7168_e256_k8", None, "auto"), ("mxfp4_h7168_e256_k8", 64, "auto")]
+        ("mxfp4_h7168_e256_k8", None, "static"), ("mxfp4_h7168_e256_k8", 64, "static")]
 
 
 @pytest.mark.parametrize("name,M,sched", FULL, ids=["%s-%s-%s" % f for f in FULL])
-def test_full_size_sampled_rows(name, M, sched, monkeypatch):
-    if sched != "auto":
-        monkeypatch.setenv("MOE_GEMM_SCHEDULE", sched)
-    cfg = synth.config(name) if M is None else synth.config(name, M=M)
+def test_full_size_every_row(name, M, sched):
+    cfg = synth.config(name, schedule=sched) if M is None else synth.config(name, M=M, schedule=sched)
     M = cfg["M"]
     inp, layer = make(cfg, seed=0, M=M)
     out, res, oq, os_ = _run(layer, inp, M)
-    rows = sorted({0, M - 1, M // 2})
+    rows = list(range(M))
     ref = _oracle_rows(cfg, inp, rows)
     _check_rows(layer, inp, rows, out, res, oq, os_, ref)
-    # routing of every row vs the oracle on the GPU's own logits is checked in the stage tests;
-    # here: every row's output is finite and the skewed workload has hot experts with several tiles
+    # rows excused by a routing margin below 1e-5 are rare
+    assert (ref["margin"] >= 1e-5).mean() >= 0.9
     assert torch.isfinite(out.float()).all()
     if cfg.get("skew"):
         counts = npy(layer.ws_tensor("expert_counts", torch.int32, (cfg["E"] + 1,)))
@@ -158,10 +156,9 @@ def test_full_size_sampled_rows(name, M, sched, monkeypatch):
 
 
 @pytest.mark.parametrize("sched", ["hybrid", "dynamic"])
-def test_full_size_counter_schedules_are_deterministic(sched, monkeypatch):
+def test_full_size_counter_schedules_are_deterministic(sched):
     # these schedules hand units to whichever CTA is free first
-    monkeypatch.setenv("MOE_GEMM_SCHEDULE", sched)
-    cfg = synth.config("mxfp8_h7168_e256_k8_8rows")
+    cfg = synth.config("mxfp8_h7168_e256_k8_8rows", schedule=sched)
     M = cfg["M"]
     inp, layer = make(cfg, seed=1, M=M)
     runs = []
@@ -198,15 +195,15 @@ def test_clamped_swiglu_full_size_sampled_rows():
 
 
 # moe_step runs gate_up and down as one launch (down items wait in the kernel for their
-# group's gate_up units); MOE_FUSED_FFN=0 gives the two separate launches. Both cut the
-# same units at the same steps, so the bytes must agree exactly.
+# group's gate_up units); a layer with ffn_launches = 2 runs the two separate launches.
+# Both cut the same units at the same steps, so the bytes must agree exactly.
 @pytest.mark.parametrize("name,M", [(n, m) for n in SMALL for m in (1, 23)] + [("full", 8)])
-def test_one_launch_ffn_equals_two_launches(name, M, monkeypatch):
+def test_one_launch_ffn_equals_two_launches(name, M):
     cfg = synth.config("mxfp8_h7168_e256_k8_8rows") if name == "full" else SMALL[name]
     inp, layer = make(cfg, seed=21 + M, M=M)
-    monkeypatch.setenv("MOE_FUSED_FFN", "0")
+    layer.d.ffn_launches = 2
     two = _run(layer, inp, M)
-    monkeypatch.delenv("MOE_FUSED_FFN")
+    layer.d.ffn_launches = 1
     one = _run(layer, inp, M)
     assert torch.equal(one[0], two[0]) and torch.equal(one[1], two[1])
     if one[2] is not None:

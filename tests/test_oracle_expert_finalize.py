@@ -162,6 +162,37 @@ def test_finalize_constant_row():
     assert (res == _bf16(np.full(H, -3.0))).all()
 
 
+@pytest.mark.parametrize("H", [256, 1280])
+def test_finalize_rmsnorm_exact_mean_square(H):
+    """Rows whose mean square is exact, so RMSNorm has a closed form (moe = 0).
+
+    |residual| = 2 everywhere: mean square 4, (4 + 1e-6)^-1/2 = 0.5 (1 - 1.25e-7), and
+    out = bf16(r / 2 * gamma) = +-gamma bit for bit (the factor 1 - 1.25e-7 is far below
+    half a bf16 ulp). A wrong mean (dividing by H - 1 or H + 1) moves out by 1 / (2H),
+    which moves gamma = 1 to another bf16 value at H = 256. 3/8 of the entries +-3 and
+    5/8 +-1 also give mean square 4 (9 * 3/8 + 5/8). eps = 12 with |r| = 2 gives
+    (4 + 12)^-1/2 = 1/4 exactly: eps inside the square root."""
+    rng = np.random.default_rng(H)
+    sign = rng.choice([-1.0, 1.0], H)
+    grid = np.array([0.5, 0.75, 1.0, 1.25, 1.5, 1.75])  # 1.5 * grid and grid / 4 stay on the bf16 grid
+    gam = rng.choice(grid, H)
+    gam[:8] = 1.0
+    gamma = _bf16(gam)
+    b2f = lambda a: torch.from_numpy(a.astype(np.int16)).view(torch.bfloat16).double().numpy()
+    L = _layer(H)
+    out, res, _, _ = oracle.finalize_row(L, np.zeros(H), _bf16(2.0 * sign), gamma)
+    assert (out == _bf16(sign * gam)).all()
+    assert (res == _bf16(2.0 * sign)).all()
+    mag = np.where(rng.permutation(H) < 3 * H // 8, 3.0, 1.0)
+    assert (mag ** 2).mean() == 4.0
+    out, _, _, _ = oracle.finalize_row(L, np.zeros(H), _bf16(mag * sign), gamma)
+    assert (b2f(out) == mag * sign * 0.5 * gam).all()
+    L12 = oracle.make_layer(dict(H=H, E=4, k=2, I=32, I_sh=32, w_fmt=FMT_MXFP8, sh_fmt=FMT_MXFP8, has_bias=False,
+                                 rsf=1.0, eps=12.0))
+    out, _, _, _ = oracle.finalize_row(L12, np.zeros(H), _bf16(2.0 * sign), gamma)
+    assert (b2f(out) == sign * 0.5 * gam).all()
+
+
 def test_finalize_scale_invariance_and_residual_rounding():
     rng = np.random.default_rng(14)
     H = 512
