@@ -15,6 +15,7 @@ namespace moe {
 __global__ void k_router(RouterParams p);
 __global__ void k_router_rows(RouterParams p);
 __global__ void k_topk_route(TopkRouteParams p);
+__global__ void k_front(FrontParams f);
 __global__ void k_finalize(FinalizeParams p);
 __global__ void k_pack(PackParams p);
 __global__ void k_expert_gemm(const __grid_constant__ GemmParams p);
@@ -82,6 +83,8 @@ moe_status check_desc(const moe_layer_desc* d) {
     REQUIRE(d->gemm_schedule >= MOE_SCHED_STATIC && d->gemm_schedule <= MOE_SCHED_DYNAMIC,
             "gemm_schedule=%d: need 0 (static), 1 (hybrid) or 2 (dynamic)", d->gemm_schedule);
     REQUIRE(d->ffn_launches >= 0 && d->ffn_launches <= 2, "ffn_launches=%d: need 0, 1 or 2", d->ffn_launches);
+    REQUIRE(d->front_launches >= 0 && d->front_launches <= 2, "front_launches=%d: need 0, 1 or 2",
+            d->front_launches);
     if (d->w_fmt == MOE_FMT_NVFP4) REQUIRE(d->gs_a1 > 0.0f && d->gs_a2 > 0.0f, "NVFP4 needs gs_a1, gs_a2 > 0");
     if (d->has_shared && d->shared_fmt == MOE_FMT_NVFP4)
         REQUIRE(d->gs_a1_shared > 0.0f && d->gs_a2_shared > 0.0f, "NVFP4 shared needs gs_a1_shared, gs_a2_shared > 0");
@@ -158,7 +161,7 @@ WsLayout layout(const moe_layer_desc* d) {
     L.partials = take(4ull * partial_slots(d->gemm_schedule) * kPartialFloats);
     L.sched = take(4ull * 4);  // gate_up and down: next work item, CTAs finished
     L.gu_done = take(4ull * (kMaxE + 2));  // one launch for both GEMMs: per-group gate_up units done
-    L.tcnt = take(16);
+    L.tcnt = take(64);  // arrival counters: [0] top-k CTAs / row blocks, [4 ..) router CTAs per row block
     L.total = o;
     return L;
 }
@@ -167,6 +170,7 @@ struct DevInfo {
     int dev = -1, sms = 0, smem_optin = 0;
     bool gemm_attr_set = false;
     bool router_rows_attr_set = false;
+    bool front_attr_set = false;
 };
 thread_local DevInfo g_dev;
 
@@ -218,9 +222,8 @@ moe_status launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_
 }
 
 // ------------------------------------------------------------------ launch helpers
-moe_status launch_router(const moe_layer_desc* d, const void* x, const void* w_gate, const float* logits_in, int M,
-                         float* logits_out, float* scores, int32_t* status, cudaStream_t st,
-                         const void* l2_pf = nullptr, size_t l2_pf_bytes = 0) {
+RouterParams router_params(const moe_layer_desc* d, const void* x, const void* w_gate, const float* logits_in, int M,
+                           float* logits_out, float* scores, int32_t* status, const void* l2_pf, size_t l2_pf_bytes) {
     RouterParams p{};
     p.status = status;
     p.l2_pf = static_cast<const uint8_t*>(l2_pf);
@@ -233,21 +236,32 @@ moe_status launch_router(const moe_layer_desc* d, const void* x, const void* w_g
     p.M = M;
     p.H = d->H;
     p.E = d->E;
+    return p;
+}
+
+// Dynamic shared memory of a router CTA: its 4 gate rows and up to 8 x rows of H bf16
+// ((4 + 8) * H * 2 <= 192 KB).
+size_t router_smem(const moe_layer_desc* d, int M) { return (size_t)(4 + (M < 8 ? M : 8)) * d->H * 2; }
+
+moe_status launch_router(const moe_layer_desc* d, const void* x, const void* w_gate, const float* logits_in, int M,
+                         float* logits_out, float* scores, int32_t* status, cudaStream_t st,
+                         const void* l2_pf = nullptr, size_t l2_pf_bytes = 0) {
+    const RouterParams p = router_params(d, x, w_gate, logits_in, M, logits_out, scores, status, l2_pf, l2_pf_bytes);
     DevInfo* di;
     moe_status s = dev_info(&di);
     if (s != MOE_OK) return s;
-    // the GEMV: CTAs of 4 experts x 8 rows over the whole of H, x rows and gate rows in
-    // shared memory ((4 + 8) * H * 2 <= 192 KB, plus ~1 KB of static shared memory)
+    // the GEMV: CTAs of 4 experts x 8 rows over the whole of H (512 threads, as in k_front,
+    // so both give the same logits), x rows and gate rows in shared memory (plus ~2 KB of
+    // static shared memory)
     if (!logits_in) {
-        const size_t rsmem = (size_t)(4 + (M < 8 ? M : 8)) * d->H * 2;
         if (!di->router_rows_attr_set) {
             cudaError_t e = cudaFuncSetAttribute(k_router_rows, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 di->smem_optin - 2048);
+                                                 di->smem_optin - 4096);
             if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(k_router_rows)");
             di->router_rows_attr_set = true;
         }
-        return launch_pdl(k_router_rows, dim3((d->E + 3) / 4, (M + 7) / 8), dim3(256), rsmem, st, p,
-                          "k_router_rows launch");
+        return launch_pdl(k_router_rows, dim3((d->E + 3) / 4, (M + 7) / 8), dim3(kRouteThreads), router_smem(d, M),
+                          st, p, "k_router_rows launch");
     }
     // the logits are given: scores only
     return launch_pdl(k_router, dim3((M * d->E + 255) / 256), dim3(256), 0, st, p, "k_router launch");
@@ -268,10 +282,10 @@ int quant_units_host(int fmt, int M, int H) {
                                                           : (fmt == MOE_FMT_NVFP4 ? Mpad * (H / 16) : Mpad * (H / 8));
 }
 
-moe_status launch_topk_route(const moe_layer_desc* d, const WsLayout& L, uint8_t* ws, int M, const float* scores,
-                             const float* bias, int32_t* topk_idx, float* topk_w, int do_topk, int do_route,
-                             int32_t* counts, int32_t* perm, int32_t* inv_perm, int32_t* tiles, int32_t* num_tiles,
-                             cudaStream_t st, const QuantArgs& qa = QuantArgs()) {
+TopkRouteParams topk_params(const moe_layer_desc* d, const WsLayout& L, uint8_t* ws, int M, const float* scores,
+                            const float* bias, int32_t* topk_idx, float* topk_w, int do_topk, int do_route,
+                            int32_t* counts, int32_t* perm, int32_t* inv_perm, int32_t* tiles, int32_t* num_tiles,
+                            const QuantArgs& qa, int* qctas_out) {
     TopkRouteParams p{};
     p.scores = scores;
     p.bias = d->has_bias ? bias : nullptr;
@@ -314,10 +328,46 @@ moe_status launch_topk_route(const moe_layer_desc* d, const WsLayout& L, uint8_t
         p.gs_s = (d->has_shared && d->shared_fmt == MOE_FMT_NVFP4) ? d->gs_a1_shared : 1.0f;
         int units = quant_units_host(p.fmt_r, M, d->H);
         if (p.quant_shared && quant_units_host(p.fmt_s, M, d->H) > units) units = quant_units_host(p.fmt_s, M, d->H);
-        qctas = (units + 511) / 512;
+        qctas = (units + kRouteThreads - 1) / kRouteThreads;
     }
+    *qctas_out = qctas;
+    return p;
+}
+
+moe_status launch_topk_route(const moe_layer_desc* d, const WsLayout& L, uint8_t* ws, int M, const float* scores,
+                             const float* bias, int32_t* topk_idx, float* topk_w, int do_topk, int do_route,
+                             int32_t* counts, int32_t* perm, int32_t* inv_perm, int32_t* tiles, int32_t* num_tiles,
+                             cudaStream_t st, const QuantArgs& qa = QuantArgs()) {
+    int qctas = 0;
+    const TopkRouteParams p = topk_params(d, L, ws, M, scores, bias, topk_idx, topk_w, do_topk, do_route, counts,
+                                          perm, inv_perm, tiles, num_tiles, qa, &qctas);
     return launch_pdl(k_topk_route, dim3(p.topk_ctas + qctas), dim3(kRouteThreads), 0, st, p,
                       "k_topk_route launch");
+}
+
+// Router, top-k, routing and quantisation as one launch (k_front): the router CTAs of
+// k_router_rows, then the quantisation CTAs of k_topk_route. Its arrival counters sit in
+// the workspace's arrival region: [0] row blocks done, [4 .. 4 + ceil(M/8)) router CTAs
+// done per row block (all self-resetting).
+moe_status launch_front(const moe_layer_desc* d, const RouterParams& r, const TopkRouteParams& t, int qctas,
+                        const WsLayout& L, uint8_t* ws, int M, cudaStream_t st) {
+    DevInfo* di;
+    moe_status s = dev_info(&di);
+    if (s != MOE_OK) return s;
+    if (!di->front_attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(k_front, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             di->smem_optin - 16384);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(k_front)");
+        di->front_attr_set = true;
+    }
+    FrontParams f{};
+    f.r = r;
+    f.t = t;
+    int32_t* arrivals = reinterpret_cast<int32_t*>(ws + L.tcnt);
+    f.t.topk_arrivals = arrivals;
+    f.rb_arrivals = arrivals + 4;
+    const int nr = ((d->E + 3) / 4) * ((M + 7) / 8);
+    return launch_pdl(k_front, dim3(nr + qctas), dim3(kRouteThreads), router_smem(d, M), st, f, "k_front launch");
 }
 
 struct GemmBuffers {
@@ -812,19 +862,30 @@ moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void
     const size_t sh13_bytes = d->has_shared ? (size_t)(2 * d->I_shared / kBlockRows) *
                                                   steps_of(d->shared_fmt, d->H) * record_bytes(d->shared_fmt)
                                             : 0;
-    s = launch_router(d, a->x, a->w_gate, nullptr, M, logits, scores, reinterpret_cast<int32_t*>(w + L.header), st,
-                      d->has_shared ? a->sh13.packed : nullptr, sh13_bytes);
-    if (s != MOE_OK) return s;
     QuantArgs qa;
     qa.x = a->x;
     qa.xq = w + L.xq;
     qa.xs = w + L.xs;
     qa.xq_sh = w + L.xq_sh;
     qa.xs_sh = w + L.xs_sh;
-    s = launch_topk_route(d, L, w, M, scores, a->bias, topk_idx, topk_w, 1, 1,
-                          reinterpret_cast<int32_t*>(w + L.counts), perm, inv_perm,
-                          reinterpret_cast<int32_t*>(w + L.tiles), reinterpret_cast<int32_t*>(w + L.num_tiles), st, qa);
-    if (s != MOE_OK) return s;
+    const RouterParams rp = router_params(d, a->x, a->w_gate, nullptr, M, logits, scores,
+                                          reinterpret_cast<int32_t*>(w + L.header),
+                                          d->has_shared ? a->sh13.packed : nullptr, sh13_bytes);
+    int qctas = 0;
+    const TopkRouteParams tp = topk_params(d, L, w, M, scores, a->bias, topk_idx, topk_w, 1, 1,
+                                           reinterpret_cast<int32_t*>(w + L.counts), perm, inv_perm,
+                                           reinterpret_cast<int32_t*>(w + L.tiles),
+                                           reinterpret_cast<int32_t*>(w + L.num_tiles), qa, &qctas);
+    if (d->front_launches != 2) {
+        s = launch_front(d, rp, tp, qctas, L, w, M, st);
+        if (s != MOE_OK) return s;
+    } else {
+        s = launch_router(d, a->x, a->w_gate, nullptr, M, logits, scores, reinterpret_cast<int32_t*>(w + L.header), st,
+                          d->has_shared ? a->sh13.packed : nullptr, sh13_bytes);
+        if (s != MOE_OK) return s;
+        s = launch_pdl(k_topk_route, dim3(tp.topk_ctas + qctas), dim3(kRouteThreads), 0, st, tp, "k_topk_route launch");
+        if (s != MOE_OK) return s;
+    }
     GemmBuffers b{};
     b.xq = w + L.xq;
     b.xs = w + L.xs;

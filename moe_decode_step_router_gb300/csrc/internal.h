@@ -114,6 +114,15 @@ struct TopkRouteParams {
     float gs_r, gs_s;
 };
 
+// k_front: the router launch's and the top-k launch's parameters, plus the per-row-block
+// arrival counters of the router CTAs ([ceil(M/8)], self-resetting); t.topk_arrivals counts
+// the row blocks whose top-k is done.
+struct FrontParams {
+    RouterParams r;
+    TopkRouteParams t;
+    int32_t* rb_arrivals;
+};
+
 struct GemmClass {            // one weight class: routed experts or the shared expert
     int fmt;                  // weight / activation format
     const uint8_t* w;         // packed records

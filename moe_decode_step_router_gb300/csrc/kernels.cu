@@ -167,23 +167,27 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(RouterParams p) {
 // and rows R j .. R j + R - 1 over the whole of H. Their gate rows are copied into shared
 // memory (one bulk copy per row) before the dependency wait (they do not depend on earlier
 // launches), the x rows (one bulk copy) after it. Thread t takes the 16-byte chunks
-// t, t + 256, ... of H for all EPC x R (expert, row) dot products; a warp then folds
+// t, t + NW * 32, ... of H for all EPC x R (expert, row) dot products; a warp then folds
 // its 32 partial sums by recursive halving, so that lane l ends with the warp's sum for
-// output l = expert * R + row, and thread l adds the 8 warps' sums in warp order. The order
-// of every addition is fixed: the logits are deterministic. The score is the same fp32
-// sigmoid as in k_router (evaluated in double, rounded once).
+// output l = expert * R + row, and thread l adds the NW warps' sums in warp order. The
+// order of every addition is fixed: the logits are deterministic, and the same in both
+// launches that run this (k_router_rows and k_front, both at NW = 16). The score is the
+// same fp32 sigmoid as in k_router (evaluated in double, rounded once).
+// (ei, rj): this CTA's expert group and row block; CTA cta of nct takes its share of the L2
+// prefetch. Returns false when a copy wait ran out (recorded in the status word; nothing
+// is written).
 constexpr uint64_t kRouterWaitNs = 2000000000ull;  // 2 s: limit of the router's copy waits
 
-template <int EPC, int R>
-__device__ __forceinline__ void router_rows(const RouterParams& p) {
+template <int EPC, int R, int NW>
+__device__ __forceinline__ bool router_rows(const RouterParams& p, int ei, int rj, int cta, int nct) {
     static_assert(EPC * R == 32, "one output per lane");
     extern __shared__ __align__(16) uint16_t rrs[];
-    __shared__ float red[kRouterThreads / 32][32];
+    __shared__ float red[NW][32];
     __shared__ __align__(8) uint64_t rbar[2];  // gate rows, x rows
     __shared__ int s_never;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int H = p.H, E = p.E;
-    const int e0 = blockIdx.x * EPC, m0 = blockIdx.y * R;
+    const int e0 = ei * EPC, m0 = rj * R;
     const int M = min(R, p.M - m0);          // rows of this CTA
     const int V = H / 8;                     // 16-byte chunks per row
     uint16_t* wsm = rrs;                     // [EPC][H]
@@ -200,9 +204,8 @@ __device__ __forceinline__ void router_rows(const RouterParams& p) {
     }
     __syncthreads();  // the barriers are initialised before anyone waits on them
     if (p.l2_pf && threadIdx.x == 32) {
-        const size_t nct = (size_t)gridDim.x * gridDim.y, cta = (size_t)blockIdx.y * gridDim.x + blockIdx.x;
-        const size_t share = (p.l2_pf_bytes / nct + 15) & ~(size_t)15;
-        const size_t b0 = cta * share, b1 = b0 + share < p.l2_pf_bytes ? b0 + share : p.l2_pf_bytes;
+        const size_t share = (p.l2_pf_bytes / (size_t)nct + 15) & ~(size_t)15;
+        const size_t b0 = (size_t)cta * share, b1 = b0 + share < p.l2_pf_bytes ? b0 + share : p.l2_pf_bytes;
         for (size_t o = b0; o < b1; o += 65536)
             prefetch_l2(p.l2_pf + o, (uint32_t)(b1 - o < 65536 ? b1 - o : 65536));
     }
@@ -219,7 +222,7 @@ __device__ __forceinline__ void router_rows(const RouterParams& p) {
         if (threadIdx.x == 0 && p.status) atomicCAS(p.status, 0, (int)MOE_ERR_TIMEOUT);
         mbar_wait_bounded(bar_w, 0, &s_never, kRouterWaitNs / 2);
         mbar_wait_bounded(bar_x, 0, &s_never, kRouterWaitNs / 2);
-        return;
+        return false;
     }
     float acc[32];
 #pragma unroll
@@ -263,15 +266,19 @@ __device__ __forceinline__ void router_rows(const RouterParams& p) {
         const int e = e0 + threadIdx.x / R, m = threadIdx.x % R;
         float lg = red[0][threadIdx.x];
 #pragma unroll
-        for (int w = 1; w < kRouterThreads / 32; ++w) lg += red[w][threadIdx.x];
+        for (int w = 1; w < NW; ++w) lg += red[w][threadIdx.x];
         if (m < M && e < E) {
             p.scores[(size_t)(m0 + m) * E + e] = (float)(1.0 / (1.0 + exp(-(double)lg)));
             if (p.logits_out) p.logits_out[(size_t)(m0 + m) * E + e] = lg;
         }
     }
+    return true;
 }
 
-__global__ void __launch_bounds__(kRouterThreads) k_router_rows(RouterParams p) { router_rows<4, 8>(p); }
+__global__ void __launch_bounds__(kRouteThreads) k_router_rows(RouterParams p) {
+    router_rows<4, 8, kRouteThreads / 32>(p, blockIdx.x, blockIdx.y, blockIdx.y * gridDim.x + blockIdx.x,
+                                          gridDim.x * gridDim.y);
+}
 
 // ------------------------------------------------------------------------------------
 // a2 + a4: top-k of the selection key (score + bias) with ties to the lower expert index
@@ -315,150 +322,103 @@ __device__ __forceinline__ void block_scan4(int4 v, int4* out_excl, int4* total,
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(kRouteThreads) k_topk_route(TopkRouteParams p) {
-    __shared__ unsigned long long sel[kMaxE + 1];
-    __shared__ int s_topk[kMaxRows * kMaxK];  // this CTA's selections, when it also routes
-    __shared__ int4 sh_warp[32];
-    __shared__ int s_bad, s_last;
-    pdl_wait();
-    pdl_trigger();  // the GEMM's CTAs may take the other SMs and wait there
-    const int tk = p.topk_ctas;
-    if ((int)blockIdx.x >= tk) {
-        // a3: the FC1 input quantisation, on the CTAs after the top-k ones
-        const int Mpad = round_up(p.M, 16);
-        const int nthreads = (gridDim.x - tk) * blockDim.x, tid = (blockIdx.x - tk) * blockDim.x + threadIdx.x;
-        const int nr = quant_units(p.fmt_r, Mpad, p.H);
-        for (int u = tid; u < nr; u += nthreads) quant_unit(p.x, p.M, p.H, Mpad, p.fmt_r, p.gs_r, p.xq, p.xs, u);
-        if (p.quant_shared) {
-            const int ns = quant_units(p.fmt_s, Mpad, p.H);
-            for (int u = tid; u < ns; u += nthreads)
-                quant_unit(p.x, p.M, p.H, Mpad, p.fmt_s, p.gs_s, p.xq_sh, p.xs_sh, u);
-        }
-        return;
-    }
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int M = p.M, E = p.E, k = p.k;
-    // without a workspace a router timeout has no status word to go to: its scores were
-    // never written, so every row gets -1 ids and zero weights instead of stale results
-    const bool router_failed = p.router_status && __ldcg(p.router_status) != 0;
-    if (p.do_topk && router_failed) {
-        for (int q = (int)blockIdx.x * blockDim.x + threadIdx.x; q < M * k; q += tk * blockDim.x) {
-            p.topk_idx[q] = -1;
-            p.topk_w[q] = 0.0f;
-        }
-    }
-    if (p.router_status) {
-        // the last top-k CTA to read the record clears it for the next call
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            bool last = true;
-            if (tk > 1) {
-                __threadfence();
-                last = atomicAdd(p.topk_arrivals, 1) == tk - 1;
-                if (last) *p.topk_arrivals = 0;
-            }
-            if (last && router_failed) *p.router_status = 0;
-        }
-        if (router_failed) return;
-    }
-    if (p.do_topk) {
-        for (int m = (int)blockIdx.x * (kRouteThreads / 32) + warp; m < M; m += tk * (kRouteThreads / 32)) {
-            // keys as order-preserving u32 (0 = taken / absent); lane owns e = lane + 32 i
-            uint32_t ku[kMaxE / 32];
-            float sc[kMaxE / 32], bi[kMaxE / 32];
-            // unconditional (clamped) loads of the row's scores and of the bias, all in
-            // flight before the first use
+// a2: the top-k of row m by one warp (the warp's lanes hold experts lane + 32 i); writes
+// topk_idx / topk_w of the row and, when s_topk is given, the ids into it too.
+__device__ __forceinline__ void topk_row(const TopkRouteParams& p, int m, int lane, int* s_topk) {
+    const int E = p.E, k = p.k;
+    // keys as order-preserving u32 (0 = taken / absent); lane owns e = lane + 32 i
+    uint32_t ku[kMaxE / 32];
+    float sc[kMaxE / 32], bi[kMaxE / 32];
+    // unconditional (clamped) loads of the row's scores and of the bias, all in flight
+    // before the first use
 #pragma unroll
-            for (int i = 0; i < kMaxE / 32; ++i) sc[i] = __ldcg(p.scores + (size_t)m * E + min(lane + 32 * i, E - 1));
-            if (p.bias) {
+    for (int i = 0; i < kMaxE / 32; ++i) sc[i] = __ldcg(p.scores + (size_t)m * E + min(lane + 32 * i, E - 1));
+    if (p.bias) {
 #pragma unroll
-                for (int i = 0; i < kMaxE / 32; ++i) bi[i] = __ldg(p.bias + min(lane + 32 * i, E - 1));
-            }
+        for (int i = 0; i < kMaxE / 32; ++i) bi[i] = __ldg(p.bias + min(lane + 32 * i, E - 1));
+    }
 #pragma unroll
-            for (int i = 0; i < kMaxE / 32; ++i) {
-                const bool valid = lane + 32 * i < E;
-                ku[i] = valid ? key_u32(p.bias ? __fadd_rn(sc[i], bi[i]) : sc[i]) : 0u;
-                if (!valid) sc[i] = 0.0f;
-            }
-            // this lane's best: largest key, lowest index among equals (ascending scan)
-            uint32_t lb = 0u;
-            int li = 0;
-            float ls = 0.0f;
+    for (int i = 0; i < kMaxE / 32; ++i) {
+        const bool valid = lane + 32 * i < E;
+        ku[i] = valid ? key_u32(p.bias ? __fadd_rn(sc[i], bi[i]) : sc[i]) : 0u;
+        if (!valid) sc[i] = 0.0f;
+    }
+    // this lane's best: largest key, lowest index among equals (ascending scan)
+    uint32_t lb = 0u;
+    int li = 0;
+    float ls = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kMaxE / 32; ++i)
+        if (ku[i] > lb) { lb = ku[i]; li = i; ls = sc[i]; }
+    int my_idx = 0;
+    float my_sc = 0.0f;
+    float ssum = 0.0f;  // fp32 in slot order: FP64 is ~50x slower than fp32 on this part
+    // Each round: one max reduction and one ballot find the winning lane (a tie between
+    // lanes, which needs the lower expert id, takes one more reduction); the winner
+    // rescans its own keys while the others read its id and score.
+    for (int j = 0; j < k; ++j) {
+        const uint32_t wmax = __reduce_max_sync(0xffffffffu, lb);
+        const uint32_t bal = __ballot_sync(0xffffffffu, lb == wmax);
+        int wl;
+        if ((bal & (bal - 1u)) == 0u) {
+            wl = __ffs(bal) - 1;
+        } else {
+            const uint32_t cand = (lb == wmax) ? (uint32_t)(lane + 32 * li) : 0xffffffffu;
+            wl = (int)(__reduce_min_sync(0xffffffffu, cand) & 31u);
+        }
+        const int wsl = __shfl_sync(0xffffffffu, li, wl);
+        const float wsc = __shfl_sync(0xffffffffu, ls, wl);
+        if (lane == wl) {
+#pragma unroll
+            for (int i = 0; i < kMaxE / 32; ++i)
+                if (i == li) ku[i] = 0u;
+            lb = 0u;
+            li = 0;
+            ls = 0.0f;
 #pragma unroll
             for (int i = 0; i < kMaxE / 32; ++i)
                 if (ku[i] > lb) { lb = ku[i]; li = i; ls = sc[i]; }
-            int my_idx = 0;
-            float my_sc = 0.0f;
-            float ssum = 0.0f;  // fp32 in slot order: FP64 is ~50x slower than fp32 on this part
-            // Each round: one max reduction and one ballot find the winning lane (a tie
-            // between lanes, which needs the lower expert id, takes one more reduction);
-            // the winner rescans its own keys while the others read its id and score.
-            for (int j = 0; j < k; ++j) {
-                const uint32_t wmax = __reduce_max_sync(0xffffffffu, lb);
-                const uint32_t bal = __ballot_sync(0xffffffffu, lb == wmax);
-                int wl;
-                if ((bal & (bal - 1u)) == 0u) {
-                    wl = __ffs(bal) - 1;
-                } else {
-                    const uint32_t cand = (lb == wmax) ? (uint32_t)(lane + 32 * li) : 0xffffffffu;
-                    wl = (int)(__reduce_min_sync(0xffffffffu, cand) & 31u);
-                }
-                const int wsl = __shfl_sync(0xffffffffu, li, wl);
-                const float wsc = __shfl_sync(0xffffffffu, ls, wl);
-                if (lane == wl) {
-#pragma unroll
-                    for (int i = 0; i < kMaxE / 32; ++i)
-                        if (i == li) ku[i] = 0u;
-                    lb = 0u;
-                    li = 0;
-                    ls = 0.0f;
-#pragma unroll
-                    for (int i = 0; i < kMaxE / 32; ++i)
-                        if (ku[i] > lb) { lb = ku[i]; li = i; ls = sc[i]; }
-                }
-                ssum = __fadd_rn(ssum, wsc);
-                if (lane == j) { my_idx = wl + 32 * wsl; my_sc = wsc; }
-            }
-            if (lane < k) {
-                p.topk_idx[(size_t)m * k + lane] = my_idx;
-                s_topk[m * k + lane] = my_idx;
-                p.topk_w[(size_t)m * k + lane] =
-                    p.renormalize ? __fmul_rn(__fdiv_rn(my_sc, ssum), p.rsf) : __fmul_rn(my_sc, p.rsf);
-            }
         }
-        __syncthreads();
+        ssum = __fadd_rn(ssum, wsc);
+        if (lane == j) { my_idx = wl + 32 * wsl; my_sc = wsc; }
     }
-    if (!p.do_route) return;
-    if (tk > 1) {
-        // the last top-k CTA to finish routes every row (the others' rows through L2)
-        __threadfence();
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            const int old = atomicAdd(p.topk_arrivals, 1);
-            s_last = (old == tk - 1) ? 1 : 0;
-            if (s_last) *p.topk_arrivals = 0;  // every CTA has arrived: ready for the next launch
-        }
-        __syncthreads();
-        if (!s_last) return;
-        __threadfence();
+    if (lane < k) {
+        p.topk_idx[(size_t)m * k + lane] = my_idx;
+        if (s_topk) s_topk[m * k + lane] = my_idx;
+        p.topk_w[(size_t)m * k + lane] =
+            p.renormalize ? __fmul_rn(__fdiv_rn(my_sc, ssum), p.rsf) : __fmul_rn(my_sc, p.rsf);
     }
-    // ---- route
+}
+
+// Shared memory of the routing CTA.
+struct RouteSmem {
+    unsigned long long sel[kMaxE + 1];  // per expert: bit m set when row m selected it
+    int s_off[kMaxE + 2];               // per expert: first position in perm
+    int4 sh_warp[32];
+    int s_bad;
+};
+
+// a4 by one CTA of kRouteThreads threads: the stable counting sort of the M*k selections
+// into 8-row tiles, perm / inv_perm and the group table. own_topk: the selections, when
+// this CTA made them all (shared memory); else they are read through L2.
+__device__ void route_all(const TopkRouteParams& p, const int* own_topk, RouteSmem& rs) {
+    const int M = p.M, E = p.E, k = p.k;
+    unsigned long long* sel = rs.sel;
+    int* s_off = rs.s_off;
     const int P = M * k;
-    if (threadIdx.x == 0) s_bad = 0;
+    if (threadIdx.x == 0) rs.s_bad = 0;
     for (int e = threadIdx.x; e <= E; e += blockDim.x) sel[e] = 0ull;
     __syncthreads();
-    // the selections: this CTA's own (shared memory) when it took every row, else through L2
-    const bool own = p.do_topk && tk == 1;
     for (int q = threadIdx.x; q < P; q += blockDim.x) {
-        const int e = own ? s_topk[q] : __ldcg(p.topk_idx + q);
+        const int e = own_topk ? own_topk[q] : __ldcg(p.topk_idx + q);
         if (e < 0 || e >= E) {
-            s_bad = 1;
+            rs.s_bad = 1;
         } else {
             atomicOr(&sel[e], 1ull << (q / k));
         }
     }
     __syncthreads();
-    if (s_bad) {
+    if (rs.s_bad) {
         if (threadIdx.x == 0) {
             atomicCAS(&p.hdr->status, 0, (int)MOE_ERR_INVALID_ARG);
             p.hdr->num_groups = 0;
@@ -479,8 +439,7 @@ __global__ void __launch_bounds__(kRouteThreads) k_topk_route(TopkRouteParams p)
     const int e0 = 2 * threadIdx.x;
     const int4 v0 = vals(e0), v1 = vals(e0 + 1);
     int4 ex, tot;
-    block_scan4(make_int4(v0.x + v1.x, v0.y + v1.y, v0.z + v1.z, v0.w + v1.w), &ex, &tot, sh_warp);
-    __shared__ int s_off[kMaxE + 2];
+    block_scan4(make_int4(v0.x + v1.x, v0.y + v1.y, v0.z + v1.z, v0.w + v1.w), &ex, &tot, rs.sh_warp);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const int e = e0 + h;
@@ -506,7 +465,7 @@ __global__ void __launch_bounds__(kRouteThreads) k_topk_route(TopkRouteParams p)
     }
     __syncthreads();
     for (int q = threadIdx.x; q < P; q += blockDim.x) {
-        const int ee = own ? s_topk[q] : __ldcg(p.topk_idx + q), m = q / k;
+        const int ee = own_topk ? own_topk[q] : __ldcg(p.topk_idx + q), m = q / k;
         const unsigned long long below = (m == 0) ? 0ull : (sel[ee] & ((1ull << m) - 1ull));
         const int pos = s_off[ee] + __popcll(below);
         p.perm[pos] = q;
@@ -517,6 +476,130 @@ __global__ void __launch_bounds__(kRouteThreads) k_topk_route(TopkRouteParams p)
             p.perm[P + m] = P + m;
             p.inv_perm[P + m] = P + m;
         }
+}
+
+// a3: the FC1 input quantisation, spread over CTAs [0, ncta) of a group (cta: this one).
+__device__ void quant_all(const TopkRouteParams& p, int cta, int ncta) {
+    const int Mpad = round_up(p.M, 16);
+    const int nthreads = ncta * blockDim.x, tid = cta * blockDim.x + threadIdx.x;
+    const int nr = quant_units(p.fmt_r, Mpad, p.H);
+    for (int u = tid; u < nr; u += nthreads) quant_unit(p.x, p.M, p.H, Mpad, p.fmt_r, p.gs_r, p.xq, p.xs, u);
+    if (p.quant_shared) {
+        const int ns = quant_units(p.fmt_s, Mpad, p.H);
+        for (int u = tid; u < ns; u += nthreads) quant_unit(p.x, p.M, p.H, Mpad, p.fmt_s, p.gs_s, p.xq_sh, p.xs_sh, u);
+    }
+}
+
+__global__ void __launch_bounds__(kRouteThreads) k_topk_route(TopkRouteParams p) {
+    __shared__ RouteSmem rs;
+    __shared__ int s_topk[kMaxRows * kMaxK];  // this CTA's selections, when it also routes
+    __shared__ int s_last;
+    pdl_wait();
+    pdl_trigger();  // the GEMM's CTAs may take the other SMs and wait there
+    const int tk = p.topk_ctas;
+    if ((int)blockIdx.x >= tk) {  // the CTAs after the top-k ones quantise x
+        quant_all(p, blockIdx.x - tk, gridDim.x - tk);
+        return;
+    }
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int M = p.M, k = p.k;
+    // without a workspace a router timeout has no status word to go to: its scores were
+    // never written, so every row gets -1 ids and zero weights instead of stale results
+    const bool router_failed = p.router_status && __ldcg(p.router_status) != 0;
+    if (p.do_topk && router_failed) {
+        for (int q = (int)blockIdx.x * blockDim.x + threadIdx.x; q < M * k; q += tk * blockDim.x) {
+            p.topk_idx[q] = -1;
+            p.topk_w[q] = 0.0f;
+        }
+    }
+    if (p.router_status) {
+        // the last top-k CTA to read the record clears it for the next call
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            bool last = true;
+            if (tk > 1) {
+                __threadfence();
+                last = atomicAdd(p.topk_arrivals, 1) == tk - 1;
+                if (last) *p.topk_arrivals = 0;
+            }
+            if (last && router_failed) *p.router_status = 0;
+        }
+        if (router_failed) return;
+    }
+    if (p.do_topk) {
+        for (int m = (int)blockIdx.x * (kRouteThreads / 32) + warp; m < M; m += tk * (kRouteThreads / 32))
+            topk_row(p, m, lane, s_topk);
+        __syncthreads();
+    }
+    if (!p.do_route) return;
+    if (tk > 1) {
+        // the last top-k CTA to finish routes every row (the others' rows through L2)
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const int old = atomicAdd(p.topk_arrivals, 1);
+            s_last = (old == tk - 1) ? 1 : 0;
+            if (s_last) *p.topk_arrivals = 0;  // every CTA has arrived: ready for the next launch
+        }
+        __syncthreads();
+        if (!s_last) return;
+        __threadfence();
+    }
+    route_all(p, (p.do_topk && tk == 1) ? s_topk : nullptr, rs);
+}
+
+// ------------------------------------------------------------------------------------
+// a1 + a2 + a3 + a4 in one launch (Qwen3.5 slot table of the "SGLang-NVIDIA-Mega" README,
+// row route: the router GEMM and the quantisation of the MoE input in one launch; here the
+// top-k and the routing join them). CTAs [0, nE * nRB) are the router's (CTA i: expert
+// group i % nE, row block i / nE, as k_router_rows); the last of a row block's router CTAs
+// to finish takes that block's rows' top-k (one warp per row), and the last row block to
+// finish routes every row; the CTAs after the router ones quantise x. No CTA waits for
+// another (arrival counters only), so the launch needs no co-residency, and its logits,
+// selections and routing are the bytes of the router launch followed by the top-k launch.
+__global__ void __launch_bounds__(kRouteThreads, 1) k_front(FrontParams f) {
+    __shared__ RouteSmem rs;
+    __shared__ int s_topk[kMaxRows * kMaxK];
+    __shared__ int s_last;
+    const RouterParams& r = f.r;
+    const TopkRouteParams& t = f.t;
+    const int nE = (r.E + 3) / 4, nRB = (r.M + 7) / 8, nr = nE * nRB;
+    if ((int)blockIdx.x >= nr) {
+        pdl_wait();
+        pdl_trigger();
+        quant_all(t, blockIdx.x - nr, gridDim.x - nr);
+        return;
+    }
+    const int rj = blockIdx.x / nE;
+    if (!router_rows<4, 8, kRouteThreads / 32>(r, blockIdx.x % nE, rj, blockIdx.x, nr)) return;
+    // the last router CTA of the row block takes its rows' top-k (the other CTAs' scores
+    // through L2)
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const int old = atomicAdd(f.rb_arrivals + rj, 1);
+        s_last = (old == nE - 1) ? 1 : 0;
+        if (s_last) f.rb_arrivals[rj] = 0;  // every CTA of the block has arrived
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, m = 8 * rj + warp;
+    if (warp < 8 && m < r.M) topk_row(t, m, lane, s_topk);
+    __threadfence();  // this block's selections, before its arrival below
+    __syncthreads();
+    if (nRB > 1) {
+        // the last row block to finish routes every row
+        if (threadIdx.x == 0) {
+            const int old = atomicAdd(t.topk_arrivals, 1);
+            s_last = (old == nRB - 1) ? 1 : 0;
+            if (s_last) *t.topk_arrivals = 0;
+        }
+        __syncthreads();
+        if (!s_last) return;
+        __threadfence();
+    }
+    route_all(t, nRB == 1 ? s_topk : nullptr, rs);
 }
 
 // ------------------------------------------------------------------------------------

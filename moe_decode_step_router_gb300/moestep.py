@@ -42,7 +42,8 @@ class LayerDesc(ctypes.Structure):
                 ("emit_next_mxfp8", ctypes.c_int32), ("routed_scaling_factor", ctypes.c_float),
                 ("rms_eps", ctypes.c_float), ("gs_a1", ctypes.c_float), ("gs_a2", ctypes.c_float),
                 ("gs_a1_shared", ctypes.c_float), ("gs_a2_shared", ctypes.c_float),
-                ("swiglu_limit", ctypes.c_float), ("gemm_schedule", ctypes.c_int32), ("ffn_launches", ctypes.c_int32)]
+                ("swiglu_limit", ctypes.c_float), ("gemm_schedule", ctypes.c_int32), ("ffn_launches", ctypes.c_int32),
+                ("front_launches", ctypes.c_int32)]
 
 
 class QWeight(ctypes.Structure):
@@ -129,13 +130,14 @@ def _check(st):
 
 
 def layer_desc(cfg, gs_a=(1.0, 1.0, 1.0, 1.0)) -> LayerDesc:
-    """The layer descriptor of a workload dict; `schedule` ("static", "hybrid", "dynamic")
-    and `ffn_launches` (1 or 2) are the optional execution choices."""
+    """The layer descriptor of a workload dict; `schedule` ("static", "hybrid", "dynamic"),
+    `ffn_launches` and `front_launches` (1 or 2) are the optional execution choices."""
     return LayerDesc(cfg["H"], cfg["E"], cfg["k"], cfg["I"], cfg["I_sh"], cfg["w_fmt"], cfg["sh_fmt"],
                      int(cfg.get("has_shared", True)), int(cfg["has_bias"]), int(cfg.get("renormalize", True)),
                      int(cfg.get("emit_next", False)), float(cfg["rsf"]), float(cfg["eps"]), float(gs_a[0]),
                      float(gs_a[1]), float(gs_a[2]), float(gs_a[3]), float(cfg.get("swiglu_limit", 0.0)),
-                     SCHEDULES[cfg.get("schedule", "static")], int(cfg.get("ffn_launches", 1)))
+                     SCHEDULES[cfg.get("schedule", "static")], int(cfg.get("ffn_launches", 1)),
+                     int(cfg.get("front_launches", 1)))
 
 
 def qweight(packed, gs=None) -> QWeight:

@@ -55,7 +55,7 @@ def test_sizes(lib):
     ("I", 300, ms.MOE_ERR_INVALID_ARG), ("w_fmt", ms.MOE_FMT_BF16, ms.MOE_ERR_UNSUPPORTED),
     ("shared_fmt", 7, ms.MOE_ERR_UNSUPPORTED), ("swiglu_limit", float("nan"), ms.MOE_ERR_INVALID_ARG),
     ("gemm_schedule", 3, ms.MOE_ERR_INVALID_ARG), ("gemm_schedule", -1, ms.MOE_ERR_INVALID_ARG),
-    ("ffn_launches", 3, ms.MOE_ERR_INVALID_ARG)])
+    ("ffn_launches", 3, ms.MOE_ERR_INVALID_ARG), ("front_launches", -1, ms.MOE_ERR_INVALID_ARG)])
 def test_bad_descriptor_rejected(lib, field, value, status):
     d = _desc()
     setattr(d, field, value)

@@ -208,3 +208,25 @@ def test_one_launch_ffn_equals_two_launches(name, M):
     assert torch.equal(one[0], two[0]) and torch.equal(one[1], two[1])
     if one[2] is not None:
         assert torch.equal(one[2], two[2]) and torch.equal(one[3], two[3])
+
+
+# moe_step runs the router, the top-k, the routing and the FC1 input quantisation as one
+# launch (the last router CTA of an 8-row block takes its rows' top-k, the last block
+# routes); a layer with front_launches = 2 runs the router launch and the top-k / routing
+# launch. Same arithmetic in the same order: the same bytes, at every row count (one row
+# block, several, and the 512-expert layer's 128 router CTAs per block).
+@pytest.mark.parametrize("name,M", [(n, m) for n in SMALL for m in (1, 23, 64)] + [("full", 8), ("full512", 16)])
+def test_one_launch_front_equals_two_launches(name, M):
+    cfg = (synth.config("mxfp8_h7168_e256_k8_8rows") if name == "full" else
+           synth.config("nvfp4_h4096_e512_k10", M=M) if name == "full512" else SMALL[name])
+    inp, layer = make(cfg, seed=31 + M, M=M)
+    layer.d.front_launches = 2
+    two = _run(layer, inp, M)
+    idx2 = layer.ws_tensor("topk_idx", torch.int32, (M, cfg["k"])).clone()
+    layer.d.front_launches = 1
+    one = _run(layer, inp, M)
+    idx1 = layer.ws_tensor("topk_idx", torch.int32, (M, cfg["k"]))
+    assert torch.equal(idx1, idx2)
+    assert torch.equal(one[0], two[0]) and torch.equal(one[1], two[1])
+    if one[2] is not None:
+        assert torch.equal(one[2], two[2]) and torch.equal(one[3], two[3])
