@@ -912,6 +912,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             // 0 only (the sum is bank 0 + bank 1, in that order)
             const uint32_t t_row = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(ab * p.Mpad);
             const bool two = it.kb - it.ka >= 2;
+            // the NVFP4 global scales (weight x activation): loaded before the accumulator,
+            // so that the load's latency overlaps the tensor-memory loads
+            const float alpha = C.gs_w ? __ldg(C.gs_w + expert) * C.gs_a : 1.0f;
+            // routed gate_up: the group's tokens (its rows' positions in x), loaded early too
+            const int tok = (it.cls == 0 && et < rows) ? __ldg(p.perm + perm_off + et) / p.k : 0;
+            if (gm == 1 && it.np == 1) {
+                // a whole down unit: each thread writes its output feature (weight row r) of
+                // every row of the group straight from the accumulator, with no staging and
+                // no barrier; the same arithmetic as the staged path (bank 0 + bank 1, then
+                // the scales)
+                float* yb = p.y + (size_t)perm_off * p.H + kBlockRows * it.b + r;
+                for (int c0 = 0; c0 < N; c0 += 16) {
+                    uint32_t v0[16], v1[16];
+                    tmem_ld16_nowait(t_row + (uint32_t)c0, v0);
+                    if (two) tmem_ld16_nowait(t_row + (uint32_t)bank + (uint32_t)c0, v1);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float a = two ? __uint_as_float(v0[i]) + __uint_as_float(v1[i]) : __uint_as_float(v0[i]);
+                        if (c0 + i < rows) yb[(size_t)(c0 + i) * p.H] = a * alpha;
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sm.acc_empty[ab]));
+                if (++ab == nacc) ab = 0;
+                continue;
+            }
             for (int c0 = 0; c0 < N; c0 += 16) {
                 uint32_t v0[16], v1[16];
                 if (two) {
@@ -935,7 +963,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             // compact the selected columns: column of group row rg -> stg[rg][r]; the
             // group's tokens are read once (in parallel) into shared memory
             if (it.cls == 0) {
-                if (et < rows) sm.tok[et] = p.perm[perm_off + et] / p.k;
+                if (et < rows) sm.tok[et] = tok;
                 named_bar(1, 128);
                 for (int rg = 0; rg < rows; ++rg) {
                     const int m = sm.tok[rg];
@@ -989,7 +1017,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             }
             named_bar(1, 128);
             // ---- final epilogue
-            const float alpha = C.gs_w ? C.gs_w[expert] * C.gs_a : 1.0f;
             if (gm == 0) {
                 // SwiGLU on (gate, up) = rows (fi, fi + 64); warps take 32 features each
                 const int fi = 32 * (ew & 1) + lane;
