@@ -105,11 +105,11 @@ typedef enum { MOE_SCHED_STATIC = 0, MOE_SCHED_HYBRID = 1, MOE_SCHED_DYNAMIC = 2
  * Execution choices, fixed when the layer is set up (the pages' engines choose their
  * kernels and tactics at load, "SGLang-NVIDIA-Mega" README, Design): gemm_schedule is a
  * moe_schedule (0 = STATIC); ffn_launches is 0 or 1 for gate_up and down in one launch in
- * moe_step (the default), 2 for two launches; front_launches is 0 or 1 for the router, the
- * top-k, the routing and the FC1 input quantisation in one launch in moe_step (the
- * default), 2 for the router launch followed by the top-k / routing launch (the same
- * bytes). A workspace serves only descriptors whose moe_workspace_bytes it was sized with
- * (the schedule changes the size). */
+ * moe_step (the default), 2 for two launches; front_launches is 0 or 2 for the router
+ * launch followed by the top-k / routing / quantisation launch (the default: on GB300 the
+ * faster of the two), 1 for all four in one launch (the same bytes). A workspace serves
+ * only descriptors whose moe_workspace_bytes it was sized with (the schedule changes the
+ * size). */
 typedef struct {
     int32_t H, E, k, I, I_shared;
     int32_t w_fmt, shared_fmt;
@@ -258,11 +258,12 @@ moe_status moe_finalize_norm(const moe_layer_desc* d, const float* y_pairs, cons
                              const int32_t* inv_perm, int M, void* residual, const void* gamma, void* out,
                              void* outq, void* outq_scales, void* ws, moe_stream_t stream);
 
-/* a1..a7 in three launches chained with programmatic dependent launch: the front (router
- * GEMV, top-k, routing and FC1 input quantisation), moe_expert_ffn, and the finalize; the
- * layer's front_launches = 2 splits the front into the router launch and the top-k /
- * routing launch, ffn_launches = 2 runs FC1 and FC2 as two launches. Intermediates in ws
- * (see moe_ws_view). M in [1, 64]. Capture-safe. */
+/* a1..a7 in three launches chained with programmatic dependent launch: the router GEMV,
+ * the top-k / routing / FC1 input quantisation, and one launch for FC1, FC2 and the
+ * finalize (the moe_expert_ffn launch followed, after a grid-wide barrier, by the
+ * moe_finalize_norm arithmetic). The layer's front_launches = 1 runs the first two as one
+ * launch; ffn_launches = 2 runs FC1, FC2 and the finalize as three launches. Intermediates
+ * in ws (see moe_ws_view). M in [1, 64]. Capture-safe. */
 moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void* ws, moe_stream_t stream);
 
 /* The router step (a1 + a2 + a3, as moe_router_topk) for callers that cannot give the

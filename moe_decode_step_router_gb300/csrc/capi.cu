@@ -162,6 +162,8 @@ WsLayout layout(const moe_layer_desc* d) {
     L.sched = take(4ull * 4);  // gate_up and down: next work item, CTAs finished
     L.gu_done = take(4ull * (kMaxE + 2));  // one launch for both GEMMs: per-group gate_up units done
     L.tcnt = take(64);  // arrival counters: [0] top-k CTAs / row blocks, [4 ..) router CTAs per row block
+    L.fin_cnt = take(4ull * (1 + kMaxRows));       // finalize in the FFN launch: grid barrier, per-row slices
+    L.fin_part = take(4ull * kMaxRows * 8);        // per row and slice: sum of squares
     L.total = o;
     return L;
 }
@@ -223,11 +225,14 @@ moe_status launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_
 
 // ------------------------------------------------------------------ launch helpers
 RouterParams router_params(const moe_layer_desc* d, const void* x, const void* w_gate, const float* logits_in, int M,
-                           float* logits_out, float* scores, int32_t* status, const void* l2_pf, size_t l2_pf_bytes) {
+                           float* logits_out, float* scores, int32_t* status, const void* l2_pf = nullptr,
+                           size_t l2_pf_bytes = 0, const void* l2_pf2 = nullptr, size_t l2_pf2_bytes = 0) {
     RouterParams p{};
     p.status = status;
-    p.l2_pf = static_cast<const uint8_t*>(l2_pf);
-    p.l2_pf_bytes = l2_pf_bytes;
+    p.l2_pf[0] = static_cast<const uint8_t*>(l2_pf);
+    p.l2_pf_bytes[0] = l2_pf_bytes;
+    p.l2_pf[1] = static_cast<const uint8_t*>(l2_pf2);
+    p.l2_pf_bytes[1] = l2_pf2_bytes;
     p.x = static_cast<const uint16_t*>(x);
     p.wg = static_cast<const uint16_t*>(w_gate);
     p.logits_in = logits_in;
@@ -245,8 +250,10 @@ size_t router_smem(const moe_layer_desc* d, int M) { return (size_t)(4 + (M < 8 
 
 moe_status launch_router(const moe_layer_desc* d, const void* x, const void* w_gate, const float* logits_in, int M,
                          float* logits_out, float* scores, int32_t* status, cudaStream_t st,
-                         const void* l2_pf = nullptr, size_t l2_pf_bytes = 0) {
-    const RouterParams p = router_params(d, x, w_gate, logits_in, M, logits_out, scores, status, l2_pf, l2_pf_bytes);
+                         const void* l2_pf = nullptr, size_t l2_pf_bytes = 0, const void* l2_pf2 = nullptr,
+                         size_t l2_pf2_bytes = 0) {
+    const RouterParams p = router_params(d, x, w_gate, logits_in, M, logits_out, scores, status, l2_pf, l2_pf_bytes,
+                                         l2_pf2, l2_pf2_bytes);
     DevInfo* di;
     moe_status s = dev_info(&di);
     if (s != MOE_OK) return s;
@@ -433,11 +440,14 @@ void gemm_classes(int g, const moe_layer_desc* d, const moe_qweight* wr, const m
 // One expert-GEMM launch: mode 0 gate_up, 1 down, 2 both (gate_up items first; a down item
 // waits in the kernel until its group's gate_up units are done).
 constexpr uint64_t kGemmWaitNs = 2000000000ull;  // 2 s: limit of every wait in the GEMM kernel
+// Records of the start of each GEMM CTA's range that the routing CTA prefetches into L2
+// (about one ring of stages).
+constexpr int kRoutePrefetchRecords = 8;
 
 moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* w13, const moe_qweight* sh13,
                        const moe_qweight* w2, const moe_qweight* sh2, const GemmBuffers& b, int M, const WsLayout& L,
                        uint8_t* ws, cudaStream_t st, bool prefetch_shared = true, uint64_t wait_ns = kGemmWaitNs,
-                       int dep_extra = 0) {
+                       int dep_extra = 0, const FinalizeParams* fin = nullptr) {
     DevInfo* di;
     moe_status s = dev_info(&di);
     if (s != MOE_OK) return s;
@@ -465,6 +475,12 @@ moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* w13
     p.prefetch_shared = prefetch_shared ? 1 : 0;
     p.wait_ns = wait_ns;
     p.dep_extra = dep_extra;
+    if (fin && mode == 2) {
+        p.fuse_finalize = 1;
+        p.fin = *fin;
+        p.fin_cnt = reinterpret_cast<int32_t*>(ws + L.fin_cnt);
+        p.fin_part = reinterpret_cast<float*>(ws + L.fin_part);
+    }
     p.pool_units = mode == 2 ? 0 : gemm_pool_units(d->gemm_schedule, di->sms < kMaxGemmCtas ? di->sms : kMaxGemmCtas);
     p.status = reinterpret_cast<int32_t*>(ws + L.header);
     if (mode != 1) gemm_classes(0, d, w13, sh13, b, M, p.cls[0]);
@@ -507,9 +523,8 @@ moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* w13
                       mode == 2);
 }
 
-moe_status launch_finalize(const moe_layer_desc* d, const float* y, const float* topk_w, const int32_t* inv_perm,
-                           int M, void* residual, const void* gamma, void* out, void* outq, void* outs,
-                           cudaStream_t st) {
+FinalizeParams finalize_params(const moe_layer_desc* d, const float* y, const float* topk_w, const int32_t* inv_perm,
+                               int M, void* residual, const void* gamma, void* out, void* outq, void* outs) {
     FinalizeParams p{};
     p.y = y;
     p.topk_w = topk_w;
@@ -524,6 +539,13 @@ moe_status launch_finalize(const moe_layer_desc* d, const float* y, const float*
     p.k = d->k;
     p.has_shared = d->has_shared;
     p.eps = d->rms_eps;
+    return p;
+}
+
+moe_status launch_finalize(const moe_layer_desc* d, const float* y, const float* topk_w, const int32_t* inv_perm,
+                           int M, void* residual, const void* gamma, void* out, void* outq, void* outs,
+                           cudaStream_t st) {
+    const FinalizeParams p = finalize_params(d, y, topk_w, inv_perm, M, residual, gamma, out, outq, outs);
     const int rows = outq ? round_up(M, 8) : M;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(8, rows);
@@ -857,11 +879,16 @@ moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void
     float* topk_w = reinterpret_cast<float*>(w + L.topk_w);
     int32_t* perm = reinterpret_cast<int32_t*>(w + L.perm);
     int32_t* inv_perm = reinterpret_cast<int32_t*>(w + L.inv_perm);
-    // the shared expert's gate_up records do not depend on the routing: the router launch
-    // prefetches them into L2 while the front end runs (the GEMM launch then does not)
+    // the shared expert's records do not depend on the routing: the router launch prefetches
+    // them into L2 while the front end runs (the GEMM launch then does not)
     const size_t sh13_bytes = d->has_shared ? (size_t)(2 * d->I_shared / kBlockRows) *
                                                   steps_of(d->shared_fmt, d->H) * record_bytes(d->shared_fmt)
                                             : 0;
+    const size_t sh2_bytes = d->has_shared ? (size_t)(d->H / kBlockRows) * steps_of(d->shared_fmt, d->I_shared) *
+                                                 record_bytes(d->shared_fmt)
+                                           : 0;
+    const void* sh13_w = d->has_shared ? a->sh13.packed : nullptr;
+    const void* sh2_w = d->has_shared ? a->sh2.packed : nullptr;
     QuantArgs qa;
     qa.x = a->x;
     qa.xq = w + L.xq;
@@ -869,19 +896,31 @@ moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void
     qa.xq_sh = w + L.xq_sh;
     qa.xs_sh = w + L.xs_sh;
     const RouterParams rp = router_params(d, a->x, a->w_gate, nullptr, M, logits, scores,
-                                          reinterpret_cast<int32_t*>(w + L.header),
-                                          d->has_shared ? a->sh13.packed : nullptr, sh13_bytes);
+                                          reinterpret_cast<int32_t*>(w + L.header), sh13_w, sh13_bytes, sh2_w,
+                                          sh2_bytes);
     int qctas = 0;
-    const TopkRouteParams tp = topk_params(d, L, w, M, scores, a->bias, topk_idx, topk_w, 1, 1,
-                                           reinterpret_cast<int32_t*>(w + L.counts), perm, inv_perm,
-                                           reinterpret_cast<int32_t*>(w + L.tiles),
-                                           reinterpret_cast<int32_t*>(w + L.num_tiles), qa, &qctas);
-    if (d->front_launches != 2) {
+    TopkRouteParams tp = topk_params(d, L, w, M, scores, a->bias, topk_idx, topk_w, 1, 1,
+                                     reinterpret_cast<int32_t*>(w + L.counts), perm, inv_perm,
+                                     reinterpret_cast<int32_t*>(w + L.tiles),
+                                     reinterpret_cast<int32_t*>(w + L.num_tiles), qa, &qctas);
+    {
+        // the routing CTA prefetches into L2 the first records of every GEMM CTA's range
+        DevInfo* di;
+        if ((s = dev_info(&di)) != MOE_OK) return s;
+        tp.pf_w = static_cast<const uint8_t*>(a->w13.packed);
+        tp.pf_MB = 2 * d->I / kBlockRows;
+        tp.pf_KS = steps_of(d->w_fmt, d->H);
+        tp.pf_rec = record_bytes(d->w_fmt);
+        tp.pf_sh_steps = d->has_shared ? (2 * d->I_shared / kBlockRows) * steps_of(d->shared_fmt, d->H) : 0;
+        tp.pf_ctas = di->sms < kMaxGemmCtas ? di->sms : kMaxGemmCtas;
+        tp.pf_recs = kRoutePrefetchRecords;
+    }
+    if (d->front_launches == 1) {
         s = launch_front(d, rp, tp, qctas, L, w, M, st);
         if (s != MOE_OK) return s;
     } else {
         s = launch_router(d, a->x, a->w_gate, nullptr, M, logits, scores, reinterpret_cast<int32_t*>(w + L.header), st,
-                          d->has_shared ? a->sh13.packed : nullptr, sh13_bytes);
+                          sh13_w, sh13_bytes, sh2_w, sh2_bytes);
         if (s != MOE_OK) return s;
         s = launch_pdl(k_topk_route, dim3(tp.topk_ctas + qctas), dim3(kRouteThreads), 0, st, tp, "k_topk_route launch");
         if (s != MOE_OK) return s;
@@ -895,18 +934,24 @@ moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void
     b.hs = w + L.hs;
     b.y = reinterpret_cast<float*>(w + L.y);
     b.perm = perm;
-    if (d->ffn_launches != 2) {
-        s = launch_gemm(2, d, &a->w13, &a->sh13, &a->w2, &a->sh2, b, M, L, w, st, false);
+    void* outq = d->emit_next_mxfp8 ? a->outq : nullptr;
+    void* outs = d->emit_next_mxfp8 ? a->outq_scales : nullptr;
+    DevInfo* di;
+    if ((s = dev_info(&di)) != MOE_OK) return s;
+    if (d->ffn_launches != 2 && di->sms >= 8) {
+        // both GEMMs and the finalize in one launch (its rows go to groups of 8 CTAs)
+        const FinalizeParams fin =
+            finalize_params(d, b.y, topk_w, inv_perm, M, a->residual, a->gamma, a->out, outq, outs);
+        s = launch_gemm(2, d, &a->w13, &a->sh13, &a->w2, &a->sh2, b, M, L, w, st, false, kGemmWaitNs, 0, &fin);
         if (s != MOE_OK) return s;
     } else {
         s = launch_gemm(0, d, &a->w13, &a->sh13, nullptr, nullptr, b, M, L, w, st, false);
         if (s != MOE_OK) return s;
         s = launch_gemm(1, d, nullptr, nullptr, &a->w2, &a->sh2, b, M, L, w, st);
         if (s != MOE_OK) return s;
+        s = launch_finalize(d, b.y, topk_w, inv_perm, M, a->residual, a->gamma, a->out, outq, outs, st);
+        if (s != MOE_OK) return s;
     }
-    s = launch_finalize(d, b.y, topk_w, inv_perm, M, a->residual, a->gamma, a->out,
-                        d->emit_next_mxfp8 ? a->outq : nullptr, d->emit_next_mxfp8 ? a->outq_scales : nullptr, st);
-    if (s != MOE_OK) return s;
     return ok();
 }
 

@@ -10,6 +10,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "finalize.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "quant.cuh"
@@ -203,11 +204,15 @@ __device__ __forceinline__ bool router_rows(const RouterParams& p, int ei, int r
             bulk_g2s(smem_u32(wsm + (size_t)r * H), p.wg + (size_t)min(e0 + r, E - 1) * H, (uint32_t)(H * 2), bar_w);
     }
     __syncthreads();  // the barriers are initialised before anyone waits on them
-    if (p.l2_pf && threadIdx.x == 32) {
-        const size_t share = (p.l2_pf_bytes / (size_t)nct + 15) & ~(size_t)15;
-        const size_t b0 = (size_t)cta * share, b1 = b0 + share < p.l2_pf_bytes ? b0 + share : p.l2_pf_bytes;
-        for (size_t o = b0; o < b1; o += 65536)
-            prefetch_l2(p.l2_pf + o, (uint32_t)(b1 - o < 65536 ? b1 - o : 65536));
+    if (threadIdx.x == 32) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            if (!p.l2_pf[r]) continue;
+            const size_t share = (p.l2_pf_bytes[r] / (size_t)nct + 15) & ~(size_t)15;
+            const size_t b0 = (size_t)cta * share, b1 = b0 + share < p.l2_pf_bytes[r] ? b0 + share : p.l2_pf_bytes[r];
+            for (size_t o = b0; o < b1; o += 65536)
+                prefetch_l2(p.l2_pf[r] + o, (uint32_t)(b1 - o < 65536 ? b1 - o : 65536));
+        }
     }
     pdl_wait();
     if (threadIdx.x == 0) {
@@ -394,6 +399,7 @@ __device__ __forceinline__ void topk_row(const TopkRouteParams& p, int m, int la
 struct RouteSmem {
     unsigned long long sel[kMaxE + 1];  // per expert: bit m set when row m selected it
     int s_off[kMaxE + 2];               // per expert: first position in perm
+    int s_gexp[kMaxE];                  // per group: its expert
     int4 sh_warp[32];
     int s_bad;
 };
@@ -454,7 +460,10 @@ __device__ void route_all(const TopkRouteParams& p, const int* own_topk, RouteSm
                 tp[1] = x0.x + kTileRows * t;
                 tp[2] = min(kTileRows, c - kTileRows * t);
             }
-            if (v.z) p.groups[x0.z] = Group{e, c, x0.x, x0.w};
+            if (v.z) {
+                p.groups[x0.z] = Group{e, c, x0.x, x0.w};
+                rs.s_gexp[x0.z] = e;
+            }
             s_off[e] = x0.x;
         }
     }
@@ -464,6 +473,24 @@ __device__ void route_all(const TopkRouteParams& p, const int* own_topk, RouteSm
         p.hdr->num_groups = tot.z;
     }
     __syncthreads();
+    if (p.pf_w && (int)threadIdx.x < p.pf_ctas) {
+        // where the GEMM launch's CTA c starts (its static range: steps c T / G .., with T the
+        // steps of the routed units, in group order, then the shared expert's, and G = min(CTAs, T))
+        const long long Tr = (long long)tot.z * p.pf_MB * p.pf_KS, T = Tr + p.pf_sh_steps;
+        const long long G = T < p.pf_ctas ? T : p.pf_ctas;
+        const long long t = (long long)threadIdx.x * T / (G > 0 ? G : 1);
+        if ((long long)threadIdx.x < G && t < Tr) {
+            const long long u = t / p.pf_KS;
+            const int g = (int)(u / p.pf_MB), b = (int)(u % p.pf_MB), k = (int)(t % p.pf_KS);
+            // the expert's records are contiguous: blocks b.., steps k..
+            const long long left = (long long)(p.pf_MB - b) * p.pf_KS - k;
+            const long long n = (left < p.pf_recs ? left : p.pf_recs) * p.pf_rec;
+            const uint8_t* src =
+                p.pf_w + (((size_t)rs.s_gexp[g] * p.pf_MB + b) * p.pf_KS + k) * (size_t)p.pf_rec;
+            for (long long o = 0; o < n; o += 65536)
+                prefetch_l2(src + o, (uint32_t)(n - o < 65536 ? n - o : 65536));
+        }
+    }
     for (int q = threadIdx.x; q < P; q += blockDim.x) {
         const int ee = own_topk ? own_topk[q] : __ldcg(p.topk_idx + q), m = q / k;
         const unsigned long long below = (m == 0) ? 0ull : (sel[ee] & ((1ull << m) - 1ull));
@@ -603,14 +630,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1) k_front(FrontParams f) {
 }
 
 // ------------------------------------------------------------------------------------
-// a7: weighted combine in fixed slot order + shared row + residual (bf16) + RMSNorm,
-// optional MXFP8 of the output per 32 along H (rows M..round_up(M,8)-1 zero).
-// One cluster of kFinCluster CTAs per row, each CTA a contiguous H slice handled as
-// float4 vectors (all k+1 row loads of a vector in flight at once); the sum of squares is
-// reduced over distributed shared memory in rank order (deterministic).
-constexpr int kFinThreads = 256;
-constexpr int kFinCluster = 8;
-
+// a7 as its own launch: one cluster of kFinSlices CTAs per row (finalize.cuh), the slices'
+// sums of squares added over distributed shared memory in rank order (deterministic).
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -628,114 +649,24 @@ __device__ __forceinline__ float dsmem_ld(const float* local, uint32_t rank) {
 }
 
 __global__ void __launch_bounds__(kFinThreads) k_finalize(FinalizeParams p) {
-    __shared__ float red[kFinThreads / 32];
-    __shared__ float part;
-    __shared__ float w_s[kMaxK];
-    __shared__ int pos_s[kMaxK + 1];
+    __shared__ FinSmem fs;
     pdl_wait();
     pdl_trigger();
-    const int m = blockIdx.y, H = p.H, k = p.k, M = p.M;
-    const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
-    const int slice = H / kFinCluster, base = (int)cluster_rank() * slice;
-    const int n = base + 4 * (int)threadIdx.x;  // this thread's 4 elements
-    const bool act = 4 * (int)threadIdx.x < slice;
-    if (m >= M) {  // padding rows of the 8-row output tiles
-        if (act) *reinterpret_cast<uint32_t*>(p.outq + (size_t)m * H + n) = 0u;
-        if (act && (n % 32) == 0) p.outs[(size_t)m * (H / 32) + n / 32] = 0;
+    const int m = blockIdx.y, s = (int)cluster_rank();
+    if (m >= p.M) {  // padding rows of the 8-row output tiles
+        fin_pad_row(p, m, s);
         cluster_sync();
         cluster_sync();
         return;
     }
-    const int P = M * k;
-    // slots beyond k read slot k-1's row (an L2 hit) with weight 0, so every load is
-    // unconditional and all of them are in flight before the first FMA
-    if (threadIdx.x < kMaxK) {
-        const int j = min((int)threadIdx.x, k - 1);
-        pos_s[threadIdx.x] = p.inv_perm[m * k + j];
-        w_s[threadIdx.x] = (int)threadIdx.x < k ? p.topk_w[m * k + j] : 0.0f;
-    }
-    if (threadIdx.x == kMaxK) pos_s[kMaxK] = p.has_shared ? p.inv_perm[P + m] : -1;
-    __syncthreads();
-    float hv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    float ss = 0.0f;
-    if (act) {
-        float4 yv[kMaxK + 1];
-        const int psh = pos_s[kMaxK];
-        const int kl = (k + 3) & ~3;  // slots loaded: k rounded up to 4 (the rest weigh 0)
-#pragma unroll
-        for (int j = 0; j < kMaxK; ++j)
-            if ((j & 3) == 0 && j >= kl) break;
-            else yv[j] = __ldcg(reinterpret_cast<const float4*>(p.y + (size_t)pos_s[j] * H + n));
-        yv[kMaxK] = __ldcg(reinterpret_cast<const float4*>(p.y + (size_t)max(psh, pos_s[0]) * H + n));
-        const uint2 rr = *reinterpret_cast<const uint2*>(p.residual + (size_t)m * H + n);
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int j = 0; j < kMaxK; ++j) {
-            if (j < k) {  // fixed slot order; FMAs only, no load below this point
-                const float w = w_s[j];
-                acc[0] = fmaf(w, yv[j].x, acc[0]);
-                acc[1] = fmaf(w, yv[j].y, acc[1]);
-                acc[2] = fmaf(w, yv[j].z, acc[2]);
-                acc[3] = fmaf(w, yv[j].w, acc[3]);
-            }
-        }
-        if (psh >= 0) {
-            acc[0] = __fadd_rn(acc[0], yv[kMaxK].x);
-            acc[1] = __fadd_rn(acc[1], yv[kMaxK].y);
-            acc[2] = __fadd_rn(acc[2], yv[kMaxK].z);
-            acc[3] = __fadd_rn(acc[3], yv[kMaxK].w);
-        }
-        const float r[4] = {bf16_lo(rr.x), bf16_hi(rr.x), bf16_lo(rr.y), bf16_hi(rr.y)};
-        uint32_t hb[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const __nv_bfloat16 b = __float2bfloat16_rn(__fadd_rn(r[i], acc[i]));
-            hb[i] = __bfloat16_as_ushort(b);
-            hv[i] = __bfloat162float(b);
-            ss = fmaf(hv[i], hv[i], ss);
-        }
-        *reinterpret_cast<uint2*>(p.residual + (size_t)m * H + n) = make_uint2(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16));
-    }
-    ss = warp_sum(ss);
-    if (lane == 0) red[warp] = ss;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float t = 0.0f;
-#pragma unroll
-        for (int i = 0; i < kFinThreads / 32; ++i) t += red[i];
-        part = t;
-    }
+    float hv[4];
+    fin_combine(p, m, s, hv, fs);
     cluster_sync();
     float tot = 0.0f;
 #pragma unroll
-    for (int rk = 0; rk < kFinCluster; ++rk) tot += dsmem_ld(&part, (uint32_t)rk);
+    for (int rk = 0; rk < kFinSlices; ++rk) tot += dsmem_ld(&fs.part, (uint32_t)rk);
     cluster_sync();  // no CTA leaves while another still reads its partial
-    const float rstd = rsqrtf(tot / (float)H + p.eps);
-    if (act) {
-        const uint2 gg = *reinterpret_cast<const uint2*>(p.gamma + n);
-        const float g[4] = {bf16_lo(gg.x), bf16_hi(gg.x), bf16_lo(gg.y), bf16_hi(gg.y)};
-        uint32_t ob[4];
-        float of[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const __nv_bfloat16 b = __float2bfloat16_rn(hv[i] * rstd * g[i]);
-            ob[i] = __bfloat16_as_ushort(b);
-            of[i] = __bfloat162float(b);
-        }
-        *reinterpret_cast<uint2*>(p.out + (size_t)m * H + n) = make_uint2(ob[0] | (ob[1] << 16), ob[2] | (ob[3] << 16));
-        if (p.outq) {
-            // a 32-element MX block = 8 consecutive lanes x 4 elements
-            float amax = fmaxf(fmaxf(fabsf(of[0]), fabsf(of[1])), fmaxf(fabsf(of[2]), fabsf(of[3])));
-#pragma unroll
-            for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o, 8));
-            const int e = mx_exponent(amax);
-            const float sc = exp2_int(-e);
-            const uint32_t lo = e4m3x2(__fmul_rn(of[1], sc), __fmul_rn(of[0], sc));
-            const uint32_t hi = e4m3x2(__fmul_rn(of[3], sc), __fmul_rn(of[2], sc));
-            *reinterpret_cast<uint32_t*>(p.outq + (size_t)m * H + n) = lo | (hi << 16);
-            if ((n % 32) == 0) p.outs[(size_t)m * (H / 32) + n / 32] = (uint8_t)(e + 127);
-        }
-    }
+    fin_output(p, m, s, hv, tot);
 }
 
 // ------------------------------------------------------------------------------------

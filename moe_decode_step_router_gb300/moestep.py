@@ -137,7 +137,7 @@ def layer_desc(cfg, gs_a=(1.0, 1.0, 1.0, 1.0)) -> LayerDesc:
                      int(cfg.get("emit_next", False)), float(cfg["rsf"]), float(cfg["eps"]), float(gs_a[0]),
                      float(gs_a[1]), float(gs_a[2]), float(gs_a[3]), float(cfg.get("swiglu_limit", 0.0)),
                      SCHEDULES[cfg.get("schedule", "static")], int(cfg.get("ffn_launches", 1)),
-                     int(cfg.get("front_launches", 1)))
+                     int(cfg.get("front_launches", 2)))
 
 
 def qweight(packed, gs=None) -> QWeight:

@@ -210,9 +210,9 @@ def test_one_launch_ffn_equals_two_launches(name, M):
         assert torch.equal(one[2], two[2]) and torch.equal(one[3], two[3])
 
 
-# moe_step runs the router, the top-k, the routing and the FC1 input quantisation as one
-# launch (the last router CTA of an 8-row block takes its rows' top-k, the last block
-# routes); a layer with front_launches = 2 runs the router launch and the top-k / routing
+# A layer with front_launches = 1 runs the router, the top-k, the routing and the FC1 input
+# quantisation as one launch (the last router CTA of an 8-row block takes its rows' top-k,
+# the last block routes); the default runs the router launch and the top-k / routing
 # launch. Same arithmetic in the same order: the same bytes, at every row count (one row
 # block, several, and the 512-expert layer's 128 router CTAs per block).
 @pytest.mark.parametrize("name,M", [(n, m) for n in SMALL for m in (1, 23, 64)] + [("full", 8), ("full512", 16)])
