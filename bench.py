@@ -3,9 +3,9 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--config NAME] [--rows M] [--no-sweep] [--no-cpu-baseline]
 
-One step = router GEMV, top-k + route + FC1 input quantisation, gate_up + down + finalize
-(moe_step: three chained launches) captured in a CUDA graph, on seeded synthetic inputs of
-the workload's shapes. Between timed steps (untimed) a 512 MiB buffer is written and another
+One step = router GEMV, top-k + route + FC1 input quantisation, gate_up + down (one
+launch), finalize (moe_step: four chained launches) captured in a CUDA graph, on seeded
+synthetic inputs of the workload's shapes. Between timed steps (untimed) a 512 MiB buffer is written and another
 read, so every step streams its weights from HBM and finds no dirty line of the flush in L2.
 
 The JSON line's value / config are the 8-row MXFP8 layer (H 7168, 256 experts, top-8);
@@ -640,7 +640,7 @@ def main(argv=None):
                         "path": "pinned host x and residual copied in, the captured moe_step graph, out copied "
                                 "back; host wall time per step (median)"},
                 "roofline": roofline, "cpu_baseline": cpu, "clocks": clk,
-                "gpu_launches": ((3 if fused else 5) - (1 if cfg["front_launches"] == 1 else 0)) * a.steps,
+                "gpu_launches": ((4 if fused else 5) - (1 if cfg["front_launches"] == 1 else 0)) * a.steps,
                 "sweep": sweep}
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -258,12 +258,11 @@ moe_status moe_finalize_norm(const moe_layer_desc* d, const float* y_pairs, cons
                              const int32_t* inv_perm, int M, void* residual, const void* gamma, void* out,
                              void* outq, void* outq_scales, void* ws, moe_stream_t stream);
 
-/* a1..a7 in three launches chained with programmatic dependent launch: the router GEMV,
- * the top-k / routing / FC1 input quantisation, and one launch for FC1, FC2 and the
- * finalize (the moe_expert_ffn launch followed, after a grid-wide barrier, by the
- * moe_finalize_norm arithmetic). The layer's front_launches = 1 runs the first two as one
- * launch; ffn_launches = 2 runs FC1, FC2 and the finalize as three launches. Intermediates
- * in ws (see moe_ws_view). M in [1, 64]. Capture-safe. */
+/* a1..a7 in four launches chained with programmatic dependent launch: the router GEMV, the
+ * top-k / routing / FC1 input quantisation, moe_expert_ffn (FC1 and FC2 in one launch), and
+ * the finalize. The layer's front_launches = 1 runs the first two as one launch;
+ * ffn_launches = 2 runs FC1 and FC2 as two launches. Intermediates in ws (see moe_ws_view).
+ * M in [1, 64]. Capture-safe. */
 moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void* ws, moe_stream_t stream);
 
 /* The router step (a1 + a2 + a3, as moe_router_topk) for callers that cannot give the

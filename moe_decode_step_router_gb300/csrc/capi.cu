@@ -162,8 +162,6 @@ WsLayout layout(const moe_layer_desc* d) {
     L.sched = take(4ull * 4);  // gate_up and down: next work item, CTAs finished
     L.gu_done = take(4ull * (kMaxE + 2));  // one launch for both GEMMs: per-group gate_up units done
     L.tcnt = take(64);  // arrival counters: [0] top-k CTAs / row blocks, [4 ..) router CTAs per row block
-    L.fin_cnt = take(4ull * (1 + kMaxRows));       // finalize in the FFN launch: grid barrier, per-row slices
-    L.fin_part = take(4ull * kMaxRows * 8);        // per row and slice: sum of squares
     L.total = o;
     return L;
 }
@@ -440,14 +438,11 @@ void gemm_classes(int g, const moe_layer_desc* d, const moe_qweight* wr, const m
 // One expert-GEMM launch: mode 0 gate_up, 1 down, 2 both (gate_up items first; a down item
 // waits in the kernel until its group's gate_up units are done).
 constexpr uint64_t kGemmWaitNs = 2000000000ull;  // 2 s: limit of every wait in the GEMM kernel
-// Records of the start of each GEMM CTA's range that the routing CTA prefetches into L2
-// (about one ring of stages).
-constexpr int kRoutePrefetchRecords = 8;
 
 moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* w13, const moe_qweight* sh13,
                        const moe_qweight* w2, const moe_qweight* sh2, const GemmBuffers& b, int M, const WsLayout& L,
                        uint8_t* ws, cudaStream_t st, bool prefetch_shared = true, uint64_t wait_ns = kGemmWaitNs,
-                       int dep_extra = 0, const FinalizeParams* fin = nullptr) {
+                       int dep_extra = 0) {
     DevInfo* di;
     moe_status s = dev_info(&di);
     if (s != MOE_OK) return s;
@@ -475,12 +470,7 @@ moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* w13
     p.prefetch_shared = prefetch_shared ? 1 : 0;
     p.wait_ns = wait_ns;
     p.dep_extra = dep_extra;
-    if (fin && mode == 2) {
-        p.fuse_finalize = 1;
-        p.fin = *fin;
-        p.fin_cnt = reinterpret_cast<int32_t*>(ws + L.fin_cnt);
-        p.fin_part = reinterpret_cast<float*>(ws + L.fin_part);
-    }
+
     p.pool_units = mode == 2 ? 0 : gemm_pool_units(d->gemm_schedule, di->sms < kMaxGemmCtas ? di->sms : kMaxGemmCtas);
     p.status = reinterpret_cast<int32_t*>(ws + L.header);
     if (mode != 1) gemm_classes(0, d, w13, sh13, b, M, p.cls[0]);
@@ -899,22 +889,10 @@ moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void
                                           reinterpret_cast<int32_t*>(w + L.header), sh13_w, sh13_bytes, sh2_w,
                                           sh2_bytes);
     int qctas = 0;
-    TopkRouteParams tp = topk_params(d, L, w, M, scores, a->bias, topk_idx, topk_w, 1, 1,
-                                     reinterpret_cast<int32_t*>(w + L.counts), perm, inv_perm,
-                                     reinterpret_cast<int32_t*>(w + L.tiles),
-                                     reinterpret_cast<int32_t*>(w + L.num_tiles), qa, &qctas);
-    {
-        // the routing CTA prefetches into L2 the first records of every GEMM CTA's range
-        DevInfo* di;
-        if ((s = dev_info(&di)) != MOE_OK) return s;
-        tp.pf_w = static_cast<const uint8_t*>(a->w13.packed);
-        tp.pf_MB = 2 * d->I / kBlockRows;
-        tp.pf_KS = steps_of(d->w_fmt, d->H);
-        tp.pf_rec = record_bytes(d->w_fmt);
-        tp.pf_sh_steps = d->has_shared ? (2 * d->I_shared / kBlockRows) * steps_of(d->shared_fmt, d->H) : 0;
-        tp.pf_ctas = di->sms < kMaxGemmCtas ? di->sms : kMaxGemmCtas;
-        tp.pf_recs = kRoutePrefetchRecords;
-    }
+    const TopkRouteParams tp = topk_params(d, L, w, M, scores, a->bias, topk_idx, topk_w, 1, 1,
+                                           reinterpret_cast<int32_t*>(w + L.counts), perm, inv_perm,
+                                           reinterpret_cast<int32_t*>(w + L.tiles),
+                                           reinterpret_cast<int32_t*>(w + L.num_tiles), qa, &qctas);
     if (d->front_launches == 1) {
         s = launch_front(d, rp, tp, qctas, L, w, M, st);
         if (s != MOE_OK) return s;
@@ -936,22 +914,17 @@ moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void
     b.perm = perm;
     void* outq = d->emit_next_mxfp8 ? a->outq : nullptr;
     void* outs = d->emit_next_mxfp8 ? a->outq_scales : nullptr;
-    DevInfo* di;
-    if ((s = dev_info(&di)) != MOE_OK) return s;
-    if (d->ffn_launches != 2 && di->sms >= 8) {
-        // both GEMMs and the finalize in one launch (its rows go to groups of 8 CTAs)
-        const FinalizeParams fin =
-            finalize_params(d, b.y, topk_w, inv_perm, M, a->residual, a->gamma, a->out, outq, outs);
-        s = launch_gemm(2, d, &a->w13, &a->sh13, &a->w2, &a->sh2, b, M, L, w, st, false, kGemmWaitNs, 0, &fin);
+    if (d->ffn_launches != 2) {
+        s = launch_gemm(2, d, &a->w13, &a->sh13, &a->w2, &a->sh2, b, M, L, w, st, false);
         if (s != MOE_OK) return s;
     } else {
         s = launch_gemm(0, d, &a->w13, &a->sh13, nullptr, nullptr, b, M, L, w, st, false);
         if (s != MOE_OK) return s;
         s = launch_gemm(1, d, nullptr, nullptr, &a->w2, &a->sh2, b, M, L, w, st);
         if (s != MOE_OK) return s;
-        s = launch_finalize(d, b.y, topk_w, inv_perm, M, a->residual, a->gamma, a->out, outq, outs, st);
-        if (s != MOE_OK) return s;
     }
+    s = launch_finalize(d, b.y, topk_w, inv_perm, M, a->residual, a->gamma, a->out, outq, outs, st);
+    if (s != MOE_OK) return s;
     return ok();
 }
 

@@ -41,7 +41,6 @@
 #include <climits>
 #include <cuda_runtime.h>
 
-#include "finalize.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "quant.cuh"
@@ -115,10 +114,6 @@ struct Walker {
         t = t1 = 0;
         if (c >= G || T == 0) return;
         seek((long long)c * T / G, (long long)(c + 1) * T / G);
-    }
-    // First step of the unit holding step s.
-    __device__ long long unit_start(long long s) const {
-        return s < T_r ? s - s % KS0 : T_r + (s - T_r) / KS1 * KS1;
     }
     // The walk [ta, tb): position of step ta, with the records of its group and the next.
     __device__ void seek(long long ta, long long tb) {
@@ -450,59 +445,6 @@ __device__ __forceinline__ int mma_segment(uint32_t ready0, uint32_t empty0, Rin
     return issued;
 }
 
-// a7 at the end of the one-launch FFN of a step. Once every CTA's down outputs are written
-// (a grid barrier: the launch is cooperative, so every CTA is resident), the CTAs in groups
-// of kFinSlices take rows: CTA c handles slice c % 8 of rows c / 8, c / 8 + R, ... (R = G / 8
-// groups). The 8 CTAs of a group handle the same rows in the same order, so each waits only
-// for its own group at its own row: no CTA waits for one that has not reached that row.
-// The slices' sums of squares meet in global memory and are added in slice order, as
-// k_finalize adds them over distributed shared memory: the same bytes.
-__device__ void finalize_in_launch(const GemmParams& p, const GemmSmem& sm) {
-    FinSmem& fs = *reinterpret_cast<FinSmem*>(sm.stg);  // the epilogue staging is free now
-    const FinalizeParams& f = p.fin;
-    __threadfence();  // every thread's outputs, before this CTA's arrival below
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        atomicAdd(p.fin_cnt, 1);
-        const bool ok = wait_at_least(p.fin_cnt, (int)gridDim.x, sm.never, p.wait_ns);
-        __threadfence();
-        *sm.bcast = ok ? 1 : 0;
-        if (!ok) atomicCAS(p.status, 0, (int)MOE_ERR_TIMEOUT);
-    }
-    __syncthreads();
-    if (!*sm.bcast) return;
-    const int R = (int)gridDim.x / kFinSlices;
-    if ((int)blockIdx.x >= R * kFinSlices) return;
-    const int s = (int)blockIdx.x % kFinSlices;
-    const int M8 = f.outq ? round_up(f.M, 8) : f.M;
-    for (int m = (int)blockIdx.x / kFinSlices; m < M8; m += R) {
-        if (m >= f.M) {
-            fin_pad_row(f, m, s);
-            continue;
-        }
-        float hv[4];
-        fin_combine(f, m, s, hv, fs);
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            p.fin_part[m * kFinSlices + s] = fs.part;
-            __threadfence();
-            atomicAdd(p.fin_cnt + 1 + m, 1);
-            const bool ok = wait_at_least(p.fin_cnt + 1 + m, kFinSlices, sm.never, p.wait_ns);
-            __threadfence();
-            float tot = 0.0f;
-#pragma unroll
-            for (int rk = 0; rk < kFinSlices; ++rk) tot += __ldcg(p.fin_part + m * kFinSlices + rk);
-            fs.tot = tot;
-            *sm.bcast = ok ? 1 : 0;
-            if (!ok) atomicCAS(p.status, 0, (int)MOE_ERR_TIMEOUT);
-        }
-        __syncthreads();
-        if (!*sm.bcast) return;
-        fin_output(f, m, s, hv, fs.tot);
-        __syncthreads();  // fs is refilled for the next row
-    }
-}
-
 __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_constant__ GemmParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -722,27 +664,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                 Walker wk;
                 wk.init(p, gm, ngroups, G, c, U0);
                 const bool deps = gm == 1 && p.mode == 2;  // down items after gate_up in one launch
-                auto walk = [&]() {
-                    while (ok && wk.next(it, G, c)) ok = issue(it, deps ? ((it.cls & 1) ? kMaxE : it.gidx) : -1);
-                };
-                // When the range ends inside a unit, that piece goes first: the CTA's last item
-                // is then a whole unit, and the cut unit's pieces (added by whichever CTA ends
-                // its last piece) are done early instead of at the end of the launch. Down
-                // items in the one-launch FFN keep their order (each waits for its group, the
-                // last group the latest).
-                const long long ta = wk.t, tb = wk.t1;
-                const long long tl = tb > ta ? wk.unit_start(tb - 1) : ta;
-                const long long tl_end = tl + (tl < wk.T_r ? wk.KS0 : wk.KS1);
-                if (!deps && tl > ta && tb < tl_end) {
-                    wk.seek(tl, tb);
-                    walk();
-                    if (ok) {
-                        wk.seek(ta, tl);
-                        walk();
-                    }
-                } else {
-                    walk();
-                }
+                while (ok && wk.next(it, G, c)) ok = issue(it, deps ? ((it.cls & 1) ? kMaxE : it.gidx) : -1);
             }
             if (ok && Up > 0) {
                 DynList dl;
@@ -1215,10 +1137,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
-    if (p.mode == 2 && p.fuse_finalize) {
-        finalize_in_launch(p, sm);
-        __syncthreads();  // every thread has read the broadcast word before it is reused below
-    }
     // both GEMMs in one launch: the last CTA to finish resets the group counters
     if (p.mode == 2) {
         if (threadIdx.x == 0) {
@@ -1232,8 +1150,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                 p.gu_done[kMaxE] = 0;
                 p.gu_done[kMaxE + 1] = 0;
             }
-            if (p.fuse_finalize)
-                for (int i = threadIdx.x; i <= p.fin.M; i += blockDim.x) p.fin_cnt[i] = 0;
             __threadfence();
         }
     }

@@ -72,7 +72,7 @@ struct WsHeader {
 // Byte offsets of the workspace regions for a layer and a maximum row count.
 struct WsLayout {
     size_t header, groups, logits, scores, topk_idx, topk_w, counts, perm, inv_perm, tiles, num_tiles;
-    size_t xq, xs, xq_sh, xs_sh, hq, hs, y, cnt_gu, cnt_dn, partials, sched, gu_done, tcnt, fin_cnt, fin_part, total;
+    size_t xq, xs, xq_sh, xs_sh, hq, hs, y, cnt_gu, cnt_dn, partials, sched, gu_done, tcnt, total;
     int max_rows, P_max, G_max, T_max, U_gu, U_dn;
     size_t hq_routed_bytes, hs_routed_bytes;  // shared group's data / scales start here
 };
@@ -112,13 +112,6 @@ struct TopkRouteParams {
     int H, fmt_r, fmt_s, quant_shared;
     uint8_t *xq, *xs, *xq_sh, *xs_sh;
     float gs_r, gs_s;
-    // Once the groups are known, the routing CTA prefetches into L2 the first records each
-    // CTA of the expert GEMM launch will stream (the start of its static range in the
-    // gate_up list), while HBM would otherwise wait for that launch's prologue. Null: none.
-    const uint8_t* pf_w;      // routed W13 records
-    int pf_MB, pf_KS, pf_rec; // a routed expert's W13: 128-row blocks, K steps, record bytes
-    int pf_sh_steps;          // K steps of the shared expert's gate_up units (0 without one)
-    int pf_ctas, pf_recs;     // CTAs of the GEMM launch; records to prefetch for each
 };
 
 // k_front: the router launch's and the top-k launch's parameters, plus the per-row-block
@@ -178,13 +171,6 @@ struct GemmParams {
     float swiglu_limit;       // > 0: clamped SwiGLU in the gate_up epilogue
     int prefetch_shared;      // 1: prefetch the shared expert's records into L2 before the wait
     uint64_t wait_ns;         // limit of every wait (2 s)
-    // mode 2 inside a step: the finalize (a7) runs at the end of this launch, after a grid
-    // barrier (every CTA is resident: the launch is cooperative)
-    int fuse_finalize;
-    int32_t* fin_cnt;         // [1 + kMaxRows]: CTAs past the GEMMs, then per row: slices done
-                              // (self-resetting)
-    float* fin_part;          // [kMaxRows][8]: each slice's sum of squares
-    FinalizeParams fin;
     int dep_extra;            // 0; 1 makes the down items' counter targets unreachable (a test
                               // of the timeout path, never set by the public calls)
 };

@@ -399,7 +399,6 @@ __device__ __forceinline__ void topk_row(const TopkRouteParams& p, int m, int la
 struct RouteSmem {
     unsigned long long sel[kMaxE + 1];  // per expert: bit m set when row m selected it
     int s_off[kMaxE + 2];               // per expert: first position in perm
-    int s_gexp[kMaxE];                  // per group: its expert
     int4 sh_warp[32];
     int s_bad;
 };
@@ -460,10 +459,7 @@ __device__ void route_all(const TopkRouteParams& p, const int* own_topk, RouteSm
                 tp[1] = x0.x + kTileRows * t;
                 tp[2] = min(kTileRows, c - kTileRows * t);
             }
-            if (v.z) {
-                p.groups[x0.z] = Group{e, c, x0.x, x0.w};
-                rs.s_gexp[x0.z] = e;
-            }
+            if (v.z) p.groups[x0.z] = Group{e, c, x0.x, x0.w};
             s_off[e] = x0.x;
         }
     }
@@ -473,24 +469,6 @@ __device__ void route_all(const TopkRouteParams& p, const int* own_topk, RouteSm
         p.hdr->num_groups = tot.z;
     }
     __syncthreads();
-    if (p.pf_w && (int)threadIdx.x < p.pf_ctas) {
-        // where the GEMM launch's CTA c starts (its static range: steps c T / G .., with T the
-        // steps of the routed units, in group order, then the shared expert's, and G = min(CTAs, T))
-        const long long Tr = (long long)tot.z * p.pf_MB * p.pf_KS, T = Tr + p.pf_sh_steps;
-        const long long G = T < p.pf_ctas ? T : p.pf_ctas;
-        const long long t = (long long)threadIdx.x * T / (G > 0 ? G : 1);
-        if ((long long)threadIdx.x < G && t < Tr) {
-            const long long u = t / p.pf_KS;
-            const int g = (int)(u / p.pf_MB), b = (int)(u % p.pf_MB), k = (int)(t % p.pf_KS);
-            // the expert's records are contiguous: blocks b.., steps k..
-            const long long left = (long long)(p.pf_MB - b) * p.pf_KS - k;
-            const long long n = (left < p.pf_recs ? left : p.pf_recs) * p.pf_rec;
-            const uint8_t* src =
-                p.pf_w + (((size_t)rs.s_gexp[g] * p.pf_MB + b) * p.pf_KS + k) * (size_t)p.pf_rec;
-            for (long long o = 0; o < n; o += 65536)
-                prefetch_l2(src + o, (uint32_t)(n - o < 65536 ? n - o : 65536));
-        }
-    }
     for (int q = threadIdx.x; q < P; q += blockDim.x) {
         const int ee = own_topk ? own_topk[q] : __ldcg(p.topk_idx + q), m = q / k;
         const unsigned long long below = (m == 0) ? 0ull : (sel[ee] & ((1ull << m) - 1ull));
