@@ -4,10 +4,9 @@
 // RMSNorm, the next input's MXFP8 scales per 8-row tile).
 //
 // A row is cut into kFinSlices contiguous slices; a slice is handled by kFinThreads threads
-// of one CTA, 4 consecutive elements (one float4 of each y row) each. Both k_finalize (one
-// 8-CTA cluster per row, the slices' sums of squares added over distributed shared memory)
-// and the one-launch FFN (the slices' sums through global memory after a grid barrier) run
-// these functions and add the slice sums in slice order, so the two give the same bytes.
+// of one CTA, 4 consecutive elements (one float4 of each y row) each; k_finalize runs one
+// 8-CTA cluster per row and adds the slices' sums of squares over distributed shared memory
+// in slice order.
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -23,7 +22,6 @@ constexpr int kFinSlices = 8;
 struct FinSmem {
     float red[kFinThreads / 32];
     float part;  // this slice's sum of squares (thread 0 writes it)
-    float tot;   // the row's (the one-launch FFN's reduction)
     float w_s[kMaxK];
     int pos_s[kMaxK + 1];
 };
@@ -40,25 +38,45 @@ __device__ __forceinline__ void fin_pad_row(const FinalizeParams& p, int m, int 
     }
 }
 
-// Combine + residual of slice s of row m (m < M): writes the new residual, leaves the bf16
-// values in hv and this slice's sum of their squares in fs.part (thread 0 writes it; the
-// caller synchronises before reading it). Every thread of the CTA calls this (it holds
-// __syncthreads); threads at or above kFinThreads take no elements.
-__device__ __forceinline__ void fin_combine(const FinalizeParams& p, int m, int s, float hv[4], FinSmem& fs) {
-    const int H = p.H, k = p.k, M = p.M;
-    const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+// What a (row m < M, slice s) task reads besides the FC2 rows: the row's pair positions
+// and weights (into fs; the caller synchronises before fin_combine) and this thread's
+// residual and gamma elements. None of it is written by the FC2 launch, so a launch that
+// follows it may read this before its dependency wait (all of it comes from launches that
+// had finished before the FC2 launch passed its own wait, or from before the step).
+struct FinPre {
+    uint2 rr, gg;  // residual, gamma: 4 bf16 each
+};
+__device__ __forceinline__ FinPre fin_preload(const FinalizeParams& p, int m, int s, FinSmem& fs) {
+    const int H = p.H, k = p.k, P = p.M * k;
     const int slice = H / kFinSlices, n = s * slice + 4 * (int)threadIdx.x;
     const bool act = threadIdx.x < kFinThreads && 4 * (int)threadIdx.x < slice;
-    const int P = M * k;
-    // slots beyond k read slot k-1's row (an L2 hit) with weight 0, so every load is
+    // slots beyond k read slot k-1's row (an L2 hit) with weight 0, so every FC2-row load is
     // unconditional and all of them are in flight before the first FMA
     if (threadIdx.x < kMaxK) {
         const int j = min((int)threadIdx.x, k - 1);
-        fs.pos_s[threadIdx.x] = p.inv_perm[m * k + j];
-        fs.w_s[threadIdx.x] = (int)threadIdx.x < k ? p.topk_w[m * k + j] : 0.0f;
+        fs.pos_s[threadIdx.x] = __ldcg(p.inv_perm + m * k + j);
+        fs.w_s[threadIdx.x] = (int)threadIdx.x < k ? __ldcg(p.topk_w + m * k + j) : 0.0f;
     }
-    if (threadIdx.x == kMaxK) fs.pos_s[kMaxK] = p.has_shared ? p.inv_perm[P + m] : -1;
-    __syncthreads();
+    if (threadIdx.x == kMaxK) fs.pos_s[kMaxK] = p.has_shared ? __ldcg(p.inv_perm + P + m) : -1;
+    FinPre pre{make_uint2(0u, 0u), make_uint2(0u, 0u)};
+    if (act) {
+        pre.rr = __ldcg(reinterpret_cast<const uint2*>(p.residual + (size_t)m * H + n));
+        pre.gg = __ldg(reinterpret_cast<const uint2*>(p.gamma + n));
+    }
+    return pre;
+}
+
+// Combine + residual of slice s of row m (m < M), after fin_preload and a barrier: writes
+// the new residual, leaves the bf16 values in hv and this slice's sum of their squares in
+// fs.part (thread 0 writes it; the caller synchronises before reading it). Every thread of
+// the CTA calls this (it holds __syncthreads); threads at or above kFinThreads take no
+// elements.
+__device__ __forceinline__ void fin_combine(const FinalizeParams& p, int m, int s, const FinPre& pre, float hv[4],
+                                            FinSmem& fs) {
+    const int H = p.H, k = p.k;
+    const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+    const int slice = H / kFinSlices, n = s * slice + 4 * (int)threadIdx.x;
+    const bool act = threadIdx.x < kFinThreads && 4 * (int)threadIdx.x < slice;
     hv[0] = hv[1] = hv[2] = hv[3] = 0.0f;
     float ss = 0.0f;
     if (act) {
@@ -70,7 +88,7 @@ __device__ __forceinline__ void fin_combine(const FinalizeParams& p, int m, int 
             if ((j & 3) == 0 && j >= kl) break;
             else yv[j] = __ldcg(reinterpret_cast<const float4*>(p.y + (size_t)fs.pos_s[j] * H + n));
         yv[kMaxK] = __ldcg(reinterpret_cast<const float4*>(p.y + (size_t)max(psh, fs.pos_s[0]) * H + n));
-        const uint2 rr = *reinterpret_cast<const uint2*>(p.residual + (size_t)m * H + n);
+        const uint2 rr = pre.rr;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int j = 0; j < kMaxK; ++j) {
@@ -113,7 +131,8 @@ __device__ __forceinline__ void fin_combine(const FinalizeParams& p, int m, int 
 
 // RMSNorm of slice s of row m from the row's sum of squares tot (the slices' sums added in
 // slice order, starting from 0): out, and the next layer's MXFP8 input when asked for.
-__device__ __forceinline__ void fin_output(const FinalizeParams& p, int m, int s, const float hv[4], float tot) {
+__device__ __forceinline__ void fin_output(const FinalizeParams& p, int m, int s, const FinPre& pre, const float hv[4],
+                                           float tot) {
     const int H = p.H, slice = H / kFinSlices, n = s * slice + 4 * (int)threadIdx.x;
     const bool act = threadIdx.x < kFinThreads && 4 * (int)threadIdx.x < slice;
     // the lanes of this warp that hold elements: whole 8-lane groups (a slice is a multiple
@@ -121,7 +140,7 @@ __device__ __forceinline__ void fin_output(const FinalizeParams& p, int m, int s
     const uint32_t amask = __ballot_sync(0xffffffffu, act);
     const float rstd = rsqrtf(tot / (float)H + p.eps);
     if (!act) return;
-    const uint2 gg = *reinterpret_cast<const uint2*>(p.gamma + n);
+    const uint2 gg = pre.gg;
     const float g[4] = {fin_bf16_lo(gg.x), fin_bf16_hi(gg.x), fin_bf16_lo(gg.y), fin_bf16_hi(gg.y)};
     uint32_t ob[4];
     float of[4];

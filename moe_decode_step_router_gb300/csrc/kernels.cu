@@ -628,23 +628,28 @@ __device__ __forceinline__ float dsmem_ld(const float* local, uint32_t rank) {
 
 __global__ void __launch_bounds__(kFinThreads) k_finalize(FinalizeParams p) {
     __shared__ FinSmem fs;
-    pdl_wait();
-    pdl_trigger();
     const int m = blockIdx.y, s = (int)cluster_rank();
-    if (m >= p.M) {  // padding rows of the 8-row output tiles
+    if (m >= p.M) {  // padding rows of the 8-row output tiles (written by no earlier launch)
+        pdl_wait();
+        pdl_trigger();
         fin_pad_row(p, m, s);
         cluster_sync();
         cluster_sync();
         return;
     }
+    // everything but the FC2 rows, before the wait for the FC2 launch
+    const FinPre pre = fin_preload(p, m, s, fs);
+    pdl_wait();
+    pdl_trigger();
+    __syncthreads();
     float hv[4];
-    fin_combine(p, m, s, hv, fs);
+    fin_combine(p, m, s, pre, hv, fs);
     cluster_sync();
     float tot = 0.0f;
 #pragma unroll
     for (int rk = 0; rk < kFinSlices; ++rk) tot += dsmem_ld(&fs.part, (uint32_t)rk);
     cluster_sync();  // no CTA leaves while another still reads its partial
-    fin_output(p, m, s, hv, tot);
+    fin_output(p, m, s, pre, hv, tot);
 }
 
 // ------------------------------------------------------------------------------------
