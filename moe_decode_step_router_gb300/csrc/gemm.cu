@@ -84,19 +84,12 @@ struct Ring {
     }
 };
 
-// Static part: this CTA's range of the steps of units [0, U0) (routed units in group
-// order, then the shared expert's units): CTA c of G takes the steps from
-// b_c = floor((2c + h) T / 2G) to b_(c+1), the last one wrapping round to b_0 when h = 1.
-// h = 0 for gate_up; h = 1 (the ranges moved on by half a range) for down, so that in the
-// one-launch FFN a CTA's first down items are of the groups in the middle of its own FC1
-// range, which it finished halfway through, rather than the group its range started in,
-// whose last FC1 units the previous CTA only reaches at the end. The position is advanced
-// incrementally (no divisions after the start) and each group record is loaded one group
-// ahead.
+// Static part: this CTA's contiguous range of the steps of units [0, U0) (routed units in
+// group order, then the shared expert's units). The position is advanced incrementally (no
+// divisions after the start) and each group record is loaded one group ahead.
 struct Walker {
     const Group* groups;
     long long T_r, T, t, t1;
-    int h;  // 0, or 1 for ranges moved on by half a range
     int gemm, ngroups, MB0, KS0, MB1, KS1, M, ktop;
     int cls, g, b, k;  // position of step t
     int4 cur, nxt;     // records of groups g and g + 1
@@ -106,14 +99,9 @@ struct Walker {
         return U0 <= NRU ? (long long)U0 * p.cls[gm][0].KS
                          : (long long)NRU * p.cls[gm][0].KS + (long long)(U0 - NRU) * p.cls[gm][1].KS;
     }
-    // Sets up the walk of GEMM gm's units [0, U0) for CTA c of G; its range is
-    // [range_a, range_b), or for the last CTA with h = 1 [range_a, T) then [0, range_b).
-    long long range_a, range_b;
-    bool wraps;
-    __device__ void init(const GemmParams& p, int gm, int ngroups_, int G, int c, int U0, int h_) {
+    __device__ void init(const GemmParams& p, int gm, int ngroups_, int G, int c, int U0) {
         groups = p.groups;
         gemm = gm;
-        h = G > 1 ? h_ : 0;  // one CTA: no range to move
         ngroups = ngroups_;
         MB0 = p.cls[gm][0].MB;
         KS0 = p.cls[gm][0].KS;
@@ -124,16 +112,8 @@ struct Walker {
         T_r = (long long)ngroups * MB0 * KS0;
         T = steps_before(p, gm, ngroups, U0);
         t = t1 = 0;
-        range_a = range_b = 0;
-        wraps = false;
         if (c >= G || T == 0) return;
-        range_a = start(c, G);
-        range_b = start(c + 1, G);
-        if (range_b > T) {  // the last CTA with h = 1: [range_a, T) and [0, b_0)
-            range_b -= T;
-            wraps = true;
-        }
-        seek(range_a, wraps ? T : range_b);
+        seek((long long)c * T / G, (long long)(c + 1) * T / G);
     }
     // The walk [ta, tb): position of step ta, with the records of its group and the next.
     __device__ void seek(long long ta, long long tb) {
@@ -155,13 +135,8 @@ struct Walker {
             k = (int)(tt - (long long)b * KS1);
         }
     }
-    // b_c; b_G = T + b_0
-    __device__ long long start(long long c, int G) const { return ((2 * c + h) * T) / (2 * (long long)G); }
-    // the CTA whose range holds step s (the last one for steps below b_0)
-    __device__ int cta_of(long long s, int G) const {
-        const long long num = 2 * (long long)G * (s + 1) - h * T;
-        return num <= 0 ? G - 1 : (int)((num - 1) / (2 * T));
-    }
+    __device__ long long start(long long c, int G) const { return c * T / G; }
+    __device__ int cta_of(long long step, int G) const { return (int)(((step + 1) * G - 1) / T); }
     // The next segment of the range (with its stream-K piece facts), or false at its end.
     __device__ __forceinline__ bool next(WorkItem& w, int G, int c) {
         if (t >= t1) return false;
@@ -190,16 +165,14 @@ struct Walker {
         }
         w.np = 1;
         if (w.ka != 0 || w.kb != KS) {
-            // the unit is cut between CTAs c_first, c_first + 1, .. c_last (round from the
-            // last CTA to CTA 0 for the unit holding b_0 when h = 1); each CTA has two slots:
-            // 2c for the unit its range starts in, 2c + 1 for the one it ends in
+            // the unit is cut between CTAs c_first..c_last; each CTA has two slots (for
+            // the unit its range starts in and the one it ends in)
             const int c_first = cta_of(us, G), c_last = cta_of(us + KS - 1, G);
-            const bool round = c_last < c_first;
-            w.np = c_last - c_first + 1 + (round ? G : 0);
-            w.s0 = 2 * c_first + (start(c_first, G) != us ? 1 : 0);
-            w.sb = 2 * c_first - (round ? 2 * G : 0);  // piece pc > 0: CTA (c_first + pc) mod G
+            w.np = c_last - c_first + 1;
+            w.s0 = 2 * c_first + (start(c_first, G) < us ? 1 : 0);
+            w.sb = 2 * c_first;
             w.sstride = 2;
-            w.myslot = 2 * c + ((c == c_first && start(c, G) != us) ? 1 : 0);
+            w.myslot = 2 * c + ((c == c_first && start(c, G) < us) ? 1 : 0);
         }
         t += w.kb - w.ka;
         k = w.kb;
@@ -689,13 +662,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
             const int G = (int)((long long)gridDim.x < Tst ? (long long)gridDim.x : Tst);
             {
                 Walker wk;
-                wk.init(p, gm, ngroups, G, c, U0, gm == 1 ? 1 : 0);
+                wk.init(p, gm, ngroups, G, c, U0);
                 const bool deps = gm == 1 && p.mode == 2;  // down items after gate_up in one launch
                 while (ok && wk.next(it, G, c)) ok = issue(it, deps ? ((it.cls & 1) ? kMaxE : it.gidx) : -1);
-                if (ok && wk.wraps) {
-                    wk.seek(0, wk.range_b);
-                    while (ok && wk.next(it, G, c)) ok = issue(it, deps ? ((it.cls & 1) ? kMaxE : it.gidx) : -1);
-                }
             }
             if (ok && Up > 0) {
                 DynList dl;
