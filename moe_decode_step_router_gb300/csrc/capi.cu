@@ -242,9 +242,9 @@ RouterParams router_params(const moe_layer_desc* d, const void* x, const void* w
     return p;
 }
 
-// Dynamic shared memory of a router CTA: its kRouterEPC gate rows and up to 8 x rows of H
-// bf16 ((2 + 8) * H * 2 <= 160 KB).
-size_t router_smem(const moe_layer_desc* d, int M) { return (size_t)(kRouterEPC + (M < 8 ? M : 8)) * d->H * 2; }
+// Dynamic shared memory of a router CTA: its 4 gate rows and up to 8 x rows of H bf16
+// ((4 + 8) * H * 2 <= 192 KB).
+size_t router_smem(const moe_layer_desc* d, int M) { return (size_t)(4 + (M < 8 ? M : 8)) * d->H * 2; }
 
 moe_status launch_router(const moe_layer_desc* d, const void* x, const void* w_gate, const float* logits_in, int M,
                          float* logits_out, float* scores, int32_t* status, cudaStream_t st,
@@ -255,7 +255,7 @@ moe_status launch_router(const moe_layer_desc* d, const void* x, const void* w_g
     DevInfo* di;
     moe_status s = dev_info(&di);
     if (s != MOE_OK) return s;
-    // the GEMV: CTAs of kRouterEPC experts x 8 rows over the whole of H (512 threads, as in k_front,
+    // the GEMV: CTAs of 4 experts x 8 rows over the whole of H (512 threads, as in k_front,
     // so both give the same logits), x rows and gate rows in shared memory (plus ~2 KB of
     // static shared memory)
     if (!logits_in) {
@@ -265,8 +265,7 @@ moe_status launch_router(const moe_layer_desc* d, const void* x, const void* w_g
             if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(k_router_rows)");
             di->router_rows_attr_set = true;
         }
-        return launch_pdl(k_router_rows, dim3((d->E + kRouterEPC - 1) / kRouterEPC, (M + 7) / 8), dim3(kRouteThreads),
-                          router_smem(d, M),
+        return launch_pdl(k_router_rows, dim3((d->E + 3) / 4, (M + 7) / 8), dim3(kRouteThreads), router_smem(d, M),
                           st, p, "k_router_rows launch");
     }
     // the logits are given: scores only
@@ -372,7 +371,7 @@ moe_status launch_front(const moe_layer_desc* d, const RouterParams& r, const To
     int32_t* arrivals = reinterpret_cast<int32_t*>(ws + L.tcnt);
     f.t.topk_arrivals = arrivals;
     f.rb_arrivals = arrivals + 4;
-    const int nr = ((d->E + kRouterEPC - 1) / kRouterEPC) * ((M + 7) / 8);
+    const int nr = ((d->E + 3) / 4) * ((M + 7) / 8);
     return launch_pdl(k_front, dim3(nr + qctas), dim3(kRouteThreads), router_smem(d, M), st, f, "k_front launch");
 }
 

@@ -91,7 +91,6 @@ struct RouterParams {
 };
 
 constexpr int kRouteThreads = 512;  // k_topk_route: 16 warps, one row each
-constexpr int kRouterEPC = 2;       // router GEMV: experts per CTA (x 8 rows)
 
 struct TopkRouteParams {
     const float* scores;      // [M, E] (topk stage)

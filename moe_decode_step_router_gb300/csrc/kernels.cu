@@ -169,12 +169,11 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(RouterParams p) {
 // memory (one bulk copy per row) before the dependency wait (they do not depend on earlier
 // launches), the x rows (one bulk copy) after it. Thread t takes the 16-byte chunks
 // t, t + NW * 32, ... of H for all EPC x R (expert, row) dot products; a warp then folds
-// its EPC x R partial sums by recursive halving, so that lane l ends with the warp's sum for
-// output l % (EPC R) = expert * R + row, and one thread per output adds the NW warps' sums
-// in warp order. The order of every addition is fixed: the logits are deterministic, and
-// the same in both launches that run this (k_router_rows and k_front, both with
-// EPC = kRouterEPC and NW = 16). The score is the same fp32 sigmoid as in k_router
-// (evaluated in double, rounded once).
+// its 32 partial sums by recursive halving, so that lane l ends with the warp's sum for
+// output l = expert * R + row, and thread l adds the NW warps' sums in warp order. The
+// order of every addition is fixed: the logits are deterministic, and the same in both
+// launches that run this (k_router_rows and k_front, both at NW = 16). The score is the
+// same fp32 sigmoid as in k_router (evaluated in double, rounded once).
 // (ei, rj): this CTA's expert group and row block; CTA cta of nct takes its share of the L2
 // prefetch. Returns false when a copy wait ran out (recorded in the status word; nothing
 // is written).
@@ -182,8 +181,7 @@ constexpr uint64_t kRouterWaitNs = 2000000000ull;  // 2 s: limit of the router's
 
 template <int EPC, int R, int NW>
 __device__ __forceinline__ bool router_rows(const RouterParams& p, int ei, int rj, int cta, int nct) {
-    constexpr int NO = EPC * R;  // outputs of the CTA: 16 or 32
-    static_assert(NO == 16 || NO == 32, "16 or 32 outputs");
+    static_assert(EPC * R == 32, "one output per lane");
     extern __shared__ __align__(16) uint16_t rrs[];
     __shared__ float red[NW][32];
     __shared__ __align__(8) uint64_t rbar[2];  // gate rows, x rows
@@ -231,9 +229,9 @@ __device__ __forceinline__ bool router_rows(const RouterParams& p, int ei, int r
         mbar_wait_bounded(bar_x, 0, &s_never, kRouterWaitNs / 2);
         return false;
     }
-    float acc[NO];
+    float acc[32];
 #pragma unroll
-    for (int i = 0; i < NO; ++i) acc[i] = 0.0f;
+    for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
     for (int c = threadIdx.x; c < V; c += blockDim.x) {
         uint4 wv[EPC];
 #pragma unroll
@@ -256,15 +254,9 @@ __device__ __forceinline__ bool router_rows(const RouterParams& p, int ei, int r
     }
     pdl_trigger();  // let the top-k launch get scheduled while the sums are folded
     // recursive halving: at the step of width s a lane keeps the half of its live values
-    // selected by its bit s and adds its partner's copy of that half; with 16 outputs the
-    // two half-warps first add their whole vectors, and lanes l and l + 16 both end with
-    // output l % 16
-    if (NO == 16) {
+    // selected by its bit s and adds its partner's copy of that half
 #pragma unroll
-        for (int i = 0; i < NO; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 16);
-    }
-#pragma unroll
-    for (int sw = NO / 2; sw >= 1; sw >>= 1) {
+    for (int sw = 16; sw >= 1; sw >>= 1) {
         const bool upper = (lane & sw) != 0;
 #pragma unroll
         for (int i = 0; i < sw; ++i) {
@@ -275,15 +267,11 @@ __device__ __forceinline__ bool router_rows(const RouterParams& p, int ei, int r
     }
     red[warp][lane] = acc[0];
     __syncthreads();
-    // output o = expert * R + row: the warps' sums added in warp order, then the FP64 sigmoid.
-    // The outputs go to the first NO / 4 lanes of warps 0..3 (one per SM sub-partition), so
-    // that their double-precision exps share four FP64 pipes instead of queueing on one.
-    if (warp < 4 && lane < NO / 4) {
-        const int o = warp * (NO / 4) + lane;
-        const int e = e0 + o / R, m = o % R;
-        float lg = red[0][o];
+    if (threadIdx.x < 32) {
+        const int e = e0 + threadIdx.x / R, m = threadIdx.x % R;
+        float lg = red[0][threadIdx.x];
 #pragma unroll
-        for (int w = 1; w < NW; ++w) lg += red[w][o];
+        for (int w = 1; w < NW; ++w) lg += red[w][threadIdx.x];
         if (m < M && e < E) {
             p.scores[(size_t)(m0 + m) * E + e] = (float)(1.0 / (1.0 + exp(-(double)lg)));
             if (p.logits_out) p.logits_out[(size_t)(m0 + m) * E + e] = lg;
@@ -293,7 +281,7 @@ __device__ __forceinline__ bool router_rows(const RouterParams& p, int ei, int r
 }
 
 __global__ void __launch_bounds__(kRouteThreads) k_router_rows(RouterParams p) {
-    router_rows<kRouterEPC, 8, kRouteThreads / 32>(p, blockIdx.x, blockIdx.y, blockIdx.y * gridDim.x + blockIdx.x,
+    router_rows<4, 8, kRouteThreads / 32>(p, blockIdx.x, blockIdx.y, blockIdx.y * gridDim.x + blockIdx.x,
                                           gridDim.x * gridDim.y);
 }
 
@@ -339,21 +327,6 @@ __device__ __forceinline__ void block_scan4(int4 v, int4* out_excl, int4* total,
     __syncthreads();
 }
 
-// A lane's best candidate of its kMaxE / 32 keys (expert lane + 32 i in slot i): the largest
-// key, and among equal keys the lowest slot (the lower expert), found by a 4-level tree over
-// (key, 15 - i) packed in 64 bits. Taken or absent slots hold key 0.
-__device__ __forceinline__ uint64_t lane_best(const uint32_t (&ku)[kMaxE / 32]) {
-    static_assert(kMaxE / 32 == 16, "16 slots per lane");
-    uint64_t v[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = ((uint64_t)ku[i] << 4) | (uint64_t)(15 - i);
-#pragma unroll
-    for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-        for (int i = 0; i < w; ++i) v[i] = v[i] > v[i + w] ? v[i] : v[i + w];
-    return v[0];
-}
-
 // a2: the top-k of row m by one warp (the warp's lanes hold experts lane + 32 i); writes
 // topk_idx / topk_w of the row and, when s_topk is given, the ids into it too.
 __device__ __forceinline__ void topk_row(const TopkRouteParams& p, int m, int lane, int* s_topk) {
@@ -375,16 +348,19 @@ __device__ __forceinline__ void topk_row(const TopkRouteParams& p, int m, int la
         ku[i] = valid ? key_u32(p.bias ? __fadd_rn(sc[i], bi[i]) : sc[i]) : 0u;
         if (!valid) sc[i] = 0.0f;
     }
-    // this lane's best: largest key, lowest index among equals
-    uint64_t best = lane_best(ku);
-    uint32_t lb = (uint32_t)(best >> 4);
-    int li = 15 - (int)(best & 15u);
+    // this lane's best: largest key, lowest index among equals (ascending scan)
+    uint32_t lb = 0u;
+    int li = 0;
+    float ls = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kMaxE / 32; ++i)
+        if (ku[i] > lb) { lb = ku[i]; li = i; ls = sc[i]; }
     int my_idx = 0;
     float my_sc = 0.0f;
     float ssum = 0.0f;  // fp32 in slot order: FP64 is ~50x slower than fp32 on this part
     // Each round: one max reduction and one ballot find the winning lane (a tie between
-    // lanes, which needs the lower expert id, takes one more reduction); the winner takes
-    // its next best (a tree, not a scan) while the others read its id and score.
+    // lanes, which needs the lower expert id, takes one more reduction); the winner
+    // rescans its own keys while the others read its id and score.
     for (int j = 0; j < k; ++j) {
         const uint32_t wmax = __reduce_max_sync(0xffffffffu, lb);
         const uint32_t bal = __ballot_sync(0xffffffffu, lb == wmax);
@@ -395,19 +371,18 @@ __device__ __forceinline__ void topk_row(const TopkRouteParams& p, int m, int la
             const uint32_t cand = (lb == wmax) ? (uint32_t)(lane + 32 * li) : 0xffffffffu;
             wl = (int)(__reduce_min_sync(0xffffffffu, cand) & 31u);
         }
-        float ls = 0.0f;  // this lane's candidate's score
-#pragma unroll
-        for (int i = 0; i < kMaxE / 32; ++i)
-            if (i == li) ls = sc[i];
         const int wsl = __shfl_sync(0xffffffffu, li, wl);
         const float wsc = __shfl_sync(0xffffffffu, ls, wl);
         if (lane == wl) {
 #pragma unroll
             for (int i = 0; i < kMaxE / 32; ++i)
                 if (i == li) ku[i] = 0u;
-            best = lane_best(ku);
-            lb = (uint32_t)(best >> 4);
-            li = 15 - (int)(best & 15u);
+            lb = 0u;
+            li = 0;
+            ls = 0.0f;
+#pragma unroll
+            for (int i = 0; i < kMaxE / 32; ++i)
+                if (ku[i] > lb) { lb = ku[i]; li = i; ls = sc[i]; }
         }
         ssum = __fadd_rn(ssum, wsc);
         if (lane == j) { my_idx = wl + 32 * wsl; my_sc = wsc; }
@@ -593,7 +568,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) k_front(FrontParams f) {
     __shared__ int s_last;
     const RouterParams& r = f.r;
     const TopkRouteParams& t = f.t;
-    const int nE = (r.E + kRouterEPC - 1) / kRouterEPC, nRB = (r.M + 7) / 8, nr = nE * nRB;
+    const int nE = (r.E + 3) / 4, nRB = (r.M + 7) / 8, nr = nE * nRB;
     if ((int)blockIdx.x >= nr) {
         pdl_wait();
         pdl_trigger();
@@ -601,7 +576,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) k_front(FrontParams f) {
         return;
     }
     const int rj = blockIdx.x / nE;
-    if (!router_rows<kRouterEPC, 8, kRouteThreads / 32>(r, blockIdx.x % nE, rj, blockIdx.x, nr)) return;
+    if (!router_rows<4, 8, kRouteThreads / 32>(r, blockIdx.x % nE, rj, blockIdx.x, nr)) return;
     // the last router CTA of the row block takes its rows' top-k (the other CTAs' scores
     // through L2)
     __threadfence();

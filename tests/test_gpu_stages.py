@@ -216,10 +216,10 @@ def test_stages_against_oracle(name, M):
     assert torch.equal(out2, t["out"]) and torch.equal(res2, res)
 
 
-# The GEMV runs in CTAs of 2 experts x 8 rows over the whole of H. (H, E, M): one row block
-# (1, 5, 8 rows), several with a ragged last one (16, 33, 48 rows), an odd E (61), the
-# 256-expert layers' shapes, and 64 rows of the 512-expert layer up to H 8192.
-ROUTER_CASES = [(4096, 64, 33), (4096, 64, 1), (4096, 61, 5), (4096, 64, 8), (4096, 62, 16), (7168, 256, 8),
+# The GEMV runs in CTAs of 4 experts x 8 rows over the whole of H. (H, E, M): one row block
+# (1, 5, 8 rows), several with a ragged last one (16, 33, 48 rows), E not a multiple of 4
+# (60, 62), the 256-expert layers' shapes, and 64 rows of the 512-expert layer up to H 8192.
+ROUTER_CASES = [(4096, 64, 33), (4096, 64, 1), (4096, 60, 5), (4096, 64, 8), (4096, 62, 16), (7168, 256, 8),
                 (6144, 256, 16), (7168, 256, 48), (4096, 512, 64), (8192, 512, 64)]
 
 
