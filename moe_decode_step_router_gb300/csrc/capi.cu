@@ -463,7 +463,7 @@ moe_status launch_gemm(int mode, const moe_layer_desc* d, const moe_qweight* w13
     float* part = reinterpret_cast<float*>(ws + L.partials);
     p.partials[0] = part;
     // in one launch both GEMMs cut units at once: down uses the pool's slots (no pool then)
-    p.partials[1] = mode == 2 ? part + (size_t)kGemmSlots * kPartialFloats : part;
+    p.partials[1] = mode == 2 ? part + (size_t)kPoolSlot0 * kPartialFloats : part;
     p.sched = reinterpret_cast<int32_t*>(ws + L.sched) + 2 * (mode == 1 ? 1 : 0);
     p.gu_done = reinterpret_cast<int32_t*>(ws + L.gu_done);
     p.swiglu_limit = d->swiglu_limit > 0.0f ? d->swiglu_limit : 0.0f;

@@ -84,40 +84,33 @@ struct Ring {
     }
 };
 
-// Static part: this CTA's contiguous range of the steps of one part of a GEMM's units:
-// the routed units of groups [g_lo, g_hi) in group order, then (when the part has them)
-// the shared expert's units, cut into G equal contiguous ranges (stream-K); at most the
-// first T_max steps. The position is advanced incrementally (no divisions after the start)
-// and each group record is loaded one group ahead.
+// Static part: this CTA's contiguous range of the steps of units [0, U0) (routed units in
+// group order, then the shared expert's units). The position is advanced incrementally (no
+// divisions after the start) and each group record is loaded one group ahead.
 struct Walker {
     const Group* groups;
     long long T_r, T, t, t1;
-    int gemm, ngroups, g_lo, g_hi, MB0, KS0, MB1, KS1, M, ktop;
-    int slot0;         // the part's first partial-sum slot (two per CTA)
+    int gemm, ngroups, MB0, KS0, MB1, KS1, M, ktop;
     int cls, g, b, k;  // position of step t
     int4 cur, nxt;     // records of groups g and g + 1
-    // Steps of the part: groups [glo, ghi) and, with with_sh, the shared expert's units.
-    __device__ static long long part_steps(const GemmParams& p, int gm, int glo, int ghi, bool with_sh) {
-        return (long long)(ghi - glo) * p.cls[gm][0].MB * p.cls[gm][0].KS +
-               (with_sh && p.has_shared ? (long long)p.cls[gm][1].MB * p.cls[gm][1].KS : 0);
+    // Steps of units [0, U0) of GEMM gm.
+    __device__ static long long steps_before(const GemmParams& p, int gm, int ngroups, int U0) {
+        const int NRU = ngroups * p.cls[gm][0].MB;
+        return U0 <= NRU ? (long long)U0 * p.cls[gm][0].KS
+                         : (long long)NRU * p.cls[gm][0].KS + (long long)(U0 - NRU) * p.cls[gm][1].KS;
     }
-    __device__ void init(const GemmParams& p, int gm, int ngroups_, int glo, int ghi, bool with_sh, long long T_max,
-                         int G, int c, int slot0_) {
+    __device__ void init(const GemmParams& p, int gm, int ngroups_, int G, int c, int U0) {
         groups = p.groups;
         gemm = gm;
         ngroups = ngroups_;
-        g_lo = glo;
-        g_hi = ghi;
-        slot0 = slot0_;
         MB0 = p.cls[gm][0].MB;
         KS0 = p.cls[gm][0].KS;
         MB1 = p.cls[gm][1].MB;
         KS1 = p.cls[gm][1].KS;
         M = p.M;
         ktop = p.k;
-        T_r = (long long)(ghi - glo) * MB0 * KS0;
-        T = part_steps(p, gm, glo, ghi, with_sh);
-        if (T > T_max) T = T_max;
+        T_r = (long long)ngroups * MB0 * KS0;
+        T = steps_before(p, gm, ngroups, U0);
         t = t1 = 0;
         if (c >= G || T == 0) return;
         seek((long long)c * T / G, (long long)(c + 1) * T / G);
@@ -132,13 +125,12 @@ struct Walker {
             g = (int)(u / MB0);
             b = (int)(u - (long long)g * MB0);
             k = (int)(t - u * KS0);
-            g += g_lo;
             cur = ld_group(groups + g);
-            nxt = ld_group(groups + (g + 1 < g_hi ? g + 1 : g));
+            nxt = ld_group(groups + (g + 1 < ngroups ? g + 1 : g));
         } else {
             const long long tt = t - T_r;
             cls = 1;
-            g = g_hi;
+            g = ngroups;
             b = (int)(tt / KS1);
             k = (int)(tt - (long long)b * KS1);
         }
@@ -177,10 +169,10 @@ struct Walker {
             // the unit its range starts in and the one it ends in)
             const int c_first = cta_of(us, G), c_last = cta_of(us + KS - 1, G);
             w.np = c_last - c_first + 1;
-            w.s0 = slot0 + 2 * c_first + (start(c_first, G) < us ? 1 : 0);
-            w.sb = slot0 + 2 * c_first;
+            w.s0 = 2 * c_first + (start(c_first, G) < us ? 1 : 0);
+            w.sb = 2 * c_first;
             w.sstride = 2;
-            w.myslot = slot0 + 2 * c + ((c == c_first && start(c, G) < us) ? 1 : 0);
+            w.myslot = 2 * c + ((c == c_first && start(c, G) < us) ? 1 : 0);
         }
         t += w.kb - w.ka;
         k = w.kb;
@@ -189,11 +181,11 @@ struct Walker {
             if (++b == (cls ? MB1 : MB0)) {
                 b = 0;
                 if (cls == 0) {
-                    if (++g == g_hi) {
+                    if (++g == ngroups) {
                         cls = 1;
                     } else {
                         cur = nxt;
-                        nxt = ld_group(groups + (g + 1 < g_hi ? g + 1 : g));
+                        nxt = ld_group(groups + (g + 1 < ngroups ? g + 1 : g));
                     }
                 }
             }
@@ -664,30 +656,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_expert_gemm(const __grid_co
                     prefetch_l2(C1.w + o, (uint32_t)(b1 - o < 65536 ? b1 - o : 65536));
             }
             const int Up = pool_of(gm), U0 = units_of(gm) - Up;  // [0, U0) static, [U0, U) pool
-            const bool deps = gm == 1 && p.mode == 2;  // down items after gate_up in one launch
-            // The static units in two parts, each cut into equal ranges over all CTAs: the
-            // first half of the groups, then the second half and the shared expert. In the
-            // one-launch FFN a CTA thus reaches the first part's down items long after every
-            // CTA has finished that part's FC1, and the second part's FC1 finishes while the
-            // first part's down items run: no CTA waits at the switch from FC1 to FC2. With
-            // a counter-fed pool the static units are one part.
-            const int nparts = (Up > 0 || ngroups < 2) ? 1 : 2;
-            for (int q = 0; ok && q < nparts; ++q) {
-                const int glo = q == 0 ? 0 : ngroups / 2, ghi = (nparts == 1 || q == 1) ? ngroups : ngroups / 2;
-                const bool with_sh = q == nparts - 1;
-                long long Tq = Walker::part_steps(p, gm, glo, ghi, with_sh);
-                if (nparts == 1) {  // the pool's units are the list's last ones
-                    const int NRU = ngroups * p.cls[gm][0].MB;
-                    const long long Tst = U0 <= NRU ? (long long)U0 * p.cls[gm][0].KS
-                                                    : (long long)NRU * p.cls[gm][0].KS +
-                                                          (long long)(U0 - NRU) * p.cls[gm][1].KS;
-                    Tq = Tq < Tst ? Tq : Tst;
-                }
-                // never more CTAs than steps, so every working CTA owns at least one step and
-                // the CTAs whose ranges meet a unit are exactly its pieces
-                const int G = (int)((long long)gridDim.x < Tq ? (long long)gridDim.x : Tq);
+            const long long Tst = Walker::steps_before(p, gm, ngroups, U0);
+            // static part: never more CTAs than steps, so every working CTA owns at least one
+            // step and the CTAs whose ranges meet a unit are exactly its pieces
+            const int G = (int)((long long)gridDim.x < Tst ? (long long)gridDim.x : Tst);
+            {
                 Walker wk;
-                wk.init(p, gm, ngroups, glo, ghi, with_sh, Tq, G, c, q * 2 * kMaxGemmCtas);
+                wk.init(p, gm, ngroups, G, c, U0);
+                const bool deps = gm == 1 && p.mode == 2;  // down items after gate_up in one launch
                 while (ok && wk.next(it, G, c)) ok = issue(it, deps ? ((it.cls & 1) ? kMaxE : it.gidx) : -1);
             }
             if (ok && Up > 0) {

@@ -18,15 +18,12 @@ constexpr int kAtomBytes = 512;      // scale atom: 128 rows x 4 bytes
 constexpr int kMaxGemmCtas = 160;    // GEMM grid cap (one CTA per SM); partial-sum slots are sized for it
 constexpr int kPartialFloats = kMaxRows * kBlockRows;  // one partial sum of a unit piece
 constexpr int kMaxPieces = 4;        // pieces of a unit cut in the dynamic pool
-constexpr int kPoolSlot0 = 2 * kMaxGemmCtas;  // one static part: 2 slots per CTA; then the pool's
-constexpr int kGemmSlots = 4 * kMaxGemmCtas;  // slots of one GEMM: two static parts of 2 per CTA
-// Partial-sum slots of a workspace: a GEMM's static ranges come in two parts, 2 slots per CTA
-// each ([0, kGemmSlots)); with a counter-fed schedule a single-GEMM launch has one static
-// part ([0, kPoolSlot0)) and the pool's kMaxPieces per CTA after it; the one-launch FFN uses
-// [0, kGemmSlots) for gate_up and the next kGemmSlots for down.
+constexpr int kPoolSlot0 = 2 * kMaxGemmCtas;  // static ranges: 2 slots per CTA; then the pool's
+// Partial-sum slots of a workspace: a single-GEMM launch uses [0, kPoolSlot0) for its
+// static ranges and, with a counter-fed schedule, the pool's kMaxPieces per CTA after them;
+// the one-launch FFN uses [0, kPoolSlot0) for gate_up and the next kPoolSlot0 for down.
 __host__ __device__ inline int partial_slots(int schedule) {
-    (void)schedule;
-    return 2 * kGemmSlots;
+    return kPoolSlot0 + (schedule == MOE_SCHED_STATIC ? kPoolSlot0 : kMaxPieces * kMaxGemmCtas);
 }
 constexpr int kGemmQueue = 16;       // work items in flight between a CTA's roles
 constexpr int kMaxStages = 16;       // ring slots of the GEMM pipeline
