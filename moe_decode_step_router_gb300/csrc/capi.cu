@@ -227,6 +227,8 @@ RouterParams router_params(const moe_layer_desc* d, const void* x, const void* w
                            size_t l2_pf_bytes = 0, const void* l2_pf2 = nullptr, size_t l2_pf2_bytes = 0) {
     RouterParams p{};
     p.status = status;
+    p.wait_ns = kRouterWaitNs;
+    p.unreachable_tx = 0;
     p.l2_pf[0] = static_cast<const uint8_t*>(l2_pf);
     p.l2_pf_bytes[0] = l2_pf_bytes;
     p.l2_pf[1] = static_cast<const uint8_t*>(l2_pf2);
@@ -249,9 +251,11 @@ size_t router_smem(const moe_layer_desc* d, int M) { return (size_t)(4 + (M < 8 
 moe_status launch_router(const moe_layer_desc* d, const void* x, const void* w_gate, const float* logits_in, int M,
                          float* logits_out, float* scores, int32_t* status, cudaStream_t st,
                          const void* l2_pf = nullptr, size_t l2_pf_bytes = 0, const void* l2_pf2 = nullptr,
-                         size_t l2_pf2_bytes = 0) {
-    const RouterParams p = router_params(d, x, w_gate, logits_in, M, logits_out, scores, status, l2_pf, l2_pf_bytes,
-                                         l2_pf2, l2_pf2_bytes);
+                         size_t l2_pf2_bytes = 0, uint64_t wait_ns = kRouterWaitNs, uint32_t unreachable_tx = 0) {
+    RouterParams p = router_params(d, x, w_gate, logits_in, M, logits_out, scores, status, l2_pf, l2_pf_bytes, l2_pf2,
+                                   l2_pf2_bytes);
+    p.wait_ns = wait_ns;
+    p.unreachable_tx = unreachable_tx;
     DevInfo* di;
     moe_status s = dev_info(&di);
     if (s != MOE_OK) return s;
@@ -973,10 +977,12 @@ static uint8_t* noalloc_scratch(moe_status* st) {
     return addr[dev];
 }
 
-extern "C" moe_status moe_router_topk_noalloc(const moe_layer_desc* d, const void* x, const void* w_gate,
-                                              const float* bias, const float* logits_in, int M, float* logits_out,
-                                              int32_t* topk_idx, float* topk_w, void* xq, void* xq_scales,
-                                              void* xq_sh, void* xq_sh_scales, moe_stream_t stream) {
+// wait_ns and unreachable_tx: the router's copy waits (kRouterWaitNs and 0 but in the test of
+// the timeout path below).
+static moe_status router_topk_noalloc(const moe_layer_desc* d, const void* x, const void* w_gate, const float* bias,
+                                      const float* logits_in, int M, float* logits_out, int32_t* topk_idx,
+                                      float* topk_w, void* xq, void* xq_scales, void* xq_sh, void* xq_sh_scales,
+                                      moe_stream_t stream, uint64_t wait_ns, uint32_t unreachable_tx) {
     moe_status s = check_desc(d);
     if (s != MOE_OK) return s;
     REQUIRE(M >= 1 && M <= kMaxRows, "M=%d: need 1..%d", M, kMaxRows);
@@ -1003,7 +1009,7 @@ extern "C" moe_status moe_router_topk_noalloc(const moe_layer_desc* d, const voi
     cudaStream_t st = (cudaStream_t)stream;
     float* scores = reinterpret_cast<float*>(scratch + kNaScores);
     s = launch_router(d, x, w_gate, logits_in, M, logits_out, scores, reinterpret_cast<int32_t*>(scratch + kNaHeader),
-                      st);
+                      st, nullptr, 0, nullptr, 0, wait_ns, unreachable_tx);
     if (s != MOE_OK) return s;
     QuantArgs qa;
     qa.x = x;
@@ -1017,6 +1023,32 @@ extern "C" moe_status moe_router_topk_noalloc(const moe_layer_desc* d, const voi
                           nullptr, st, qa);
     if (s != MOE_OK) return s;
     return ok();
+}
+
+extern "C" moe_status moe_router_topk_noalloc(const moe_layer_desc* d, const void* x, const void* w_gate,
+                                              const float* bias, const float* logits_in, int M, float* logits_out,
+                                              int32_t* topk_idx, float* topk_w, void* xq, void* xq_scales,
+                                              void* xq_sh, void* xq_sh_scales, moe_stream_t stream) {
+    return router_topk_noalloc(d, x, w_gate, bias, logits_in, M, logits_out, topk_idx, topk_w, xq, xq_scales, xq_sh,
+                               xq_sh_scales, stream, kRouterWaitNs, 0);
+}
+
+// Test of the allocation-free router's timeout path, not part of the public ABI (the header
+// does not declare it): moe_router_topk_noalloc with the router GEMV's gate-row barrier
+// expecting 16 bytes that no copy brings and its copy waits limited to wait_ns, so every
+// router CTA gives up after wait_ns, records the timeout in the scratch header, waits for its
+// real copies and returns without writing scores; the top-k launch then gives every row -1
+// ids and zero weights and clears the record. Needs w_gate (no logits_in).
+moe_status moe_internal_router_noalloc_unreachable_wait(const moe_layer_desc* d, const void* x, const void* w_gate,
+                                                        const float* bias, int M, float* logits_out,
+                                                        int32_t* topk_idx, float* topk_w, void* xq, void* xq_scales,
+                                                        void* xq_sh, void* xq_sh_scales, uint64_t wait_ns,
+                                                        moe_stream_t stream) {
+    REQUIRE(wait_ns >= 1000000ull && wait_ns <= kRouterWaitNs, "wait_ns=%llu: need 1 ms .. 2 s",
+            (unsigned long long)wait_ns);
+    REQUIRE_PTR(w_gate, "w_gate");
+    return router_topk_noalloc(d, x, w_gate, bias, nullptr, M, logits_out, topk_idx, topk_w, xq, xq_scales, xq_sh,
+                               xq_sh_scales, stream, wait_ns, 16);
 }
 
 // Test of the GEMM's timeout path, not part of the public ABI (the header does not declare

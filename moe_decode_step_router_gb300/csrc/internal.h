@@ -88,7 +88,12 @@ struct RouterParams {
     int32_t* status;          // status word (MOE_ERR_TIMEOUT when a copy wait runs out)
     const uint8_t* l2_pf[2];  // bytes a later launch streams that do not depend on this one
     size_t l2_pf_bytes[2];    // (the shared expert's gate_up and down records): prefetched into L2
+    uint64_t wait_ns;         // limit of each copy wait (kRouterWaitNs)
+    uint32_t unreachable_tx;  // 0; a test of the timeout path makes the gate rows' barrier expect
+                              // this many bytes more than its copies bring, so its wait runs out
 };
+
+constexpr uint64_t kRouterWaitNs = 2000000000ull;  // 2 s: limit of the router's copy waits
 
 constexpr int kRouteThreads = 512;  // k_topk_route: 16 warps, one row each
 

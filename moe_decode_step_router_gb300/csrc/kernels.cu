@@ -177,8 +177,6 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(RouterParams p) {
 // (ei, rj): this CTA's expert group and row block; CTA cta of nct takes its share of the L2
 // prefetch. Returns false when a copy wait ran out (recorded in the status word; nothing
 // is written).
-constexpr uint64_t kRouterWaitNs = 2000000000ull;  // 2 s: limit of the router's copy waits
-
 template <int EPC, int R, int NW>
 __device__ __forceinline__ bool router_rows(const RouterParams& p, int ei, int rj, int cta, int nct) {
     static_assert(EPC * R == 32, "one output per lane");
@@ -199,7 +197,7 @@ __device__ __forceinline__ bool router_rows(const RouterParams& p, int ei, int r
         mbar_init(bar_w, 1);
         mbar_init(bar_x, 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(bar_w, (uint32_t)(EPC * H * 2));
+        mbar_arrive_expect_tx(bar_w, (uint32_t)(EPC * H * 2) + p.unreachable_tx);
         for (int r = 0; r < EPC; ++r)
             bulk_g2s(smem_u32(wsm + (size_t)r * H), p.wg + (size_t)min(e0 + r, E - 1) * H, (uint32_t)(H * 2), bar_w);
     }
@@ -219,14 +217,19 @@ __device__ __forceinline__ bool router_rows(const RouterParams& p, int ei, int r
         mbar_arrive_expect_tx(bar_x, (uint32_t)(M * H * 2));
         bulk_g2s(smem_u32(xsm), p.x + (size_t)m0 * H, (uint32_t)(M * H * 2), bar_x);
     }
-    bool ok = mbar_wait_bounded(bar_w, 0, &s_never, kRouterWaitNs);
-    ok = mbar_wait_bounded(bar_x, 0, &s_never, kRouterWaitNs) && ok;
+    bool ok = mbar_wait_bounded(bar_w, 0, &s_never, p.wait_ns);
+    ok = mbar_wait_bounded(bar_x, 0, &s_never, p.wait_ns) && ok;
     if (!__syncthreads_and(ok)) {
         // a copy did not land in time: record it, give the copies one more bounded wait so
         // that none still writes shared memory when the CTA leaves, and produce nothing
-        if (threadIdx.x == 0 && p.status) atomicCAS(p.status, 0, (int)MOE_ERR_TIMEOUT);
-        mbar_wait_bounded(bar_w, 0, &s_never, kRouterWaitNs / 2);
-        mbar_wait_bounded(bar_x, 0, &s_never, kRouterWaitNs / 2);
+        // (bytes a test asked for that no copy brings are counted first, so that this wait
+        // ends exactly when the real copies have landed)
+        if (threadIdx.x == 0) {
+            if (p.status) atomicCAS(p.status, 0, (int)MOE_ERR_TIMEOUT);
+            if (p.unreachable_tx) mbar_complete_tx(bar_w, p.unreachable_tx);
+        }
+        mbar_wait_bounded(bar_w, 0, &s_never, p.wait_ns / 2);
+        mbar_wait_bounded(bar_x, 0, &s_never, p.wait_ns / 2);
         return false;
     }
     float acc[32];

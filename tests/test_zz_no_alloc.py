@@ -7,7 +7,16 @@ inputs, it must give what moe_router_topk gives on the same inputs: the same exp
 weights, logits and quantised FC1 inputs (these are the same kernels, so the comparison is
 exact, which is within every tolerance the other tests use), up to the largest layer the
 descriptor allows.
+
+A library-internal call (not in the public header) also makes the router's copy wait run
+out on purpose (its gate-row barrier expects 16 bytes that no copy brings, with a 50 ms
+limit): the call must return on its own with every expert id -1 and every weight 0 rather
+than a top-k of stale scores, and the next ordinary call must give the results of one on a
+fresh library (the timeout record is cleared).
 """
+import ctypes
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -82,3 +91,45 @@ def test_noalloc_with_given_logits_twice():
         _same(ref, got)
 
 
+def _router_unreachable_wait():
+    f = ms.lib().moe_internal_router_noalloc_unreachable_wait
+    P = ctypes.c_void_p
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.POINTER(ms.LayerDesc), P, P, P, ctypes.c_int, P, P, P, P, P, P, P, ctypes.c_uint64, P]
+    return f
+
+
+@pytest.mark.parametrize("name", ["nvfp4_e512", "mxfp8_bias"])
+def test_noalloc_router_wait_runs_out_then_recovers(name):
+    cfg = CASES[name]
+    M = cfg["M"]
+    d = ms.layer_desc(cfg, synth.act_global_scales(cfg))
+    inp = synth.make_inputs(cfg, 6, device="cuda", weights=False)
+    ref = _outputs(cfg, M)
+    ms.moe_router_topk_noalloc(d, inp["x"], inp["wg"], inp["bias"], None, M, ref["logits"], ref["idx"], ref["w"],
+                               ref["xq"], ref["xs"], ref["xq_sh"], ref["xs_sh"])
+    torch.cuda.synchronize()
+    assert (ref["idx"] >= 0).all() and (ref["w"] > 0).all()
+    got = _outputs(cfg, M)
+    got["idx"].fill_(3)  # what a caller's buffers hold from an earlier step
+    got["w"].fill_(0.5)
+    t0 = time.perf_counter()
+    st = _router_unreachable_wait()(ctypes.byref(d), ms._ptr(inp["x"]), ms._ptr(inp["wg"]), ms._ptr(inp["bias"]), M,
+                                    ms._ptr(got["logits"]), ms._ptr(got["idx"]), ms._ptr(got["w"]), ms._ptr(got["xq"]),
+                                    ms._ptr(got["xs"]), ms._ptr(got["xq_sh"]), ms._ptr(got["xs_sh"]), 50_000_000,
+                                    ms._stream(None))
+    assert st == ms.MOE_OK, ms.lib().moe_last_error_string().decode()
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert 0.04 < dt < 1.5, "the call took %.3f s" % dt
+    assert (got["idx"] == -1).all() and (got["w"] == 0).all()
+    assert (got["logits"] == -1.0).all()  # the router wrote nothing
+    for q in ("xq", "xs", "xq_sh", "xs_sh"):  # the FC1 inputs do not depend on the router
+        assert torch.equal(got[q], ref[q]), q
+    assert torch.ones(4, device="cuda").sum().item() == 4.0  # the context is still usable
+    for _ in range(2):
+        again = _outputs(cfg, M)
+        ms.moe_router_topk_noalloc(d, inp["x"], inp["wg"], inp["bias"], None, M, again["logits"], again["idx"],
+                                   again["w"], again["xq"], again["xs"], again["xq_sh"], again["xs_sh"])
+        torch.cuda.synchronize()
+        _same(ref, again)
