@@ -351,19 +351,30 @@ __device__ __forceinline__ void topk_row(const TopkRouteParams& p, int m, int la
         ku[i] = valid ? key_u32(p.bias ? __fadd_rn(sc[i], bi[i]) : sc[i]) : 0u;
         if (!valid) sc[i] = 0.0f;
     }
-    // this lane's best: largest key, lowest index among equals (ascending scan)
-    uint32_t lb = 0u;
-    int li = 0;
-    float ls = 0.0f;
+    // Lane-local order: larger key first, lower index among equal keys. Each lane keeps its
+    // first element in that order (best) and the one after it (second); a lane whose best is
+    // taken promotes its second, and scans its keys again only when it has no second left
+    // (from its second win on), for the elements after the one just taken. So most rounds
+    // cost one max reduction, one ballot and two shuffles, not a scan.
+    uint32_t lb = 0u, l2 = 0u;
+    int li = 0, i2 = 0;
+    float ls = 0.0f, s2 = 0.0f;
 #pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i)
-        if (ku[i] > lb) { lb = ku[i]; li = i; ls = sc[i]; }
+    for (int i = 0; i < kMaxE / 32; ++i) {
+        if (ku[i] > lb) {
+            l2 = lb; i2 = li; s2 = ls;
+            lb = ku[i]; li = i; ls = sc[i];
+        } else if (ku[i] > l2) {
+            l2 = ku[i]; i2 = i; s2 = sc[i];
+        }
+    }
+    bool has2 = true;
     int my_idx = 0;
     float my_sc = 0.0f;
     float ssum = 0.0f;  // fp32 in slot order: FP64 is ~50x slower than fp32 on this part
     // Each round: one max reduction and one ballot find the winning lane (a tie between
-    // lanes, which needs the lower expert id, takes one more reduction); the winner
-    // rescans its own keys while the others read its id and score.
+    // lanes, which needs the lower expert id, takes one more reduction); the winner moves on
+    // to its next element while the others read its id and score.
     for (int j = 0; j < k; ++j) {
         const uint32_t wmax = __reduce_max_sync(0xffffffffu, lb);
         const uint32_t bal = __ballot_sync(0xffffffffu, lb == wmax);
@@ -377,15 +388,26 @@ __device__ __forceinline__ void topk_row(const TopkRouteParams& p, int m, int la
         const int wsl = __shfl_sync(0xffffffffu, li, wl);
         const float wsc = __shfl_sync(0xffffffffu, ls, wl);
         if (lane == wl) {
+            if (has2) {
+                lb = l2; li = i2; ls = s2;
+                has2 = false;
+            } else {
+                // the elements after the taken one (key lt, index lti) in the lane's order
+                const uint32_t lt = lb;
+                const int lti = li;
+                lb = 0u; l2 = 0u; li = 0; i2 = 0; ls = 0.0f; s2 = 0.0f;
 #pragma unroll
-            for (int i = 0; i < kMaxE / 32; ++i)
-                if (i == li) ku[i] = 0u;
-            lb = 0u;
-            li = 0;
-            ls = 0.0f;
-#pragma unroll
-            for (int i = 0; i < kMaxE / 32; ++i)
-                if (ku[i] > lb) { lb = ku[i]; li = i; ls = sc[i]; }
+                for (int i = 0; i < kMaxE / 32; ++i) {
+                    const uint32_t kv = (ku[i] < lt || (ku[i] == lt && i > lti)) ? ku[i] : 0u;
+                    if (kv > lb) {
+                        l2 = lb; i2 = li; s2 = ls;
+                        lb = kv; li = i; ls = sc[i];
+                    } else if (kv > l2) {
+                        l2 = kv; i2 = i; s2 = sc[i];
+                    }
+                }
+                has2 = true;
+            }
         }
         ssum = __fadd_rn(ssum, wsc);
         if (lane == j) { my_idx = wl + 32 * wsl; my_sc = wsc; }
