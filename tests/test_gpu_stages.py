@@ -311,6 +311,45 @@ def _tie_logits(M, E, k, rng):
     return lg
 
 
+def _one_lane_logits(M, E, k, rng):
+    """Rows whose top keys sit in one or two lanes of the top-k warp (experts e with the same
+    e % 32), so one lane wins round after round: its next-best key is promoted, then its keys
+    are scanned again after the one just taken, many times over. Some rows repeat a key inside
+    the lane (exact ties in the lane's own order) or tie a lane key with another lane's."""
+    lg = rng.standard_normal((M, E)).astype(np.float32)
+    per_lane = E // 32
+    for m in range(M):
+        lanes = [m % 32] if k <= per_lane else [m % 32, (m + 7) % 32]
+        ids = [ln + 32 * i for ln in lanes for i in range(per_lane)][:k + 2]
+        vals = np.float32(6.0) + rng.permutation(len(ids)).astype(np.float32) * np.float32(0.25)
+        if m % 3 == 1:
+            vals[::3] = np.float32(7.0)  # equal keys within the lane, several of them
+        lg[m, ids] = vals
+        if m % 3 == 2:
+            lg[m, (m + 1) % 32] = lg[m, ids[0]]  # a key of another lane equal to one of these
+    return lg
+
+
+@pytest.mark.parametrize("E,k", [(512, 16), (512, 10), (256, 16), (256, 8)])
+def test_topk_when_one_lane_holds_the_top_keys(E, k):
+    M = 24
+    cfg = synth.config("tiny_mxfp8", E=E, k=k, has_bias=False, rsf=1.0)
+    inp, layer = make(cfg, seed=5, M=M)
+    li = _one_lane_logits(M, E, k, np.random.default_rng(E * 31 + k))
+    t = _alloc(layer, M)
+    ms.moe_router_topk(layer.d, inp["x"], inp["wg"], None, torch.from_numpy(li).cuda(), M, t["logits"], t["idx"],
+                       t["w"], t["xq"], t["xs"], t["xq_sh"], t["xs_sh"], layer.ws)
+    torch.cuda.synchronize()
+    L = oracle_layer(cfg, inp)
+    _, _, oidx, ow, _ = oracle.router(L, u16(inp["x"]), u16(inp["wg"]), logits_in=li)
+    gidx = npy(t["idx"])
+    assert (gidx == oidx).all(), "rows %s differ" % np.nonzero((gidx != oidx).any(1))[0]
+    assert np.allclose(npy(t["w"]), ow, rtol=2 ** -20, atol=0)
+    # the rows are what they claim to be: most of each row's top-k share one lane
+    share = [np.bincount(oidx[m] % 32).max() for m in range(M)]
+    assert min(share) >= min(k, E // 32) - 2
+
+
 @pytest.mark.parametrize("E,k,bias", [(256, 8, False), (256, 8, True), (512, 10, True), (512, 10, False)])
 def test_topk_ties_go_to_the_lower_index(E, k, bias):
     M = 12
