@@ -244,9 +244,9 @@ RouterParams router_params(const moe_layer_desc* d, const void* x, const void* w
     return p;
 }
 
-// Dynamic shared memory of a router CTA: its 4 gate rows and up to 8 x rows of H bf16
-// ((4 + 8) * H * 2 <= 192 KB).
-size_t router_smem(const moe_layer_desc* d, int M) { return (size_t)(4 + (M < 8 ? M : 8)) * d->H * 2; }
+// Dynamic shared memory of a router CTA: its 4 gate rows and up to 8 x rows of H bf16, each
+// padded by 8 elements ((4 + 8) * (H + 8) * 2 <= 192.2 KB).
+size_t router_smem(const moe_layer_desc* d, int M) { return (size_t)(4 + (M < 8 ? M : 8)) * (d->H + 8) * 2; }
 
 moe_status launch_router(const moe_layer_desc* d, const void* x, const void* w_gate, const float* logits_in, int M,
                          float* logits_out, float* scores, int32_t* status, cudaStream_t st,
@@ -275,6 +275,9 @@ moe_status launch_router(const moe_layer_desc* d, const void* x, const void* w_g
     // the logits are given: scores only
     return launch_pdl(k_router, dim3((M * d->E + 255) / 256), dim3(256), 0, st, p, "k_router launch");
 }
+
+// CTAs of a step's top-k launch that prefetch the shared expert's records into L2.
+constexpr int kTopkPrefetchCtas = 64;
 
 // FC1 input quantisation arguments, carried by the top-k launch (CTAs 1..).
 struct QuantArgs {
@@ -889,6 +892,9 @@ moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void
     qa.xs = w + L.xs;
     qa.xq_sh = w + L.xq_sh;
     qa.xs_sh = w + L.xs_sh;
+    // one front launch: its router CTAs prefetch the shared expert; two launches: the top-k
+    // launch's extra CTAs do (the router CTAs then leave as soon as their logits are out)
+    const bool one_front = d->front_launches == 1;
     const RouterParams rp = router_params(d, a->x, a->w_gate, nullptr, M, logits, scores,
                                           reinterpret_cast<int32_t*>(w + L.header), sh13_w, sh13_bytes, sh2_w,
                                           sh2_bytes);
@@ -897,14 +903,22 @@ moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void
                                            reinterpret_cast<int32_t*>(w + L.counts), perm, inv_perm,
                                            reinterpret_cast<int32_t*>(w + L.tiles),
                                            reinterpret_cast<int32_t*>(w + L.num_tiles), qa, &qctas);
-    if (d->front_launches == 1) {
+    if (one_front) {
         s = launch_front(d, rp, tp, qctas, L, w, M, st);
         if (s != MOE_OK) return s;
     } else {
-        s = launch_router(d, a->x, a->w_gate, nullptr, M, logits, scores, reinterpret_cast<int32_t*>(w + L.header), st,
-                          sh13_w, sh13_bytes, sh2_w, sh2_bytes);
+        s = launch_router(d, a->x, a->w_gate, nullptr, M, logits, scores, reinterpret_cast<int32_t*>(w + L.header), st);
         if (s != MOE_OK) return s;
-        s = launch_pdl(k_topk_route, dim3(tp.topk_ctas + qctas), dim3(kRouteThreads), 0, st, tp, "k_topk_route launch");
+        TopkRouteParams tpp = tp;
+        if (d->has_shared) {
+            tpp.l2_pf[0] = static_cast<const uint8_t*>(sh13_w);
+            tpp.l2_pf_bytes[0] = sh13_bytes;
+            tpp.l2_pf[1] = static_cast<const uint8_t*>(sh2_w);
+            tpp.l2_pf_bytes[1] = sh2_bytes;
+            tpp.pf_ctas = kTopkPrefetchCtas;
+        }
+        s = launch_pdl(k_topk_route, dim3(tpp.topk_ctas + qctas + tpp.pf_ctas), dim3(kRouteThreads), 0, st, tpp,
+                       "k_topk_route launch");
         if (s != MOE_OK) return s;
     }
     GemmBuffers b{};

@@ -117,6 +117,12 @@ struct TopkRouteParams {
     int H, fmt_r, fmt_s, quant_shared;
     uint8_t *xq, *xs, *xq_sh, *xs_sh;
     float gs_r, gs_s;
+    // the last pf_ctas CTAs of the launch (0: none) prefetch these bytes into L2 (records a
+    // later launch streams that do not depend on the routing), 128-byte lines spread over
+    // their threads
+    const uint8_t* l2_pf[2];
+    size_t l2_pf_bytes[2];
+    int pf_ctas;
 };
 
 // k_front: the router launch's and the top-k launch's parameters, plus the per-row-block

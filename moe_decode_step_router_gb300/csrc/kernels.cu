@@ -148,6 +148,11 @@ __device__ __forceinline__ int quant_units(int fmt, int Mpad, int H) {
 }
 
 // ------------------------------------------------------------------------------------
+// One 128-byte line into L2 (no data returned, no copy engine involved).
+__device__ __forceinline__ void prefetch_line_l2(const void* src) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(src) : "memory");
+}
+
 // a2 with the logits given (moe_router_topk with logits_in): the fp32 sigmoid score,
 // evaluated in double and rounded once, as after the GEMV below.
 constexpr int kRouterThreads = 256;
@@ -167,19 +172,36 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(RouterParams p) {
 // a1 with no partial sums leaving the CTA: CTA (i, j) takes experts EPC i .. EPC i + EPC - 1
 // and rows R j .. R j + R - 1 over the whole of H. Their gate rows are copied into shared
 // memory (one bulk copy per row) before the dependency wait (they do not depend on earlier
-// launches), the x rows (one bulk copy) after it. Thread t takes the 16-byte chunks
-// t, t + NW * 32, ... of H for all EPC x R (expert, row) dot products; a warp then folds
-// its 32 partial sums by recursive halving, so that lane l ends with the warp's sum for
-// output l = expert * R + row, and thread l adds the NW warps' sums in warp order. The
-// order of every addition is fixed: the logits are deterministic, and the same in both
-// launches that run this (k_router_rows and k_front, both at NW = 16). The score is the
-// same fp32 sigmoid as in k_router (evaluated in double, rounded once).
+// launches), the x rows (one bulk copy per row) after it; rows are kRouterRowPad elements
+// apart beyond H, so that the fragment loads below hit 32 different banks.
+// The dot products run on the tensor cores as bf16 x bf16 -> fp32 products of 16-wide K
+// chunks (mma.sync m16n8k16): A holds the EPC gate rows (rows EPC..15 zero), B the R x rows
+// (one per column), so D's rows 0..EPC-1 are this CTA's logits. Warp w takes the K chunks
+// w, w + NW, ..., alternating between two accumulators; thread l then adds, for output
+// l = expert * R + row, the two accumulators of every warp in warp order. The order of every
+// addition is fixed: the logits are deterministic, and the same in both launches that run
+// this (k_router_rows and k_front, both at NW = 16). The score is the same fp32 sigmoid as in
+// k_router (evaluated in double, rounded once).
 // (ei, rj): this CTA's expert group and row block; CTA cta of nct takes its share of the L2
-// prefetch. Returns false when a copy wait ran out (recorded in the status word; nothing
-// is written).
+// prefetch (k_front only; in the two-launch front the top-k launch prefetches). Returns false
+// when a copy wait ran out (recorded in the status word; nothing is written).
+constexpr int kRouterRowPad = 8;  // bf16 elements between the end of a row and the next row
+
+// D += A B for one m16n8k16 tile: bf16 inputs, fp32 accumulators (register layouts of the
+// PTX ISA's mma fragments).
+__device__ __forceinline__ void mma_bf16_16816(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 template <int EPC, int R, int NW>
 __device__ __forceinline__ bool router_rows(const RouterParams& p, int ei, int rj, int cta, int nct) {
     static_assert(EPC * R == 32, "one output per lane");
+    static_assert(EPC <= 8 && R == 8, "A rows 0..EPC-1 and B columns 0..7 of one m16n8k16 tile");
     extern __shared__ __align__(16) uint16_t rrs[];
     __shared__ float red[NW][32];
     __shared__ __align__(8) uint64_t rbar[2];  // gate rows, x rows
@@ -188,9 +210,9 @@ __device__ __forceinline__ bool router_rows(const RouterParams& p, int ei, int r
     const int H = p.H, E = p.E;
     const int e0 = ei * EPC, m0 = rj * R;
     const int M = min(R, p.M - m0);          // rows of this CTA
-    const int V = H / 8;                     // 16-byte chunks per row
-    uint16_t* wsm = rrs;                     // [EPC][H]
-    uint16_t* xsm = rrs + (size_t)EPC * H;   // [M][H]: rows m0 ..
+    const int LD = H + kRouterRowPad;        // shared-memory row stride (elements)
+    uint16_t* wsm = rrs;                     // [EPC][LD]
+    uint16_t* xsm = rrs + (size_t)EPC * LD;  // [M][LD]: rows m0 ..
     const uint32_t bar_w = smem_u32(&rbar[0]), bar_x = smem_u32(&rbar[1]);
     if (threadIdx.x == 0) {
         s_never = 0;
@@ -199,7 +221,7 @@ __device__ __forceinline__ bool router_rows(const RouterParams& p, int ei, int r
         fence_mbar_init();
         mbar_arrive_expect_tx(bar_w, (uint32_t)(EPC * H * 2) + p.unreachable_tx);
         for (int r = 0; r < EPC; ++r)
-            bulk_g2s(smem_u32(wsm + (size_t)r * H), p.wg + (size_t)min(e0 + r, E - 1) * H, (uint32_t)(H * 2), bar_w);
+            bulk_g2s(smem_u32(wsm + (size_t)r * LD), p.wg + (size_t)min(e0 + r, E - 1) * H, (uint32_t)(H * 2), bar_w);
     }
     __syncthreads();  // the barriers are initialised before anyone waits on them
     if (threadIdx.x == 32) {
@@ -215,7 +237,8 @@ __device__ __forceinline__ bool router_rows(const RouterParams& p, int ei, int r
     pdl_wait();
     if (threadIdx.x == 0) {
         mbar_arrive_expect_tx(bar_x, (uint32_t)(M * H * 2));
-        bulk_g2s(smem_u32(xsm), p.x + (size_t)m0 * H, (uint32_t)(M * H * 2), bar_x);
+        for (int m = 0; m < M; ++m)
+            bulk_g2s(smem_u32(xsm + (size_t)m * LD), p.x + (size_t)(m0 + m) * H, (uint32_t)(H * 2), bar_x);
     }
     bool ok = mbar_wait_bounded(bar_w, 0, &s_never, p.wait_ns);
     ok = mbar_wait_bounded(bar_x, 0, &s_never, p.wait_ns) && ok;
@@ -232,43 +255,32 @@ __device__ __forceinline__ bool router_rows(const RouterParams& p, int ei, int r
         mbar_wait_bounded(bar_x, 0, &s_never, p.wait_ns / 2);
         return false;
     }
-    float acc[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
-    for (int c = threadIdx.x; c < V; c += blockDim.x) {
-        uint4 wv[EPC];
-#pragma unroll
-        for (int e = 0; e < EPC; ++e) wv[e] = *reinterpret_cast<const uint4*>(wsm + (size_t)e * H + 8 * c);
-#pragma unroll
-        for (int m = 0; m < R; ++m) {
-            if (m < M) {
-                const uint4 xv = *reinterpret_cast<const uint4*>(xsm + (size_t)m * H + 8 * c);
-#pragma unroll
-                for (int e = 0; e < EPC; ++e) {
-                    float a = acc[e * R + m];
-                    a = fmaf(bf16_lo(xv.x), bf16_lo(wv[e].x), a); a = fmaf(bf16_hi(xv.x), bf16_hi(wv[e].x), a);
-                    a = fmaf(bf16_lo(xv.y), bf16_lo(wv[e].y), a); a = fmaf(bf16_hi(xv.y), bf16_hi(wv[e].y), a);
-                    a = fmaf(bf16_lo(xv.z), bf16_lo(wv[e].z), a); a = fmaf(bf16_hi(xv.z), bf16_hi(wv[e].z), a);
-                    a = fmaf(bf16_lo(xv.w), bf16_lo(wv[e].w), a); a = fmaf(bf16_hi(xv.w), bf16_hi(wv[e].w), a);
-                    acc[e * R + m] = a;
-                }
-            }
-        }
+    // fragments: lane (g = lane / 4, t = lane % 4) holds A rows g (and g + 8: zero) at columns
+    // 2t, 2t + 1 and 2t + 8, 2t + 9 of the chunk, B column g at the same K, and D rows g,
+    // g + 8 at columns 2t, 2t + 1
+    const int g = lane >> 2, t = lane & 3;
+    const bool a_live = g < EPC, b_live = g < M;
+    const uint32_t* wrow = reinterpret_cast<const uint32_t*>(wsm + (size_t)(a_live ? g : 0) * LD) + t;
+    const uint32_t* xrow = reinterpret_cast<const uint32_t*>(xsm + (size_t)(b_live ? g : 0) * LD) + t;
+    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};  // chunks w + 2 i NW / w + (2 i + 1) NW
+    auto chunk = [&](int kc, float* d) {
+        const int o = kc * 8;  // 32-bit words before the chunk
+        const uint32_t a0 = a_live ? wrow[o] : 0u, a2 = a_live ? wrow[o + 4] : 0u;
+        const uint32_t b0 = b_live ? xrow[o] : 0u, b1 = b_live ? xrow[o + 4] : 0u;
+        mma_bf16_16816(d, a0, 0u, a2, 0u, b0, b1);
+    };
+    const int KC = H / 16;
+    int kc = warp;
+    for (; kc + NW < KC; kc += 2 * NW) {
+        chunk(kc, d0);
+        chunk(kc + NW, d1);
     }
-    pdl_trigger();  // let the top-k launch get scheduled while the sums are folded
-    // recursive halving: at the step of width s a lane keeps the half of its live values
-    // selected by its bit s and adds its partner's copy of that half
-#pragma unroll
-    for (int sw = 16; sw >= 1; sw >>= 1) {
-        const bool upper = (lane & sw) != 0;
-#pragma unroll
-        for (int i = 0; i < sw; ++i) {
-            const float send = upper ? acc[i] : acc[i + sw];
-            const float keep = upper ? acc[i + sw] : acc[i];
-            acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, sw);
-        }
+    if (kc < KC) chunk(kc, d0);
+    pdl_trigger();  // let the top-k launch get scheduled while the sums are added
+    if (a_live) {
+        red[warp][g * R + 2 * t] = d0[0] + d1[0];
+        red[warp][g * R + 2 * t + 1] = d0[1] + d1[1];
     }
-    red[warp][lane] = acc[0];
     __syncthreads();
     if (threadIdx.x < 32) {
         const int e = e0 + threadIdx.x / R, m = threadIdx.x % R;
@@ -524,11 +536,27 @@ __global__ void __launch_bounds__(kRouteThreads) k_topk_route(TopkRouteParams p)
     __shared__ RouteSmem rs;
     __shared__ int s_topk[kMaxRows * kMaxK];  // this CTA's selections, when it also routes
     __shared__ int s_last;
+    const int npf = p.pf_ctas;
+    if ((int)blockIdx.x >= (int)gridDim.x - npf) {
+        // L2 prefetch of records a later launch streams: they depend on no earlier launch, so
+        // these CTAs neither wait for the router nor hold anything up (line prefetches leave
+        // the SM at once; HBM is otherwise idle while the front end runs)
+        const int cta = blockIdx.x - (gridDim.x - npf);
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            if (!p.l2_pf[r]) continue;
+            const size_t share = (p.l2_pf_bytes[r] / (size_t)npf + 127) & ~(size_t)127;
+            const size_t b0 = (size_t)cta * share, b1 = b0 + share < p.l2_pf_bytes[r] ? b0 + share : p.l2_pf_bytes[r];
+            for (size_t o = b0 + 128 * (size_t)threadIdx.x; o < b1; o += 128 * (size_t)blockDim.x)
+                prefetch_line_l2(p.l2_pf[r] + o);
+        }
+        return;
+    }
     pdl_wait();
     pdl_trigger();  // the GEMM's CTAs may take the other SMs and wait there
     const int tk = p.topk_ctas;
     if ((int)blockIdx.x >= tk) {  // the CTAs after the top-k ones quantise x
-        quant_all(p, blockIdx.x - tk, gridDim.x - tk);
+        quant_all(p, blockIdx.x - tk, gridDim.x - tk - npf);
         return;
     }
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
