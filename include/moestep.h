@@ -259,8 +259,9 @@ moe_status moe_finalize_norm(const moe_layer_desc* d, const float* y_pairs, cons
                              void* outq, void* outq_scales, void* ws, moe_stream_t stream);
 
 /* a1..a7 in four launches chained with programmatic dependent launch: the router GEMV, the
- * top-k / routing / FC1 input quantisation, moe_expert_ffn (FC1 and FC2 in one launch), and
- * the finalize. The layer's front_launches = 1 runs the first two as one launch;
+ * top-k / routing / FC1 input quantisation (whose extra CTAs also prefetch the shared
+ * expert's weight records into L2), moe_expert_ffn (FC1 and FC2 in one launch), and the
+ * finalize. The layer's front_launches = 1 runs the first two as one launch;
  * ffn_launches = 2 runs FC1 and FC2 as two launches. Intermediates in ws (see moe_ws_view).
  * M in [1, 64]. Capture-safe. */
 moe_status moe_step(const moe_layer_desc* d, const moe_step_args* a, int M, void* ws, moe_stream_t stream);
