@@ -5,8 +5,8 @@
 //
 // A row is cut into kFinSlices contiguous slices; a slice is handled by kFinThreads threads
 // of one CTA, 4 consecutive elements (one float4 of each y row) each; k_finalize runs one
-// 8-CTA cluster per row and adds the slices' sums of squares over distributed shared memory
-// in slice order.
+// 8-CTA cluster per row: every CTA pushes its slice's sum of squares into all the cluster's
+// CTAs over distributed shared memory, and each adds them in slice order.
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -21,7 +21,8 @@ constexpr int kFinSlices = 8;
 
 struct FinSmem {
     float red[kFinThreads / 32];
-    float part;  // this slice's sum of squares (thread 0 writes it)
+    float part;               // this slice's sum of squares (thread 0 writes it)
+    float parts[kFinSlices];  // every slice's sum of squares, pushed here by the cluster's CTAs
     float w_s[kMaxK];
     int pos_s[kMaxK + 1];
 };

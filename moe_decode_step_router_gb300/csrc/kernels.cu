@@ -662,7 +662,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1) k_front(FrontParams f) {
 
 // ------------------------------------------------------------------------------------
 // a7 as its own launch: one cluster of kFinSlices CTAs per row (finalize.cuh), the slices'
-// sums of squares added over distributed shared memory in rank order (deterministic).
+// sums of squares exchanged over distributed shared memory and added in rank order
+// (deterministic).
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -671,12 +672,16 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-__device__ __forceinline__ float dsmem_ld(const float* local, uint32_t rank) {
+// The two halves of a cluster barrier, for an arrival long before the wait.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+// v into the copy of *local in the shared memory of the cluster's CTA `rank`.
+__device__ __forceinline__ void dsmem_st(float* local, uint32_t rank, float v) {
     uint32_t a = smem_u32(local), ra;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
-    return v;
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ra), "f"(v) : "memory");
 }
 
 __global__ void __launch_bounds__(kFinThreads) k_finalize(FinalizeParams p) {
@@ -687,9 +692,11 @@ __global__ void __launch_bounds__(kFinThreads) k_finalize(FinalizeParams p) {
         pdl_trigger();
         fin_pad_row(p, m, s);
         cluster_sync();
-        cluster_sync();
         return;
     }
+    // every CTA of the cluster has started once this barrier completes (waited on before
+    // the first store into another CTA's shared memory)
+    cluster_arrive_relaxed();
     // everything but the FC2 rows, before the wait for the FC2 launch
     const FinPre pre = fin_preload(p, m, s, fs);
     pdl_wait();
@@ -697,11 +704,16 @@ __global__ void __launch_bounds__(kFinThreads) k_finalize(FinalizeParams p) {
     __syncthreads();
     float hv[4];
     fin_combine(p, m, s, pre, hv, fs);
+    cluster_wait();
+    // this slice's sum of squares into slot s of every CTA of the cluster (thread 0 wrote
+    // fs.part); after the barrier each CTA holds all of them and no CTA touches another's
+    // shared memory again
+    if (threadIdx.x == 0)
+        for (int rk = 0; rk < kFinSlices; ++rk) dsmem_st(&fs.parts[s], (uint32_t)rk, fs.part);
     cluster_sync();
     float tot = 0.0f;
 #pragma unroll
-    for (int rk = 0; rk < kFinSlices; ++rk) tot += dsmem_ld(&fs.part, (uint32_t)rk);
-    cluster_sync();  // no CTA leaves while another still reads its partial
+    for (int rk = 0; rk < kFinSlices; ++rk) tot += fs.parts[rk];
     fin_output(p, m, s, pre, hv, tot);
 }
 
