@@ -344,7 +344,16 @@ __device__ __forceinline__ void block_scan4(int4 v, int4* out_excl, int4* total,
 
 // a2: the top-k of row m by one warp (the warp's lanes hold experts lane + 32 i); writes
 // topk_idx / topk_w of the row and, when s_topk is given, the ids into it too.
-__device__ __forceinline__ void topk_row(const TopkRouteParams& p, int m, int lane, int* s_topk) {
+// The lane's bias values (a layer constant, so a launch may load them before its dependency
+// wait): experts lane + 32 i, clamped.
+__device__ __forceinline__ void topk_bias(const TopkRouteParams& p, int lane, float bi[kMaxE / 32]) {
+#pragma unroll
+    for (int i = 0; i < kMaxE / 32; ++i) bi[i] = __ldg(p.bias + min(lane + 32 * i, p.E - 1));
+}
+
+// bias_pre: the lane's bias values when the caller has loaded them (topk_bias), else null.
+__device__ __forceinline__ void topk_row(const TopkRouteParams& p, int m, int lane, int* s_topk,
+                                         const float* bias_pre = nullptr) {
     const int E = p.E, k = p.k;
     // keys as order-preserving u32 (0 = taken / absent); lane owns e = lane + 32 i
     uint32_t ku[kMaxE / 32];
@@ -354,8 +363,12 @@ __device__ __forceinline__ void topk_row(const TopkRouteParams& p, int m, int la
 #pragma unroll
     for (int i = 0; i < kMaxE / 32; ++i) sc[i] = __ldcg(p.scores + (size_t)m * E + min(lane + 32 * i, E - 1));
     if (p.bias) {
+        if (bias_pre) {
 #pragma unroll
-        for (int i = 0; i < kMaxE / 32; ++i) bi[i] = __ldg(p.bias + min(lane + 32 * i, E - 1));
+            for (int i = 0; i < kMaxE / 32; ++i) bi[i] = bias_pre[i];
+        } else {
+            topk_bias(p, lane, bi);
+        }
     }
 #pragma unroll
     for (int i = 0; i < kMaxE / 32; ++i) {
@@ -552,6 +565,10 @@ __global__ void __launch_bounds__(kRouteThreads) k_topk_route(TopkRouteParams p)
         }
         return;
     }
+    // the top-k CTAs' bias values are a layer constant: loaded while the dependency wait runs
+    float bias_r[kMaxE / 32];
+    const bool pre_bias = p.bias && p.do_topk && (int)blockIdx.x < p.topk_ctas;
+    if (pre_bias) topk_bias(p, threadIdx.x % 32, bias_r);
     pdl_wait();
     pdl_trigger();  // the GEMM's CTAs may take the other SMs and wait there
     const int tk = p.topk_ctas;
@@ -586,7 +603,7 @@ __global__ void __launch_bounds__(kRouteThreads) k_topk_route(TopkRouteParams p)
     }
     if (p.do_topk) {
         for (int m = (int)blockIdx.x * (kRouteThreads / 32) + warp; m < M; m += tk * (kRouteThreads / 32))
-            topk_row(p, m, lane, s_topk);
+            topk_row(p, m, lane, s_topk, pre_bias ? bias_r : nullptr);
         __syncthreads();
     }
     if (!p.do_route) return;
