@@ -552,8 +552,9 @@ __global__ void __launch_bounds__(kRouteThreads) k_topk_route(TopkRouteParams p)
     const int npf = p.pf_ctas;
     if ((int)blockIdx.x >= (int)gridDim.x - npf) {
         // L2 prefetch of records a later launch streams: they depend on no earlier launch, so
-        // these CTAs neither wait for the router nor hold anything up (line prefetches leave
-        // the SM at once; HBM is otherwise idle while the front end runs)
+        // these CTAs do not wait for the router, and they are done (line prefetches leave the
+        // SM at once) long before the routing CTA, whose end the next launch waits for; HBM
+        // is otherwise idle while the front end runs
         const int cta = blockIdx.x - (gridDim.x - npf);
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
